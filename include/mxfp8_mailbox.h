@@ -1,0 +1,192 @@
+/*
+ * mxfp8_mailbox.h -- C ABI of the MXFP8 low-batch publishing GEMM and its
+ * Lamport mailbox (one GPU, sm_103a).
+ *
+ * The operation (page "vllm.models.deepseek_v41.nvidia.specialized_decode.
+ * boundary.publishing_gemm", module description "GEMM structure" and
+ * "Ordering"):
+ *
+ *   C[t][n] = sum_k W[n][k] * x[t][k]        t < m <= 8, n < N, k < K
+ *
+ * with W and x MXFP8 (E4M3FN elements, one E8M0FNU scale per 32-element K
+ * block), FP32 accumulation and a BF16 result.  The GEMM's epilogue publishes
+ * every output, rounded to BF16 with negative zero cleared, into generation
+ * stage_state[0] of a Lamport mailbox and sets stage_state[1] to that
+ * generation.  A consumer (page "vllm.models.deepseek_v41.nvidia.ops.cute_dsl.
+ * all_gather", module description steps 2 and 3), launched as the GEMM's
+ * programmatic dependent, polls the slots until no word is the sentinel,
+ * copies them out, stores the sentinel back and advances the generation.
+ *
+ * Conventions for every function below:
+ *  - Pointers named "device" are device (HBM) addresses owned by the caller;
+ *    the library never allocates, frees or retains them beyond what is stated.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Every launch is asynchronous on that stream; calls on one
+ *    mailbox must be issued in order on one stream and must not overlap.
+ *  - Argument errors are found on the host before any launch; the function
+ *    then returns MXFP8_ERR_INVALID or MXFP8_ERR_UNSUPPORTED, launches
+ *    nothing, and mxfp8_last_error() describes the problem.
+ *  - Every device-side wait is bounded: a wait that runs out sets a bit in
+ *    stage_state[3] (read with mxfp8_mailbox_status) instead of hanging.
+ *  - All functions are thread-compatible; mxfp8_last_error() is per thread.
+ */
+#ifndef MXFP8_MAILBOX_H
+#define MXFP8_MAILBOX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Three generations (all_gather page, module description step 3). */
+#define MXFP8_MAILBOX_GENERATIONS 3
+/* The Lamport sentinel word, FP32 negative zero / INT32_MIN (all_gather page,
+ * module description step 1). */
+#define MXFP8_MAILBOX_SENTINEL 0x80000000u
+/* At most eight activation rows (publishing_gemm page, PublishingMxfp8Linear.
+ * supports: 0 < num_tokens <= min(LOW_BATCH_MAX_ROWS, capacity)). */
+#define MXFP8_MAX_ROWS 8
+
+/* Bits of stage_state[3]. */
+#define MXFP8_FLAG_POLL_TIMEOUT 0x1 /* the consumer's poll ran out of time   */
+#define MXFP8_FLAG_GEMM_TIMEOUT 0x2 /* a GEMM pipeline wait ran out of time  */
+#define MXFP8_FLAG_BAD_STATE 0x4    /* a kernel read a generation not in 0..2 */
+
+typedef enum mxfp8_status {
+  MXFP8_OK = 0,
+  MXFP8_ERR_INVALID = 1,     /* bad argument: NULL, misaligned, bad shape        */
+  MXFP8_ERR_UNSUPPORTED = 2, /* well-formed but not taken (m, split_k, stages)   */
+  MXFP8_ERR_CUDA = 3,        /* a CUDA runtime call failed                       */
+  MXFP8_ERR_TIMEOUT = 4,     /* a device-side wait ran out (mxfp8_mailbox_status) */
+  MXFP8_ERR_STATE = 5        /* the state words hold a generation not in 0..2    */
+} mxfp8_status;
+
+/* Shape and tactic of one publishing GEMM (the tactic fields follow the
+ * publishing_gemm page's (cta_k, ab_stages, sfb_tmem_stages, split_k); the
+ * scale factors of x live in tensor memory for the whole K range, so there is
+ * no sfb stage count).  Zero in a tactic field asks the library to choose. */
+typedef struct mxfp8_gemm_desc {
+  int32_t n;          /* output columns N ("hidden"): a positive multiple of 128     */
+  int32_t k;          /* reduction length K: a positive multiple of 32, <= 32768     */
+  int32_t capacity_m; /* mailbox rows per generation: 1..8                           */
+  int32_t split_k;    /* cluster split-K S: 1, 2 or 4 (0 = choose)                   */
+  int32_t cta_k;      /* K elements per pipeline stage: 128 (0 = 128)                */
+  int32_t stages;     /* shared-memory ring depth: 2..16 (0 = choose)                */
+} mxfp8_gemm_desc;
+
+typedef struct mxfp8_publish_gemm mxfp8_publish_gemm; /* opaque */
+
+/* Bytes of a mailbox of `capacity_m` rows and `n` columns: 3 generations x
+ * capacity_m x n BF16 values, as 16-byte packs (all_gather page, module
+ * description: mailbox[generation][rank][pack], here with one rank).  The
+ * mailbox is laid out [generation][row][column] BF16, row-major.  Returns 0
+ * for an invalid shape (capacity_m not in 1..8, n not a positive multiple of
+ * 8). */
+size_t mxfp8_mailbox_bytes(int32_t capacity_m, int32_t n);
+
+/* Arm a mailbox (all_gather page, LamportAllGather.__init__: every slot
+ * starts as the sentinel, the state is zero).  mailbox: device, 16-byte
+ * aligned, mxfp8_mailbox_bytes(capacity_m, n) bytes.  stage_state: device,
+ * 16-byte aligned int32[4]: [0] next generation (written by the consumer,
+ * read by the GEMM), [1] active generation (written by the GEMM, read by the
+ * consumer), [2] the consumer's arrival count, [3] error flags.  Launches one
+ * kernel on `stream`. */
+mxfp8_status mxfp8_mailbox_init(void* mailbox, int32_t* stage_state, int32_t capacity_m,
+                                int32_t n, void* stream);
+
+/* Device bytes the handle needs for W's scale factors, re-laid once at
+ * create into the tiled order the tensor-core copy reads: N/128 x ceil(K/128)
+ * chunks of 512 bytes.  0 for an invalid descriptor. */
+size_t mxfp8_publish_gemm_workspace_bytes(const mxfp8_gemm_desc* desc);
+
+/* Build a publishing GEMM for one weight and one mailbox (publishing_gemm
+ * page, module description "Addresses": the mailbox, stage-state address,
+ * capacity and hidden size are fixed per publisher, whose buffers live as
+ * long as it does).
+ *  w:          device, 16-byte aligned, [N][K] E4M3FN bytes, K contiguous.
+ *  w_scale:    device, [N][K/32] E8M0FNU bytes, row-major.
+ *  mailbox:    device, 16-byte aligned, as for mxfp8_mailbox_init.
+ *  stage_state:device, 16-byte aligned int32[4].
+ *  workspace:  device, 256-byte aligned, >= mxfp8_publish_gemm_workspace_bytes.
+ * The handle borrows w, mailbox, stage_state and workspace until destroy
+ * (w_scale is read once, by a kernel launched here on `stream`, and not
+ * afterwards).  On success *out receives the handle. */
+mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* w,
+                                       const void* w_scale, void* mailbox,
+                                       int32_t* stage_state, void* workspace,
+                                       size_t workspace_bytes, void* stream,
+                                       mxfp8_publish_gemm** out);
+
+/* The resolved shape and tactic of a handle (split_k, cta_k, stages filled
+ * in), plus the dynamic shared memory, tensor-memory columns and grid size of
+ * its launch. */
+mxfp8_status mxfp8_publish_gemm_config(const mxfp8_publish_gemm* gemm, mxfp8_gemm_desc* desc,
+                                       int32_t* smem_bytes, int32_t* tmem_columns,
+                                       int32_t* grid_ctas);
+
+/* Everything a run with m rows needs, done ahead, launching nothing
+ * (publishing_gemm page, PublishingMxfp8Linear.precompile: a publish without
+ * its consumer would desynchronise the mailbox).  Call before CUDA-graph
+ * capture.  Returns MXFP8_ERR_UNSUPPORTED for m not in 1..min(8, capacity_m). */
+mxfp8_status mxfp8_publish_gemm_precompile(mxfp8_publish_gemm* gemm, int32_t m);
+
+/* One publishing GEMM (publishing_gemm page, PublishingMxfp8Linear.__call__
+ * and PublishingLowLatencyBlockscaledGemmKernel.epilog_warp):
+ *  x:       device, 16-byte aligned, [m][K] E4M3FN bytes.
+ *  x_scale: device, [m][K/32] E8M0FNU bytes, row-major.
+ *  m:       1..min(8, capacity_m), else MXFP8_ERR_UNSUPPORTED.
+ *  c:       device, 16-byte aligned, [m][N] BF16, or NULL to skip C.  C keeps
+ *           negative zero; the mailbox copy clears it.
+ * Publishes into generation g = stage_state[0] and sets stage_state[1] = g.
+ * Launched with programmatic stream serialisation: weight loads may start
+ * before the previous kernel on `stream` finishes; x, x_scale and the state
+ * are read only after it has.  Every run must be followed, on the same
+ * stream, by exactly one mailbox_consume before the next run. */
+mxfp8_status mxfp8_publish_gemm_run(mxfp8_publish_gemm* gemm, const void* x,
+                                    const void* x_scale, int32_t m, void* c, void* stream);
+
+/* The same GEMM without the publish (the unfused path of the publishing_gemm
+ * page's module description: the plain GEMM writes C, a separate publish
+ * kernel reads it back).  c is required. */
+mxfp8_status mxfp8_gemm_run_unfused(mxfp8_publish_gemm* gemm, const void* x,
+                                    const void* x_scale, int32_t m, void* c, void* stream);
+
+/* The standalone publish kernel of the unfused path: reads C [m][n] BF16
+ * (device, 16-byte aligned), writes it with negative zero cleared into
+ * generation stage_state[0], then sets stage_state[1].  Its result is bit-
+ * identical to the fused epilogue's. */
+mxfp8_status mailbox_publish(void* mailbox, int32_t* stage_state, int32_t capacity_m,
+                             int32_t n, int32_t m, const void* c, void* stream);
+
+/* The consumer (all_gather page, module description steps 2 and 3, one
+ * rank), launched as the previous kernel's programmatic dependent: reads
+ * g = stage_state[1]; polls mailbox[g][t][*] for t < m until no 32-bit word
+ * is the sentinel; writes out[t][*] (device, 16-byte aligned, [m][n] BF16);
+ * stores the sentinel back; the last CTA to arrive sets stage_state[0] =
+ * (g + 1) mod 3 and clears stage_state[2].  A poll still unsatisfied after
+ * timeout_ns nanoseconds (0 = one second) gives up: it sets
+ * MXFP8_FLAG_POLL_TIMEOUT, still copies and resets its slot, and the
+ * generation still advances, so the stream drains. */
+mxfp8_status mailbox_consume(void* mailbox, int32_t* stage_state, int32_t capacity_m,
+                             int32_t n, int32_t m, void* out, uint64_t timeout_ns,
+                             void* stream);
+
+/* Synchronises `stream`, copies stage_state (device int32[4]) into words
+ * (host int32[4]) and reports: MXFP8_ERR_TIMEOUT if a timeout flag is set,
+ * MXFP8_ERR_STATE if the bad-state flag is set or a generation word is not in
+ * 0..2, else MXFP8_OK. */
+mxfp8_status mxfp8_mailbox_status(const int32_t* stage_state, int32_t* words, void* stream);
+
+/* Releases the handle (host memory only; the caller's buffers stay). */
+void mxfp8_publish_gemm_destroy(mxfp8_publish_gemm* gemm);
+
+/* Text of the calling thread's last error ("" if none). */
+const char* mxfp8_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP8_MAILBOX_H */

@@ -1,0 +1,142 @@
+"""Thin Python binding over the C ABI: argument marshalling only.
+
+PyTorch provides device memory and streams; every step of the path runs in the
+library's CUDA kernels.  Names follow the C ABI (``include/mxfp8_mailbox.h``).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import GemmDesc, check
+
+
+def _ptr(t: torch.Tensor | None):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(None)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return ctypes.c_void_p(handle)
+
+
+def _bytes_tensor(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.element_size() != 1:
+        raise TypeError(f"{name} must hold one-byte codes (uint8 / float8), got {t.dtype}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return t
+
+
+class Mailbox:
+    """A 3-generation Lamport mailbox ``[3][capacity_m][n]`` BF16 and its four
+    state words ``[next generation, active generation, arrivals, flags]``."""
+
+    def __init__(self, capacity_m: int, n: int, device=None, stream=None):
+        lib = _lib.load()
+        nbytes = lib.mxfp8_mailbox_bytes(capacity_m, n)
+        if nbytes == 0:
+            raise ValueError(f"invalid mailbox shape capacity_m={capacity_m}, n={n}")
+        device = torch.device(device or "cuda")
+        self.capacity = capacity_m
+        self.n = n
+        self.words = torch.empty(nbytes // 4, dtype=torch.int32, device=device)
+        self.state = torch.zeros(4, dtype=torch.int32, device=device)
+        self.init(stream)
+
+    def init(self, stream=None) -> None:
+        check(_lib.load().mxfp8_mailbox_init(_ptr(self.words), _ptr(self.state), self.capacity,
+                                             self.n, _stream(stream)), "mxfp8_mailbox_init")
+
+    def publish(self, c: torch.Tensor, stream=None) -> None:
+        """The unfused path's standalone publish of C [m][n] BF16."""
+        check(_lib.load().mailbox_publish(_ptr(self.words), _ptr(self.state), self.capacity,
+                                          self.n, c.shape[0], _ptr(c), _stream(stream)),
+              "mailbox_publish")
+
+    def consume(self, m: int, out: torch.Tensor | None = None, timeout_ns: int = 0,
+                stream=None) -> torch.Tensor:
+        """The consumer: [m][n] BF16 copied out of the active generation."""
+        if out is None:
+            out = torch.empty((m, self.n), dtype=torch.bfloat16, device=self.words.device)
+        check(_lib.load().mailbox_consume(_ptr(self.words), _ptr(self.state), self.capacity,
+                                          self.n, m, _ptr(out), timeout_ns, _stream(stream)),
+              "mailbox_consume")
+        return out
+
+    def status(self, stream=None):
+        """(status code, [4] state words); synchronises the stream."""
+        words = (ctypes.c_int32 * 4)()
+        st = _lib.load().mxfp8_mailbox_status(_ptr(self.state), words, _stream(stream))
+        return st, list(words)
+
+
+class PublishGemm:
+    """One MXFP8 weight ``W [N][K]`` (E4M3 codes) with its scales ``[N][K/32]``
+    (E8M0 codes), publishing into ``mailbox``.  The weight, mailbox and the
+    workspace this object allocates stay borrowed by the native handle until
+    :meth:`close`."""
+
+    def __init__(self, w: torch.Tensor, w_scale: torch.Tensor, mailbox: Mailbox,
+                 split_k: int = 0, stages: int = 0, stream=None):
+        lib = _lib.load()
+        _bytes_tensor(w, "w")
+        _bytes_tensor(w_scale, "w_scale")
+        n, k = w.shape
+        self.desc = GemmDesc(n, k, mailbox.capacity, split_k, 0, stages)
+        ws_bytes = lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(self.desc))
+        if ws_bytes == 0:
+            raise ValueError(f"invalid GEMM shape N={n}, K={k}")
+        self.workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=w.device)
+        self.w = w
+        self.mailbox = mailbox
+        self.n, self.k = n, k
+        handle = ctypes.c_void_p()
+        check(lib.mxfp8_publish_gemm_create(ctypes.byref(self.desc), _ptr(w), _ptr(w_scale),
+                                            _ptr(mailbox.words), _ptr(mailbox.state),
+                                            _ptr(self.workspace), ws_bytes, _stream(stream),
+                                            ctypes.byref(handle)), "mxfp8_publish_gemm_create")
+        self._handle = handle
+
+    def config(self) -> dict:
+        d = GemmDesc()
+        smem, tmem, grid = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        check(_lib.load().mxfp8_publish_gemm_config(self._handle, ctypes.byref(d),
+                                                    ctypes.byref(smem), ctypes.byref(tmem),
+                                                    ctypes.byref(grid)), "mxfp8_publish_gemm_config")
+        return {"n": d.n, "k": d.k, "capacity_m": d.capacity_m, "split_k": d.split_k,
+                "cta_k": d.cta_k, "stages": d.stages, "smem_bytes": smem.value,
+                "tmem_columns": tmem.value, "grid_ctas": grid.value}
+
+    def precompile(self, m: int) -> None:
+        check(_lib.load().mxfp8_publish_gemm_precompile(self._handle, m),
+              "mxfp8_publish_gemm_precompile")
+
+    def run(self, x: torch.Tensor, x_scale: torch.Tensor, c: torch.Tensor | None = None,
+            stream=None) -> torch.Tensor | None:
+        """One publishing GEMM on x [m][K]; writes C [m][N] BF16 into ``c`` if
+        given.  Must be followed by exactly one ``mailbox.consume``."""
+        check(_lib.load().mxfp8_publish_gemm_run(self._handle, _ptr(x), _ptr(x_scale), x.shape[0],
+                                                 _ptr(c), _stream(stream)), "mxfp8_publish_gemm_run")
+        return c
+
+    def run_unfused(self, x: torch.Tensor, x_scale: torch.Tensor, c: torch.Tensor,
+                    stream=None) -> torch.Tensor:
+        check(_lib.load().mxfp8_gemm_run_unfused(self._handle, _ptr(x), _ptr(x_scale), x.shape[0],
+                                                 _ptr(c), _stream(stream)), "mxfp8_gemm_run_unfused")
+        return c
+
+    def close(self) -> None:
+        if getattr(self, "_handle", None):
+            _lib.load().mxfp8_publish_gemm_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,396 @@
+// The C ABI declared in include/mxfp8_mailbox.h: argument checks, the
+// publishing-GEMM handle (tensor maps, tactic, launch configuration) and the
+// mailbox calls.  Every check happens on the host before a launch; a failed
+// check returns a status and leaves a message for mxfp8_last_error().
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "internal.h"
+#include "mxfp8_mailbox.h"
+
+using namespace mxfp8;
+
+struct mxfp8_publish_gemm {
+  mxfp8_gemm_desc desc;  // resolved tactic
+  const uint8_t* w;
+  uint8_t* w_sf;
+  uint16_t* mailbox;
+  int32_t* state;
+  int device;
+  int k_tiles;
+  int tiles_per_split;
+  uint32_t tmem_cols, sfb_col, sfa_col;
+  GemmSmemLayout layout;
+  CUtensorMap tmap_w;
+  // Tensor map of the last activation buffer seen (x pointer, m).
+  const void* x_cached;
+  int m_cached;
+  CUtensorMap tmap_x;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+mxfp8_status fail(mxfp8_status status, const std::string& message) {
+  g_last_error = message;
+  return status;
+}
+
+mxfp8_status cuda_fail(cudaError_t err, const char* what) {
+  return fail(MXFP8_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(err));
+}
+
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+constexpr uint64_t kDefaultPollTimeoutNs = 1000000000ull;
+constexpr uint64_t kGemmWaitLimitNs = 2000000000ull;
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_tiled() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+// A 2-D uint8 tensor [outer][inner] (row stride `inner` bytes), read in boxes
+// of box_outer rows x 128 bytes with the 128-byte swizzle; out-of-range
+// elements read as zero.
+mxfp8_status encode_rows(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                         uint32_t box_outer) {
+  EncodeTiled fn = encode_tiled();
+  if (!fn) return fail(MXFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), box_outer};
+  cuuint32_t elem[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MXFP8_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
+  return MXFP8_OK;
+}
+
+mxfp8_status check_desc(const mxfp8_gemm_desc* d) {
+  if (!d) return fail(MXFP8_ERR_INVALID, "desc is NULL");
+  if (d->n <= 0 || d->n % kBlockN)
+    return fail(MXFP8_ERR_INVALID, "n must be a positive multiple of 128, got " + std::to_string(d->n));
+  if (d->k <= 0 || d->k % 32)
+    return fail(MXFP8_ERR_INVALID, "k must be a positive multiple of 32, got " + std::to_string(d->k));
+  if (d->k > 32768) return fail(MXFP8_ERR_UNSUPPORTED, "k above 32768 is not supported");
+  if (d->capacity_m < 1 || d->capacity_m > MXFP8_MAX_ROWS)
+    return fail(MXFP8_ERR_INVALID, "capacity_m must be in 1..8");
+  if (d->split_k != 0 && d->split_k != 1 && d->split_k != 2 && d->split_k != 4)
+    return fail(MXFP8_ERR_UNSUPPORTED, "split_k must be 1, 2 or 4 (or 0 to choose)");
+  if (d->cta_k != 0 && d->cta_k != kTileK) return fail(MXFP8_ERR_UNSUPPORTED, "cta_k must be 128");
+  if (d->stages != 0 && (d->stages < 2 || d->stages > kMaxStages))
+    return fail(MXFP8_ERR_UNSUPPORTED, "stages must be in 2..16 (or 0 to choose)");
+  return MXFP8_OK;
+}
+
+int k_tiles_of(int k) { return (k + kTileK - 1) / kTileK; }
+
+struct DeviceLimits {
+  int sms = 0;
+  int smem_optin = 0;
+  int smem_per_sm = 0;
+};
+
+mxfp8_status device_limits(int device, DeviceLimits* out) {
+  cudaError_t e;
+  if ((e = cudaDeviceGetAttribute(&out->sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+  if ((e = cudaDeviceGetAttribute(&out->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                  device)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute(shared memory per block)");
+  if ((e = cudaDeviceGetAttribute(&out->smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                  device)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute(shared memory per SM)");
+  return MXFP8_OK;
+}
+
+// Fill split_k, cta_k and stages: split_k so the grid has about one or two
+// CTAs per SM; the deepest ring that still lets the intended number of CTAs
+// share an SM.
+mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
+  const int tiles = d->n / kBlockN;
+  const int k_tiles = k_tiles_of(d->k);
+  if (d->split_k == 0) {
+    int s = 1;
+    for (int cand : {2, 4})
+      if (tiles * cand <= 2 * lim.sms && k_tiles >= 2 * cand) s = cand;
+    d->split_k = s;
+  }
+  d->cta_k = kTileK;
+  const int tps = (k_tiles + d->split_k - 1) / d->split_k;
+  if (tps > kMaxTilesPerSplit)
+    return fail(MXFP8_ERR_UNSUPPORTED, "too many K tiles per split: raise split_k");
+  const int ctas = tiles * d->split_k;
+  const int per_sm = ctas > lim.sms ? 2 : 1;
+  const int budget = per_sm == 2 ? lim.smem_per_sm / 2 - 1024 : lim.smem_optin;
+  if (d->stages == 0) {
+    int best = 0;
+    for (int s = 2; s <= kMaxStages; ++s) {
+      if (static_cast<int>(gemm_smem_layout(s, d->split_k, tps).total) > budget) break;
+      if (gemm_tmem_columns(s, tps, nullptr, nullptr) > static_cast<uint32_t>(512 / per_sm)) break;
+      best = s;
+      if (s >= tps) break;  // more stages than K tiles buy nothing
+    }
+    if (best == 0) return fail(MXFP8_ERR_UNSUPPORTED, "no stage count fits in shared memory");
+    d->stages = best;
+  }
+  if (static_cast<int>(gemm_smem_layout(d->stages, d->split_k, tps).total) > lim.smem_optin)
+    return fail(MXFP8_ERR_UNSUPPORTED, "the requested stages do not fit in shared memory");
+  if (gemm_tmem_columns(d->stages, tps, nullptr, nullptr) > 512)
+    return fail(MXFP8_ERR_UNSUPPORTED, "the requested stages do not fit in tensor memory");
+  return MXFP8_OK;
+}
+
+mxfp8_status check_rows(const mxfp8_publish_gemm* g, int32_t m) {
+  const int limit = std::min(MXFP8_MAX_ROWS, static_cast<int>(g->desc.capacity_m));
+  if (m < 1 || m > limit)
+    return fail(MXFP8_ERR_UNSUPPORTED,
+                "m must be in 1.." + std::to_string(limit) + ", got " + std::to_string(m));
+  return MXFP8_OK;
+}
+
+mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale, int32_t m,
+                      void* c, void* stream, bool publish) {
+  if (!g) return fail(MXFP8_ERR_INVALID, "gemm handle is NULL");
+  mxfp8_status st = check_rows(g, m);
+  if (st != MXFP8_OK) return st;
+  if (!x || !aligned(x, 16)) return fail(MXFP8_ERR_INVALID, "x must be a 16-byte aligned device pointer");
+  if (!x_scale) return fail(MXFP8_ERR_INVALID, "x_scale is NULL");
+  if (c && !aligned(c, 16)) return fail(MXFP8_ERR_INVALID, "c must be 16-byte aligned");
+  if (!publish && !c) return fail(MXFP8_ERR_INVALID, "the unfused GEMM needs c");
+  if (g->x_cached != x || g->m_cached != m) {
+    st = encode_rows(&g->tmap_x, x, static_cast<uint64_t>(g->desc.k), static_cast<uint64_t>(m), kRows);
+    if (st != MXFP8_OK) return st;
+    g->x_cached = x;
+    g->m_cached = m;
+  }
+  GemmParams p{};
+  p.n = g->desc.n;
+  p.k = g->desc.k;
+  p.m = m;
+  p.k_tiles = g->k_tiles;
+  p.tiles_per_split = g->tiles_per_split;
+  p.stages = g->desc.stages;
+  p.capacity = g->desc.capacity_m;
+  p.publish = publish ? 1 : 0;
+  p.tmem_cols = g->tmem_cols;
+  p.sfb_col = g->sfb_col;
+  p.sfa_col = g->sfa_col;
+  p.x_scale = static_cast<const uint8_t*>(x_scale);
+  p.w_sf = g->w_sf;
+  p.c = static_cast<uint16_t*>(c);
+  p.mailbox = g->mailbox;
+  p.state = g->state;
+  p.wait_limit_ns = kGemmWaitLimitNs;
+  p.smem = g->layout;
+  cudaError_t e = launch_publish_gemm(g->tmap_w, g->tmap_x, p, g->desc.split_k,
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the publishing GEMM");
+  return MXFP8_OK;
+}
+
+mxfp8_status check_mailbox(const void* mailbox, const int32_t* state, int32_t capacity_m,
+                           int32_t n) {
+  if (!mailbox || !aligned(mailbox, 16))
+    return fail(MXFP8_ERR_INVALID, "mailbox must be a 16-byte aligned device pointer");
+  if (!state || !aligned(state, 16))
+    return fail(MXFP8_ERR_INVALID, "stage_state must be a 16-byte aligned device int32[4]");
+  if (capacity_m < 1 || capacity_m > MXFP8_MAX_ROWS)
+    return fail(MXFP8_ERR_INVALID, "capacity_m must be in 1..8");
+  if (n <= 0 || n % 8) return fail(MXFP8_ERR_INVALID, "n must be a positive multiple of 8");
+  return MXFP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mxfp8_mailbox_bytes(int32_t capacity_m, int32_t n) {
+  if (capacity_m < 1 || capacity_m > MXFP8_MAX_ROWS || n <= 0 || n % 8) return 0;
+  return static_cast<size_t>(MXFP8_MAILBOX_GENERATIONS) * capacity_m * n * 2;
+}
+
+mxfp8_status mxfp8_mailbox_init(void* mailbox, int32_t* stage_state, int32_t capacity_m,
+                                int32_t n, void* stream) {
+  mxfp8_status st = check_mailbox(mailbox, stage_state, capacity_m, n);
+  if (st != MXFP8_OK) return st;
+  cudaError_t e = launch_mailbox_init(static_cast<uint16_t*>(mailbox), stage_state, capacity_m, n,
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the mailbox init kernel");
+  return MXFP8_OK;
+}
+
+size_t mxfp8_publish_gemm_workspace_bytes(const mxfp8_gemm_desc* desc) {
+  if (!desc || desc->n <= 0 || desc->n % kBlockN || desc->k <= 0 || desc->k % 32) return 0;
+  return static_cast<size_t>(desc->n / kBlockN) * k_tiles_of(desc->k) * kSfChunkBytes;
+}
+
+mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* w,
+                                       const void* w_scale, void* mailbox,
+                                       int32_t* stage_state, void* workspace,
+                                       size_t workspace_bytes, void* stream,
+                                       mxfp8_publish_gemm** out) {
+  if (!out) return fail(MXFP8_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  mxfp8_status st = check_desc(desc);
+  if (st != MXFP8_OK) return st;
+  if (!w || !aligned(w, 16)) return fail(MXFP8_ERR_INVALID, "w must be a 16-byte aligned device pointer");
+  if (!w_scale) return fail(MXFP8_ERR_INVALID, "w_scale is NULL");
+  st = check_mailbox(mailbox, stage_state, desc->capacity_m, desc->n);
+  if (st != MXFP8_OK) return st;
+  const size_t need = mxfp8_publish_gemm_workspace_bytes(desc);
+  if (!workspace || !aligned(workspace, 16))
+    return fail(MXFP8_ERR_INVALID, "workspace must be a 16-byte aligned device pointer");
+  if (workspace_bytes < need)
+    return fail(MXFP8_ERR_INVALID, "workspace too small: need " + std::to_string(need) + " bytes");
+
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceLimits lim;
+  st = device_limits(device, &lim);
+  if (st != MXFP8_OK) return st;
+
+  mxfp8_publish_gemm* g = new (std::nothrow) mxfp8_publish_gemm();
+  if (!g) return fail(MXFP8_ERR_INVALID, "out of host memory");
+  g->desc = *desc;
+  st = resolve_tactic(&g->desc, lim);
+  if (st != MXFP8_OK) {
+    delete g;
+    return st;
+  }
+  g->w = static_cast<const uint8_t*>(w);
+  g->w_sf = static_cast<uint8_t*>(workspace);
+  g->mailbox = static_cast<uint16_t*>(mailbox);
+  g->state = stage_state;
+  g->device = device;
+  g->k_tiles = k_tiles_of(desc->k);
+  g->tiles_per_split = (g->k_tiles + g->desc.split_k - 1) / g->desc.split_k;
+  g->tmem_cols = gemm_tmem_columns(g->desc.stages, g->tiles_per_split, &g->sfb_col, &g->sfa_col);
+  g->layout = gemm_smem_layout(g->desc.stages, g->desc.split_k, g->tiles_per_split);
+  g->x_cached = nullptr;
+  g->m_cached = 0;
+  st = encode_rows(&g->tmap_w, w, static_cast<uint64_t>(desc->k), static_cast<uint64_t>(desc->n),
+                   kBlockN);
+  if (st != MXFP8_OK) {
+    delete g;
+    return st;
+  }
+  e = set_gemm_smem_attribute(g->desc.split_k, static_cast<int>(g->layout.total));
+  if (e != cudaSuccess) {
+    delete g;
+    return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+  }
+  e = launch_relayout_w_scales(static_cast<const uint8_t*>(w_scale), g->w_sf, desc->n, desc->k,
+                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    delete g;
+    return cuda_fail(e, "launching the W scale re-layout");
+  }
+  *out = g;
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_publish_gemm_config(const mxfp8_publish_gemm* gemm, mxfp8_gemm_desc* desc,
+                                       int32_t* smem_bytes, int32_t* tmem_columns,
+                                       int32_t* grid_ctas) {
+  if (!gemm) return fail(MXFP8_ERR_INVALID, "gemm handle is NULL");
+  if (desc) *desc = gemm->desc;
+  if (smem_bytes) *smem_bytes = static_cast<int32_t>(gemm->layout.total);
+  if (tmem_columns) *tmem_columns = static_cast<int32_t>(gemm->tmem_cols);
+  if (grid_ctas) *grid_ctas = (gemm->desc.n / kBlockN) * gemm->desc.split_k;
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_publish_gemm_precompile(mxfp8_publish_gemm* gemm, int32_t m) {
+  if (!gemm) return fail(MXFP8_ERR_INVALID, "gemm handle is NULL");
+  mxfp8_status st = check_rows(gemm, m);
+  if (st != MXFP8_OK) return st;
+  if (!encode_tiled()) return fail(MXFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cudaError_t e = set_gemm_smem_attribute(gemm->desc.split_k, static_cast<int>(gemm->layout.total));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_publish_gemm_run(mxfp8_publish_gemm* gemm, const void* x, const void* x_scale,
+                                    int32_t m, void* c, void* stream) {
+  return run_gemm(gemm, x, x_scale, m, c, stream, true);
+}
+
+mxfp8_status mxfp8_gemm_run_unfused(mxfp8_publish_gemm* gemm, const void* x, const void* x_scale,
+                                    int32_t m, void* c, void* stream) {
+  return run_gemm(gemm, x, x_scale, m, c, stream, false);
+}
+
+mxfp8_status mailbox_publish(void* mailbox, int32_t* stage_state, int32_t capacity_m, int32_t n,
+                             int32_t m, const void* c, void* stream) {
+  mxfp8_status st = check_mailbox(mailbox, stage_state, capacity_m, n);
+  if (st != MXFP8_OK) return st;
+  if (m < 1 || m > capacity_m) return fail(MXFP8_ERR_UNSUPPORTED, "m must be in 1..capacity_m");
+  if (!c || !aligned(c, 16)) return fail(MXFP8_ERR_INVALID, "c must be a 16-byte aligned device pointer");
+  cudaError_t e = launch_mailbox_publish(static_cast<uint16_t*>(mailbox), stage_state, capacity_m,
+                                         n, m, static_cast<const uint16_t*>(c),
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the publish kernel");
+  return MXFP8_OK;
+}
+
+mxfp8_status mailbox_consume(void* mailbox, int32_t* stage_state, int32_t capacity_m, int32_t n,
+                             int32_t m, void* out, uint64_t timeout_ns, void* stream) {
+  mxfp8_status st = check_mailbox(mailbox, stage_state, capacity_m, n);
+  if (st != MXFP8_OK) return st;
+  if (m < 1 || m > capacity_m) return fail(MXFP8_ERR_UNSUPPORTED, "m must be in 1..capacity_m");
+  if (!out || !aligned(out, 16)) return fail(MXFP8_ERR_INVALID, "out must be a 16-byte aligned device pointer");
+  cudaError_t e = launch_mailbox_consume(static_cast<uint16_t*>(mailbox), stage_state, capacity_m,
+                                         n, m, static_cast<uint16_t*>(out),
+                                         timeout_ns ? timeout_ns : kDefaultPollTimeoutNs,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the consumer");
+  return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_mailbox_status(const int32_t* stage_state, int32_t* words, void* stream) {
+  if (!stage_state || !words) return fail(MXFP8_ERR_INVALID, "stage_state and words are required");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(words, stage_state, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the state words");
+  if (words[3] & (MXFP8_FLAG_POLL_TIMEOUT | MXFP8_FLAG_GEMM_TIMEOUT))
+    return fail(MXFP8_ERR_TIMEOUT, "a device-side wait ran out of time (flags " +
+                                       std::to_string(words[3]) + ")");
+  if ((words[3] & MXFP8_FLAG_BAD_STATE) || words[0] < 0 || words[0] >= MXFP8_MAILBOX_GENERATIONS ||
+      words[1] < 0 || words[1] >= MXFP8_MAILBOX_GENERATIONS)
+    return fail(MXFP8_ERR_STATE, "the state words hold a generation outside 0..2");
+  return MXFP8_OK;
+}
+
+void mxfp8_publish_gemm_destroy(mxfp8_publish_gemm* gemm) { delete gemm; }
+
+const char* mxfp8_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

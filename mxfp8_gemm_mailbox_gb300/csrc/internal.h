@@ -1,0 +1,72 @@
+// Declarations shared by the kernels and the C-ABI layer of the library.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace mxfp8 {
+
+constexpr int kBlockN = 128;      // output columns per CTA: the MMA's M
+constexpr int kRows = 8;          // activation rows per tile: the MMA's N
+constexpr int kTileK = 128;       // K elements per stage: one 128-byte swizzle row
+constexpr int kSfPerTile = 4;     // scale blocks of 32 per stage
+constexpr int kThreads = 192;     // warp 0 loads, warp 1 issues MMAs, warps 2-5 epilogue
+constexpr int kSfChunkBytes = 512;
+constexpr int kWTileBytes = kBlockN * kTileK;  // 16384
+constexpr int kXTileBytes = kRows * kTileK;    // 1024
+constexpr int kGenerations = 3;
+constexpr uint32_t kSentinel = 0x80000000u;
+constexpr int kMaxStages = 16;
+constexpr int kMaxTilesPerSplit = 256;
+
+// Byte offsets inside the GEMM's dynamic shared memory (after aligning the
+// base to 1024 bytes), computed once on the host.
+struct GemmSmemLayout {
+  uint32_t w;         // stages x 16 KB W tiles
+  uint32_t x;         // stages x 1 KB activation tiles
+  uint32_t sfa;       // stages x 512 B W scale chunks
+  uint32_t ctile;     // 8 x 128 BF16 epilogue staging
+  uint32_t recv;      // split-K partials received from peers
+  uint32_t sx;        // x scale words of this CTA's K range
+  uint32_t bars;      // mbarriers
+  uint32_t misc;      // tensor-memory base, generation broadcast
+  uint32_t total;     // bytes including the alignment slack
+};
+
+struct GemmParams {
+  int32_t n, k, m;
+  int32_t k_tiles;          // ceil(k / 128)
+  int32_t tiles_per_split;  // ceil(k_tiles / split_k)
+  int32_t stages;
+  int32_t capacity;
+  int32_t publish;          // 1: fused publish into the mailbox; 0: C only
+  uint32_t tmem_cols;
+  uint32_t sfb_col;         // first tensor-memory column of the x scales
+  uint32_t sfa_col;         // first tensor-memory column of the W scale ring
+  const uint8_t* x_scale;   // [m][k/32]
+  const uint8_t* w_sf;      // [n/128][k_tiles][512] tiled W scales
+  uint16_t* c;              // [m][n] BF16 or nullptr
+  uint16_t* mailbox;        // [3][capacity][n] BF16
+  int32_t* state;           // int32[4]
+  uint64_t wait_limit_ns;
+  GemmSmemLayout smem;
+};
+
+GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split);
+uint32_t gemm_tmem_columns(int stages, int tiles_per_split, uint32_t* sfb_col, uint32_t* sfa_col);
+
+// Kernel launchers (return the CUDA error of the launch).
+cudaError_t launch_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
+                                const GemmParams& p, int split_k, cudaStream_t stream);
+cudaError_t set_gemm_smem_attribute(int split_k, int bytes);
+cudaError_t launch_relayout_w_scales(const uint8_t* w_scale, uint8_t* w_sf, int n, int k,
+                                     cudaStream_t stream);
+cudaError_t launch_mailbox_init(uint16_t* mailbox, int32_t* state, int capacity, int n,
+                                cudaStream_t stream);
+cudaError_t launch_mailbox_consume(uint16_t* mailbox, int32_t* state, int capacity, int n, int m,
+                                   uint16_t* out, uint64_t timeout_ns, cudaStream_t stream);
+cudaError_t launch_mailbox_publish(uint16_t* mailbox, int32_t* state, int capacity, int n, int m,
+                                   const uint16_t* c, cudaStream_t stream);
+
+}  // namespace mxfp8
