@@ -21,10 +21,10 @@
 //               8 tokens), split-K exchange, BF16 rounding, C store, publish.
 //
 // Tensor-memory columns: [0, 8) FP32 accumulator (lane = output column,
-// column = token); [sfb_col, +tiles) x scales, one 32-bit column per 128-K
-// tile holding its four E8M0 bytes in lanes 0..7 of every 32-lane quarter;
-// [sfa_col, +4*stages) the W scale ring, one 4-column slot per stage filled by
-// tcgen05.cp from the 128 x 4 scale chunk in shared memory.
+// column = token); [sfa_col, +4*stages) the W scale ring and [sfb_col,
+// +4*stages) the x scale ring, one 4-column slot per stage each, filled by
+// tcgen05.cp (32x128b, multicast to the four lane quarters) from 16-byte-row
+// scale chunks in shared memory.  Every scale address is 4-column aligned.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -200,8 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t sfa_t = tmem + p.sfa_col + 4u * s;
-        const uint32_t sfb_t = tmem + p.sfb_col + static_cast<uint32_t>(i);
+        const uint32_t sfb_t = tmem + p.sfb_col + 4u * s;
         ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::desc_rows16(sbase + L.sfa + s * kSfChunkBytes));
+        ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::desc_rows16(sbase + L.sx + i * 128));
         const uint32_t a0 = sbase + L.w + s * kWTileBytes;
         const uint32_t b0 = sbase + L.x + s * kXTileBytes;
 #pragma unroll
@@ -226,33 +227,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::grid_dependency_wait();
     if (etid == 0) misc[1] = ptx::ld_volatile_u32(p.state + 0);
 
-    // x scales of this CTA's K range: bytes sx[r][4 * j + b] for tile j,
-    // block b; rows >= m and blocks past K take 127 (a scale of 1; those x
-    // elements are zero).
+    // x scales of this CTA's K range as one 128-byte chunk per K tile: row r
+    // (< 8) of tile j at byte j * 128 + r * 16, its four E8M0 codes first.
+    // Rows >= m and blocks past K take 127 (a scale of 1; those x elements
+    // are zero).  The copy of a chunk reads 32 rows; rows 8..31 (the next
+    // chunks, or the zero tail) feed no output column.
     uint8_t* sx = smem + L.sx;
     const int kblocks = p.k / 32;
-    const int row_bytes = p.tiles_per_split * 4;
-    for (int b = etid; b < kRows * row_bytes; b += 128) {
-      const int r = b / row_bytes;
-      const int kb = kt_begin * 4 + (b % row_bytes);
-      uint8_t v = 127;
-      if (r < p.m && kb < kblocks) v = p.x_scale[static_cast<size_t>(r) * kblocks + kb];
+    const int sx_bytes = p.tiles_per_split * 128 + 384;
+    for (int b = etid; b < sx_bytes; b += 128) {
+      const int j = b / 128;
+      const int r = (b % 128) / 16;
+      const int q = b % 16;
+      uint8_t v = 0;
+      if (q < kSfPerTile && j < nkt) {
+        const int kb = (kt_begin + j) * kSfPerTile + q;
+        v = 127;
+        if (r < p.m && kb < kblocks) v = p.x_scale[static_cast<size_t>(r) * kblocks + kb];
+      }
       sx[b] = v;
     }
-    epilogue_barrier();
-    for (int j0 = 0; j0 < nkt; j0 += 8) {
-      uint32_t v[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int j = j0 + q;
-        v[q] = (lane < kRows && j < nkt)
-                   ? *reinterpret_cast<const uint32_t*>(sx + lane * row_bytes + 4 * j)
-                   : 0x7F7F7F7Fu;
-      }
-      ptx::tmem_st_32x32b_x8(tmem + lane_base + p.sfb_col + static_cast<uint32_t>(j0), v);
-    }
-    ptx::tmem_wait_st();
-    ptx::tc_fence_before();
+    ptx::fence_proxy_async_smem();  // the tensor-memory copy reads them
     ptx::mbar_arrive(bar_sfb);
 
     if (!ptx::mbar_wait(bar_acc, 0, p.wait_limit_ns)) raise_flag(p.state, 0x2u);
@@ -415,7 +410,7 @@ GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split) {
   const uint32_t recv_bytes =
       split_k > 1 ? static_cast<uint32_t>((split_k - 1) * (kRows / split_k) * kBlockN * 4) : 0u;
   L.sx = L.recv + recv_bytes;
-  const uint32_t sx_bytes = (static_cast<uint32_t>(kRows * tiles_per_split * 4) + 15u) & ~15u;
+  const uint32_t sx_bytes = static_cast<uint32_t>(tiles_per_split * 128 + 384);
   L.bars = (L.sx + sx_bytes + 7u) & ~7u;
   L.misc = L.bars + static_cast<uint32_t>(2 * stages + 3) * 8u;
   L.total = L.misc + 16u + 1024u;
@@ -423,10 +418,10 @@ GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split) {
 }
 
 uint32_t gemm_tmem_columns(int stages, int tiles_per_split, uint32_t* sfb_col, uint32_t* sfa_col) {
-  const uint32_t sfb = 8u;
-  const uint32_t sfb_cols = (static_cast<uint32_t>(tiles_per_split) + 7u) & ~7u;
-  const uint32_t sfa = sfb + sfb_cols;
-  const uint32_t used = sfa + 4u * static_cast<uint32_t>(stages);
+  (void)tiles_per_split;
+  const uint32_t sfa = 8u;
+  const uint32_t sfb = sfa + 4u * static_cast<uint32_t>(stages);
+  const uint32_t used = sfb + 4u * static_cast<uint32_t>(stages);
   uint32_t cols = 32;
   while (cols < used) cols <<= 1;
   if (sfb_col) *sfb_col = sfb;
