@@ -1,0 +1,469 @@
+"""Benchmark of the MXFP8 decode projection with its mailbox publish/consume.
+
+One step = one call of the whole path on the N=7168, K=16384, m=8, S=4
+workload: the publishing GEMM followed by the PDL consumer (generation
+handed over, slots polled, copied out and reset).  The headline is the
+weight-stream bandwidth: (N*K + N*K/32) bytes per call / time per call.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timed region: K steps replayed from CUDA graphs of chained calls that rotate
+through enough weight copies (3 x 121 MB > 2 x the 129 MB L2) that every
+call streams its weight from HBM; CUDA events on the launching stream,
+barrier + synchronize on both sides, max over ranks.  Under torchrun every
+rank runs an independent replica on its own GPU (the path does not shard);
+``value`` is the weight bytes all ranks streamed / the slowest rank's time.
+The reference arm times the CPU oracle on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "us/call and weight-stream HBM GB/s (% of GB300 peak), MXFP8 GEMM m<=8"
+UNIT = "GB/s"
+WEIGHT_COPIES = 3
+GRAPH_STEPS = 30  # calls per captured graph (a multiple of WEIGHT_COPIES)
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("mxfp8_gemm_mailbox_gb300/csrc/publish_gemm.cu",
+                  "mxfp8_gemm_mailbox_gb300/csrc/ptx.cuh")
+TRAFFIC_FILE = ROOT / "profiles" / "publish_gemm_headline_traffic.json"
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=60000)
+    p.add_argument("--warmup", type=int, default=300)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="budget of the oracle CPU-baseline sample")
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------- ranks
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(seconds: float, units: float, group_initialised: bool):
+    """(max seconds over ranks, sum of units over ranks)."""
+    if not group_initialised:
+        return seconds, units
+    import torch
+    import torch.distributed as dist
+
+    backend = dist.get_backend()
+    dev = torch.device("cuda") if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(group_initialised: bool):
+    if group_initialised:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={CLOCK_QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names[1:], f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+def measured_peak():
+    f = ROOT / "MEASURED_PEAKS.json"
+    if f.exists():
+        try:
+            return float(json.loads(f.read_text())["hbm_gbs"]), "measured"
+        except (KeyError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        h.update((ROOT / rel).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the GEMM from the committed ncu summary, if it
+    was taken on the kernel as it is now."""
+    if not TRAFFIC_FILE.exists():
+        return None
+    try:
+        rec = json.loads(TRAFFIC_FILE.read_text())
+    except ValueError:
+        return None
+    if rec.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def workload():
+    import synthetic
+
+    return synthetic.HEADLINE
+
+
+# ------------------------------------------------------------ CPU oracle
+class OracleSample:
+    """The oracle's whole chain (FP64 GEMM, publish, consume) on the first
+    ``columns`` output columns and the first ``k`` of K (all m rows)."""
+
+    def __init__(self, columns: int, k: int | None = None):
+        import oracle
+        import synthetic
+
+        wl = workload()
+        self.columns = columns
+        self.k = k or wl.k
+        sub = synthetic.Workload(wl.name, columns, self.k, wl.m, wl.split_k, wl.capacity,
+                                 wl.exp_lo, wl.exp_hi, wl.x_zero_fraction, wl.signed_pairs,
+                                 wl.seed)
+        self.weight_bytes = sub.weight_bytes
+        self.w, self.ws = synthetic.make_weights(sub)
+        self.x, self.xs = synthetic.make_activations(sub)
+        self.mb = oracle.Mailbox(wl.capacity, columns)
+        self.ok = oracle.OK
+
+    def call(self) -> float:
+        t0 = time.perf_counter()
+        st, _, _ = self.mb.chain(self.w, self.ws, self.x, self.xs, want_c=False)
+        t1 = time.perf_counter()
+        if st != self.ok:
+            raise RuntimeError(f"oracle chain status {st}")
+        return t1 - t0
+
+    def describe(self, calls: int) -> str:
+        wl = workload()
+        return (f"{calls} oracle calls (FP64 GEMM + publish + consume, one thread) on the first "
+                f"{self.columns} of {wl.n} output columns and {self.k} of K={wl.k}, m={wl.m}: "
+                f"{self.weight_bytes} weight bytes per call")
+
+
+def oracle_baseline(seconds_budget: float, columns: int = 1024):
+    """(GB/s of weight stream, calls, seconds, sample text) of the oracle
+    repeated on a column slice until the budget is spent."""
+    sample = OracleSample(columns)
+    calls, total = 0, 0.0
+    while total < seconds_budget or calls == 0:
+        total += sample.call()
+        calls += 1
+    return sample.weight_bytes * calls / total / 1e9, calls, total, sample.describe(calls)
+
+
+# -------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_env()
+    group = False
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        group = True
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    import mxfp8_gemm_mailbox_gb300 as mx
+    import synthetic
+
+    wl = workload()
+    w, ws = synthetic.make_weights(wl)
+    x, xs = synthetic.make_activations(wl)
+    W0 = torch.from_numpy(w).to(device)
+    WS = torch.from_numpy(ws).to(device)
+    X = torch.from_numpy(x).to(device)
+    XS = torch.from_numpy(xs).to(device)
+    weights = [W0] + [W0.clone() for _ in range(WEIGHT_COPIES - 1)]
+    mb = mx.Mailbox(wl.capacity, wl.n, device=device)
+    gemms = [mx.PublishGemm(Wc, WS, mb, split_k=wl.split_k) for Wc in weights]
+    cfg = gemms[0].config()
+    for g in gemms:
+        g.precompile(wl.m)
+    out = torch.empty((wl.m, wl.n), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.Stream(device=device)
+
+    # Graphs of GRAPH_STEPS chained calls rotating through the weight copies.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for i in range(WEIGHT_COPIES):  # eager warm-up before capture
+            gemms[i].run(X, XS)
+            mb.consume(wl.m, out)
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(GRAPH_STEPS):
+                gemms[i % WEIGHT_COPIES].run(X, XS)
+                mb.consume(wl.m, out)
+    replays = max(1, -(-args.steps // GRAPH_STEPS))
+    steps = replays * GRAPH_STEPS
+    warm = max(1, -(-max(args.warmup, 3) // GRAPH_STEPS))
+
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            graph.replay()
+    stream.synchronize()
+    barrier(group)
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(replays):
+                graph.replay()
+            e1.record(stream)
+        stream.synchronize()
+    barrier(group)
+    torch.cuda.synchronize(device)
+    local_s = e0.elapsed_time(e1) / 1e3
+    seconds, bytes_all = aggregate(local_s, float(steps * wl.weight_bytes), group)
+    us_per_call = seconds / steps * 1e6
+    value = bytes_all / seconds / 1e9
+
+    # The dominant kernel alone: CUDA events around each GEMM launch.
+    n_gemm = min(2000, steps)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_gemm)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_gemm)]
+    with torch.cuda.stream(stream):
+        for i in range(n_gemm):
+            starts[i].record(stream)
+            gemms[i % WEIGHT_COPIES].run(X, XS)
+            ends[i].record(stream)
+            mb.consume(wl.m, out)
+    stream.synchronize()
+    gemm_us = statistics.mean(s.elapsed_time(e) * 1e3 for s, e in zip(starts, ends))
+    peak, peak_kind = measured_peak()
+    achieved = wl.weight_bytes / (gemm_us * 1e-6) / 1e9
+
+    # End to end through the public API from pinned host buffers.
+    hx = torch.from_numpy(x).pin_memory()
+    hxs = torch.from_numpy(xs).pin_memory()
+    hout = torch.empty((wl.m, wl.n), dtype=torch.bfloat16).pin_memory()
+    dX = torch.empty_like(X)
+    dXS = torch.empty_like(XS)
+    n_e2e = min(3000, steps)
+    with torch.cuda.stream(stream):
+        for i in range(20):
+            dX.copy_(hx, non_blocking=True)
+            dXS.copy_(hxs, non_blocking=True)
+            gemms[i % WEIGHT_COPIES].run(dX, dXS)
+            mb.consume(wl.m, out)
+            hout.copy_(out, non_blocking=True)
+        stream.synchronize()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for i in range(n_e2e):
+            dX.copy_(hx, non_blocking=True)
+            dXS.copy_(hxs, non_blocking=True)
+            gemms[i % WEIGHT_COPIES].run(dX, dXS)
+            mb.consume(wl.m, out)
+            hout.copy_(out, non_blocking=True)
+        f1.record(stream)
+    stream.synchronize()
+    e2e_s, e2e_bytes = aggregate(f0.elapsed_time(f1) / 1e3, float(n_e2e * wl.weight_bytes), group)
+    status, words = mb.status(stream)
+    if status != mx.OK:
+        raise RuntimeError(f"mailbox status {status} after the run: state {words}")
+
+    cpu = None
+    if rank == 0 and world == 1:
+        gbs, calls, secs, sample = oracle_baseline(args.cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": sample, "seconds": round(secs, 2)}
+
+    if rank == 0:
+        traffic = recorded_traffic()
+        line = {
+            "metric": METRIC,
+            "value": round(value, 1),
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": steps,
+            "warmup": warm * GRAPH_STEPS,
+            "ms_per_step": round(us_per_call / 1e3, 6),
+            "us_per_call": round(us_per_call, 3),
+            "pct_of_peak": round(100 * (value / world) / peak, 1),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "e4m3",
+            "data": "synthetic (seeded N(0,1) E4M3, E8M0 block-32 scales, 1% zero x)",
+            "config": {
+                "workload": "decode projection N=7168 K=16384 m=8 S=4 + mailbox publish/consume",
+                "n": wl.n, "k": wl.k, "m": wl.m, "split_k": cfg["split_k"],
+                "stages": cfg["stages"], "grid_ctas": cfg["grid_ctas"],
+                "smem_bytes": cfg["smem_bytes"],
+                "weight_bytes_per_call": wl.weight_bytes,
+                "l2": f"{WEIGHT_COPIES} rotating weight copies ({WEIGHT_COPIES * wl.weight_bytes >> 20}"
+                      " MiB > 2 x 129 MB L2): every call streams its weight from HBM",
+                "timing": f"CUDA graphs of {GRAPH_STEPS} chained calls (GEMM -> PDL consumer)",
+                "parallelism": "replicas" if world > 1 else "single GPU",
+            },
+            "roofline": {
+                "bound": "hbm",
+                "kernel": "publish_gemm_kernel<4>",
+                "achieved": round(achieved, 1),
+                "peak": peak,
+                "peak_kind": peak_kind,
+                "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": wl.weight_bytes,
+                "launch_us": round(gemm_us, 3),
+            },
+            "cpu_baseline": cpu,
+            "e2e": {
+                "value": round(e2e_bytes / e2e_s / 1e9, 1),
+                "unit": UNIT,
+                "us_per_call": round(e2e_s / n_e2e * 1e6, 3),
+                "steps": n_e2e,
+                "h2d_bytes_per_step": int(X.numel() + XS.numel()),
+                "d2h_bytes_per_step": int(out.numel() * out.element_size()),
+            },
+            "gpu_launches": 2 * steps,
+            "clocks": clocks.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    for g in gemms:
+        g.close()
+    if group:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+# -------------------------------------------------------- reference arm
+def run_reference(args):
+    """The oracle as the reference arm: each step one oracle call of the
+    whole chain on a column slice of the workload, the slice sized so all
+    warm-up and timed steps fit in about two minutes."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return  # rank 0 alone runs the oracle; the others exit without work
+    steps, warm = max(1, args.steps), max(0, args.warmup)
+    per_step = min(3.0, 120.0 / (steps + warm))
+    wl = workload()
+    k = wl.k
+    while True:  # shrink K until an 8-column call fits the per-step budget
+        probe = OracleSample(8, k)
+        t8 = min(probe.call() for _ in range(3))
+        if t8 <= per_step or k <= 128:
+            break
+        k //= 2
+    columns = int(max(8, min(1024, 8 * int(per_step / max(t8, 1e-6)))))
+    sample = OracleSample(columns, k)
+    for _ in range(warm):
+        sample.call()
+    total = sum(sample.call() for _ in range(steps))
+    gbs = sample.weight_bytes * steps / total / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(gbs, 6),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warm,
+        "ms_per_step": round(total / steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) E4M3, E8M0 block-32 scales, 1% zero x)",
+        "config": {
+            "workload": "decode projection N=7168 K=16384 m=8 S=4 + mailbox publish/consume",
+            "n": wl.n, "k": wl.k, "m": wl.m, "split_k": wl.split_k,
+            "sample_columns": columns, "sample_k": k,
+            "weight_bytes_per_step": sample.weight_bytes,
+        },
+        "cpu_baseline": {"value": round(gbs, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample.describe(steps)},
+        "e2e": {"value": round(gbs, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

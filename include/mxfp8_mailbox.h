@@ -64,9 +64,14 @@ typedef enum mxfp8_status {
 } mxfp8_status;
 
 /* Shape and tactic of one publishing GEMM (the tactic fields follow the
- * publishing_gemm page's (cta_k, ab_stages, sfb_tmem_stages, split_k); the
- * scale factors of x live in tensor memory for the whole K range, so there is
- * no sfb stage count).  Zero in a tactic field asks the library to choose. */
+ * publishing_gemm page's (cta_k, ab_stages, sfb_tmem_stages, split_k); the x
+ * scales ride in the same ring as the W scales, so there is no separate sfb
+ * stage count).  acc_blocks is this library's addition: how many 32-wide K
+ * blocks the tensor core sums in one accumulator before the epilogue folds
+ * the partial into its compensated (two-float) sum; 1 keeps every output
+ * within 2 BF16 ULPs of the exact sum on near-cancelling outputs that a single
+ * long FP32 accumulation misses.  Zero in a tactic field asks the library to
+ * choose. */
 typedef struct mxfp8_gemm_desc {
   int32_t n;          /* output columns N ("hidden"): a positive multiple of 128     */
   int32_t k;          /* reduction length K: a positive multiple of 32, <= 32768     */
@@ -74,7 +79,17 @@ typedef struct mxfp8_gemm_desc {
   int32_t split_k;    /* cluster split-K S: 1, 2 or 4 (0 = choose)                   */
   int32_t cta_k;      /* K elements per pipeline stage: 128 (0 = 128)                */
   int32_t stages;     /* shared-memory ring depth: 2..16 (0 = choose)                */
+  int32_t acc_blocks; /* K blocks per promoted partial sum: 1 or 4 (0 = 4)           */
+  int32_t w_layout;   /* MXFP8_W_IN_PLACE or MXFP8_W_TILED (0 = choose)              */
 } mxfp8_gemm_desc;
+
+/* Where the GEMM streams W from.  IN_PLACE: the caller's [N][K] buffer,
+ * through 2-D TMA tiles (the handle borrows w).  TILED: a copy made once at
+ * create inside the workspace, laid out tile by tile (128 rows x 128 K bytes,
+ * already in the order shared memory holds it) so every pipeline stage is one
+ * contiguous 16 KB read; the caller's w is not read after create. */
+#define MXFP8_W_IN_PLACE 1
+#define MXFP8_W_TILED 2
 
 typedef struct mxfp8_publish_gemm mxfp8_publish_gemm; /* opaque */
 
@@ -96,9 +111,11 @@ size_t mxfp8_mailbox_bytes(int32_t capacity_m, int32_t n);
 mxfp8_status mxfp8_mailbox_init(void* mailbox, int32_t* stage_state, int32_t capacity_m,
                                 int32_t n, void* stream);
 
-/* Device bytes the handle needs for W's scale factors, re-laid once at
- * create into the tiled order the tensor-core copy reads: N/128 x ceil(K/128)
- * chunks of 512 bytes.  0 for an invalid descriptor. */
+/* Device bytes the handle needs: W's scale factors re-laid once at create
+ * into the tiled order the tensor-core copy reads (N/128 x ceil(K/128) chunks
+ * of 512 bytes), plus, for MXFP8_W_TILED (and for w_layout 0, which chooses
+ * it), the tiled copy of W (N x ceil(K/128) x 128 bytes).  0 for an invalid
+ * descriptor. */
 size_t mxfp8_publish_gemm_workspace_bytes(const mxfp8_gemm_desc* desc);
 
 /* Build a publishing GEMM for one weight and one mailbox (publishing_gemm
@@ -110,17 +127,18 @@ size_t mxfp8_publish_gemm_workspace_bytes(const mxfp8_gemm_desc* desc);
  *  mailbox:    device, 16-byte aligned, as for mxfp8_mailbox_init.
  *  stage_state:device, 16-byte aligned int32[4].
  *  workspace:  device, 256-byte aligned, >= mxfp8_publish_gemm_workspace_bytes.
- * The handle borrows w, mailbox, stage_state and workspace until destroy
- * (w_scale is read once, by a kernel launched here on `stream`, and not
- * afterwards).  On success *out receives the handle. */
+ * The handle borrows mailbox, stage_state and workspace until destroy, and w
+ * too for MXFP8_W_IN_PLACE (w_scale, and w for MXFP8_W_TILED, are read once,
+ * by kernels launched here on `stream`, and not afterwards).  On success *out
+ * receives the handle. */
 mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* w,
                                        const void* w_scale, void* mailbox,
                                        int32_t* stage_state, void* workspace,
                                        size_t workspace_bytes, void* stream,
                                        mxfp8_publish_gemm** out);
 
-/* The resolved shape and tactic of a handle (split_k, cta_k, stages filled
- * in), plus the dynamic shared memory, tensor-memory columns and grid size of
+/* The resolved shape and tactic of a handle (split_k, cta_k, stages,
+ * acc_blocks filled in), plus the dynamic shared memory, tensor-memory columns and grid size of
  * its launch. */
 mxfp8_status mxfp8_publish_gemm_config(const mxfp8_publish_gemm* gemm, mxfp8_gemm_desc* desc,
                                        int32_t* smem_bytes, int32_t* tmem_columns,

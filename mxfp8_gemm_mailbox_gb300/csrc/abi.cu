@@ -21,12 +21,13 @@ struct mxfp8_publish_gemm {
   mxfp8_gemm_desc desc;  // resolved tactic
   const uint8_t* w;
   uint8_t* w_sf;
+  uint8_t* w_tiled;  // nullptr when W is read in place
   uint16_t* mailbox;
   int32_t* state;
   int device;
   int k_tiles;
   int tiles_per_split;
-  uint32_t tmem_cols, sfb_col, sfa_col;
+  TmemPlan tmem;
   GemmSmemLayout layout;
   CUtensorMap tmap_w;
   // Tensor map of the last activation buffer seen (x pointer, m).
@@ -105,10 +106,22 @@ mxfp8_status check_desc(const mxfp8_gemm_desc* d) {
   if (d->cta_k != 0 && d->cta_k != kTileK) return fail(MXFP8_ERR_UNSUPPORTED, "cta_k must be 128");
   if (d->stages != 0 && (d->stages < 2 || d->stages > kMaxStages))
     return fail(MXFP8_ERR_UNSUPPORTED, "stages must be in 2..16 (or 0 to choose)");
+  if (d->acc_blocks != 0 && d->acc_blocks != 1 && d->acc_blocks != 4)
+    return fail(MXFP8_ERR_UNSUPPORTED, "acc_blocks must be 1 or 4 (or 0 to choose)");
+  if (d->w_layout != 0 && d->w_layout != MXFP8_W_IN_PLACE && d->w_layout != MXFP8_W_TILED)
+    return fail(MXFP8_ERR_UNSUPPORTED, "w_layout must be MXFP8_W_IN_PLACE or MXFP8_W_TILED");
   return MXFP8_OK;
 }
 
 int k_tiles_of(int k) { return (k + kTileK - 1) / kTileK; }
+
+int resolved_w_layout(int w_layout) { return w_layout == 0 ? MXFP8_W_TILED : w_layout; }
+
+size_t scale_chunk_bytes(int n, int k) {
+  return static_cast<size_t>(n / kBlockN) * k_tiles_of(k) * kSfChunkBytes;
+}
+
+size_t tiled_w_offset(int n, int k) { return (scale_chunk_bytes(n, k) + 255) & ~size_t{255}; }
 
 struct DeviceLimits {
   int sms = 0;
@@ -142,6 +155,8 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
     d->split_k = s;
   }
   d->cta_k = kTileK;
+  if (d->acc_blocks == 0) d->acc_blocks = 4;
+  d->w_layout = resolved_w_layout(d->w_layout);
   const int tps = (k_tiles + d->split_k - 1) / d->split_k;
   if (tps > kMaxTilesPerSplit)
     return fail(MXFP8_ERR_UNSUPPORTED, "too many K tiles per split: raise split_k");
@@ -152,7 +167,7 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
     int best = 0;
     for (int s = 2; s <= kMaxStages; ++s) {
       if (static_cast<int>(gemm_smem_layout(s, d->split_k, tps).total) > budget) break;
-      if (gemm_tmem_columns(s, tps, nullptr, nullptr) > static_cast<uint32_t>(512 / per_sm)) break;
+      if (gemm_tmem_plan(s, d->acc_blocks).cols > static_cast<uint32_t>(512 / per_sm)) break;
       best = s;
       if (s >= tps) break;  // more stages than K tiles buy nothing
     }
@@ -161,7 +176,7 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
   }
   if (static_cast<int>(gemm_smem_layout(d->stages, d->split_k, tps).total) > lim.smem_optin)
     return fail(MXFP8_ERR_UNSUPPORTED, "the requested stages do not fit in shared memory");
-  if (gemm_tmem_columns(d->stages, tps, nullptr, nullptr) > 512)
+  if (gemm_tmem_plan(d->stages, d->acc_blocks).cols > 512)
     return fail(MXFP8_ERR_UNSUPPORTED, "the requested stages do not fit in tensor memory");
   return MXFP8_OK;
 }
@@ -198,11 +213,11 @@ mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale,
   p.stages = g->desc.stages;
   p.capacity = g->desc.capacity_m;
   p.publish = publish ? 1 : 0;
-  p.tmem_cols = g->tmem_cols;
-  p.sfb_col = g->sfb_col;
-  p.sfa_col = g->sfa_col;
+  p.acc_blocks = g->desc.acc_blocks;
+  p.tmem = g->tmem;
   p.x_scale = static_cast<const uint8_t*>(x_scale);
   p.w_sf = g->w_sf;
+  p.w_tiled = g->w_tiled;
   p.c = static_cast<uint16_t*>(c);
   p.mailbox = g->mailbox;
   p.state = g->state;
@@ -247,7 +262,9 @@ mxfp8_status mxfp8_mailbox_init(void* mailbox, int32_t* stage_state, int32_t cap
 
 size_t mxfp8_publish_gemm_workspace_bytes(const mxfp8_gemm_desc* desc) {
   if (!desc || desc->n <= 0 || desc->n % kBlockN || desc->k <= 0 || desc->k % 32) return 0;
-  return static_cast<size_t>(desc->n / kBlockN) * k_tiles_of(desc->k) * kSfChunkBytes;
+  if (resolved_w_layout(desc->w_layout) != MXFP8_W_TILED) return scale_chunk_bytes(desc->n, desc->k);
+  return tiled_w_offset(desc->n, desc->k) +
+         static_cast<size_t>(desc->n / kBlockN) * k_tiles_of(desc->k) * kWTileBytes;
 }
 
 mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* w,
@@ -286,12 +303,15 @@ mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* 
   }
   g->w = static_cast<const uint8_t*>(w);
   g->w_sf = static_cast<uint8_t*>(workspace);
+  g->w_tiled = g->desc.w_layout == MXFP8_W_TILED
+                   ? static_cast<uint8_t*>(workspace) + tiled_w_offset(desc->n, desc->k)
+                   : nullptr;
   g->mailbox = static_cast<uint16_t*>(mailbox);
   g->state = stage_state;
   g->device = device;
   g->k_tiles = k_tiles_of(desc->k);
   g->tiles_per_split = (g->k_tiles + g->desc.split_k - 1) / g->desc.split_k;
-  g->tmem_cols = gemm_tmem_columns(g->desc.stages, g->tiles_per_split, &g->sfb_col, &g->sfa_col);
+  g->tmem = gemm_tmem_plan(g->desc.stages, g->desc.acc_blocks);
   g->layout = gemm_smem_layout(g->desc.stages, g->desc.split_k, g->tiles_per_split);
   g->x_cached = nullptr;
   g->m_cached = 0;
@@ -312,6 +332,14 @@ mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* 
     delete g;
     return cuda_fail(e, "launching the W scale re-layout");
   }
+  if (g->w_tiled != nullptr) {
+    e = launch_tile_weights(static_cast<const uint8_t*>(w), g->w_tiled, desc->n, desc->k,
+                            static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+      delete g;
+      return cuda_fail(e, "launching the W tiling copy");
+    }
+  }
   *out = g;
   return MXFP8_OK;
 }
@@ -322,7 +350,7 @@ mxfp8_status mxfp8_publish_gemm_config(const mxfp8_publish_gemm* gemm, mxfp8_gem
   if (!gemm) return fail(MXFP8_ERR_INVALID, "gemm handle is NULL");
   if (desc) *desc = gemm->desc;
   if (smem_bytes) *smem_bytes = static_cast<int32_t>(gemm->layout.total);
-  if (tmem_columns) *tmem_columns = static_cast<int32_t>(gemm->tmem_cols);
+  if (tmem_columns) *tmem_columns = static_cast<int32_t>(gemm->tmem.cols);
   if (grid_ctas) *grid_ctas = (gemm->desc.n / kBlockN) * gemm->desc.split_k;
   return MXFP8_OK;
 }

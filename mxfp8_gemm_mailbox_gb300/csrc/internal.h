@@ -19,6 +19,7 @@ constexpr int kGenerations = 3;
 constexpr uint32_t kSentinel = 0x80000000u;
 constexpr int kMaxStages = 16;
 constexpr int kMaxTilesPerSplit = 256;
+constexpr int kAccRing = 4;       // accumulator slots in tensor memory (in stages)
 
 // Byte offsets inside the GEMM's dynamic shared memory (after aligning the
 // base to 1024 bytes), computed once on the host.
@@ -34,6 +35,16 @@ struct GemmSmemLayout {
   uint32_t total;     // bytes including the alignment slack
 };
 
+// Tensor-memory columns of one CTA: the accumulator ring, then the W and x
+// scale rings (4 columns a stage each).
+struct TmemPlan {
+  uint32_t cols;       // allocated (a power of two >= 32)
+  uint32_t acc;        // first accumulator column
+  uint32_t acc_slot;   // columns per accumulator slot (one stage of MMAs)
+  uint32_t sfa;        // first column of the W scale ring
+  uint32_t sfb;        // first column of the x scale ring
+};
+
 struct GemmParams {
   int32_t n, k, m;
   int32_t k_tiles;          // ceil(k / 128)
@@ -41,11 +52,11 @@ struct GemmParams {
   int32_t stages;
   int32_t capacity;
   int32_t publish;          // 1: fused publish into the mailbox; 0: C only
-  uint32_t tmem_cols;
-  uint32_t sfb_col;         // first tensor-memory column of the x scales
-  uint32_t sfa_col;         // first tensor-memory column of the W scale ring
+  int32_t acc_blocks;       // 32-wide K blocks summed in TMEM per promoted partial: 1 or 4
+  TmemPlan tmem;
   const uint8_t* x_scale;   // [m][k/32]
   const uint8_t* w_sf;      // [n/128][k_tiles][512] tiled W scales
+  const uint8_t* w_tiled;   // [n/128][k_tiles][16384] shared-memory images of W, or nullptr
   uint16_t* c;              // [m][n] BF16 or nullptr
   uint16_t* mailbox;        // [3][capacity][n] BF16
   int32_t* state;           // int32[4]
@@ -54,7 +65,7 @@ struct GemmParams {
 };
 
 GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split);
-uint32_t gemm_tmem_columns(int stages, int tiles_per_split, uint32_t* sfb_col, uint32_t* sfa_col);
+TmemPlan gemm_tmem_plan(int stages, int acc_blocks);
 
 // Kernel launchers (return the CUDA error of the launch).
 cudaError_t launch_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
@@ -62,6 +73,8 @@ cudaError_t launch_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
 cudaError_t set_gemm_smem_attribute(int split_k, int bytes);
 cudaError_t launch_relayout_w_scales(const uint8_t* w_scale, uint8_t* w_sf, int n, int k,
                                      cudaStream_t stream);
+cudaError_t launch_tile_weights(const uint8_t* w, uint8_t* w_tiled, int n, int k,
+                                cudaStream_t stream);
 cudaError_t launch_mailbox_init(uint16_t* mailbox, int32_t* state, int capacity, int n,
                                 cudaStream_t stream);
 cudaError_t launch_mailbox_consume(uint16_t* mailbox, int32_t* state, int capacity, int n, int m,

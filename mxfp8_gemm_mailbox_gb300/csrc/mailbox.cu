@@ -53,10 +53,11 @@ __global__ void __launch_bounds__(kConsumeThreads)
                            int capacity, int n, int m, uint16_t* __restrict__ out,
                            uint64_t timeout_ns) {
   __shared__ uint32_t shared_generation;
-  // The GEMM (or publish kernel) before this one has completed and its stores
+  // The next kernel may launch now (its own grid wait covers this grid); the
+  // GEMM (or publish kernel) before this one has completed and its stores
   // are visible after the grid wait.
-  ptx::grid_dependency_wait();
   ptx::launch_dependents();
+  ptx::grid_dependency_wait();
   if (threadIdx.x == 0) {
     // One read of the generation per CTA, before the CTA counts itself, so
     // the last CTA may advance it while the others still run.
@@ -103,8 +104,8 @@ __global__ void __launch_bounds__(kConsumeThreads)
 __global__ void __launch_bounds__(kConsumeThreads)
     mailbox_publish_kernel(uint16_t* __restrict__ mailbox, int32_t* __restrict__ state,
                            int capacity, int n, int m, const uint16_t* __restrict__ c) {
-  ptx::grid_dependency_wait();
   ptx::launch_dependents();
+  ptx::grid_dependency_wait();
   const uint32_t g = ptx::ld_volatile_u32(state + 0);
   const bool first = blockIdx.x == 0 && threadIdx.x == 0;
   if (g >= static_cast<uint32_t>(kGenerations)) {

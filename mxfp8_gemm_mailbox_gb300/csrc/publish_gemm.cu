@@ -4,27 +4,36 @@
 // specialized_decode.boundary.publishing_gemm", module description "GEMM
 // structure"): the weight is the MMA's A operand (128 output columns per CTA,
 // N/128 tiles), the at most 8 activation rows its B operand (N = 8).  Each
-// CTA of a split-K cluster of S multiplies one K slice; the FP32 partials are
+// CTA of a split-K cluster of S multiplies one K slice; the partials are
 // exchanged through distributed shared memory and each CTA reduces 1/S of
 // the tokens.  The epilogue rounds to BF16, writes C, and publishes every
 // value with negative zero cleared into generation stage_state[0] of the
 // mailbox as aligned 16-byte packs of eight consecutive columns, then one
 // thread sets stage_state[1] (same page, publish_value and epilog_warp).
 //
+// Accumulation.  The tensor core's own FP32 accumulation over a long K loses
+// too much on outputs that nearly cancel, so partial sums leave tensor memory
+// early: each MMA (or each group of acc_blocks MMAs) writes a fresh
+// accumulator slot of a ring, and the epilogue warps fold every slot into a
+// compensated FP32 pair (hi + lo, Knuth's TwoSum) as soon as it completes.
+// The pair is widened to FP64 and rounded once to BF16.
+//
 // Warp roles (192 threads):
 //   warp 0      TMA producer: W tile + W scale chunk per stage (started
 //               before the programmatic grid wait), x tile (after it).
-//   warp 1      tensor-memory allocation; one thread issues tcgen05.cp of the
-//               W scales and the block-scaled tcgen05.mma per 32-wide K block.
-//   warps 2-5   epilogue: x scales into tensor memory, accumulator read-back
-//               (tcgen05.ld 32x32b: thread = output column, 8 registers =
-//               8 tokens), split-K exchange, BF16 rounding, C store, publish.
+//   warp 1      tensor-memory allocation; one thread issues, per stage,
+//               tcgen05.cp of the W and x scale chunks and one block-scaled
+//               tcgen05.mma per 32-wide K block.
+//   warps 2-5   epilogue: x scales staged for the copies, partial sums read
+//               back (tcgen05.ld 32x32b: thread = output column, registers =
+//               tokens) and folded into the compensated sums, split-K
+//               exchange, BF16 rounding, C store, publish.
 //
-// Tensor-memory columns: [0, 8) FP32 accumulator (lane = output column,
-// column = token); [sfa_col, +4*stages) the W scale ring and [sfb_col,
-// +4*stages) the x scale ring, one 4-column slot per stage each, filled by
-// tcgen05.cp (32x128b, multicast to the four lane quarters) from 16-byte-row
-// scale chunks in shared memory.  Every scale address is 4-column aligned.
+// Tensor-memory columns: [acc, +4 * acc_slot) the accumulator ring (FP32,
+// lane = output column, column = block * 8 + token); then the W and x scale
+// rings, one 4-column slot per stage each, filled by tcgen05.cp (32x128b,
+// multicast to the four lane quarters) from 16-byte-row scale chunks in
+// shared memory.  Every scale address is 4-column aligned.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -41,8 +50,8 @@ constexpr uint32_t kStageTxBytes = kWTileBytes + kXTileBytes + kSfChunkBytes;
 // (format 0), both K-major, N = 8 (bits 17-22: N >> 3), E8M0 scales (bit 23),
 // M = 128 (bits 24-28: M >> 4).  The scale-factor byte ids of A (bits 29-30)
 // and B (bits 4-5) select the K block inside a 32-bit scale column.
-constexpr uint32_t kIdescBase =
-    (static_cast<uint32_t>(kRows >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(kBlockN >> 4) << 24);
+constexpr uint32_t kIdescBase = (static_cast<uint32_t>(kRows >> 3) << 17) | (1u << 23) |
+                                (static_cast<uint32_t>(kBlockN >> 4) << 24);
 
 __device__ __forceinline__ uint32_t idesc_for_block(uint32_t kb) {
   return kIdescBase | (kb << 4) | (kb << 29);
@@ -64,17 +73,50 @@ __device__ __forceinline__ void epilogue_barrier() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
-// acc[index] for a runtime index without spilling the array to local memory.
-template <int N>
-__device__ __forceinline__ float select(const float (&acc)[N], int index) {
-  float v = acc[0];
-#pragma unroll
-  for (int q = 1; q < N; ++q) v = (q == index) ? acc[q] : v;
-  return v;
+// Compensated summation: (hi, lo) += v with the rounding error of the add
+// kept in lo (TwoSum: exact error of a floating-point addition, valid for
+// operands of either magnitude order).
+__device__ __forceinline__ void two_sum_add(float& hi, float& lo, float v) {
+  const float s = __fadd_rn(hi, v);
+  const float bp = __fsub_rn(s, hi);
+  const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(v, bp));
+  hi = s;
+  lo = __fadd_rn(lo, err);
 }
 
-__device__ __forceinline__ uint16_t bf16_bits_rn(float v) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+// A double rounded once to BF16 bits, to nearest with ties to even, from the
+// two formats' bit layouts (BF16: 8 exponent bits, bias 127, 7 stored
+// mantissa bits; subnormal quantum 2^-133).
+__device__ __forceinline__ uint16_t bf16_bits_from_double(double v) {
+  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(v));
+  const uint32_t sign = static_cast<uint32_t>(b >> 63) << 15;
+  const int exp = static_cast<int>((b >> 52) & 0x7FF);
+  const unsigned long long mant = b & ((1ull << 52) - 1);
+  if (exp == 0x7FF) return static_cast<uint16_t>(sign | (mant ? 0x7FC0u : 0x7F80u));
+  if (exp == 0) return static_cast<uint16_t>(sign);  // below 2^-1022: rounds to zero
+  int e = exp - 1023;
+  if (e >= -126) {
+    unsigned long long keep = mant >> 45;
+    const unsigned long long rest = mant & ((1ull << 45) - 1);
+    const unsigned long long half = 1ull << 44;
+    if (rest > half || (rest == half && (keep & 1ull))) ++keep;
+    if (keep == 128) {
+      keep = 0;
+      ++e;
+    }
+    if (e > 127) return static_cast<uint16_t>(sign | 0x7F80u);
+    return static_cast<uint16_t>(sign | (static_cast<uint32_t>(e + 127) << 7) |
+                                 static_cast<uint32_t>(keep));
+  }
+  // Subnormal in BF16: units of 2^-133 = significand * 2^(e + 81).
+  const unsigned long long sig = mant | (1ull << 52);
+  const int drop = -(e + 81);  // >= 46
+  if (drop > 54) return static_cast<uint16_t>(sign);
+  unsigned long long q = sig >> drop;
+  const unsigned long long rest = sig & ((1ull << drop) - 1);
+  const unsigned long long half = 1ull << (drop - 1);
+  if (rest > half || (rest == half && (q & 1ull))) ++q;
+  return static_cast<uint16_t>(sign | static_cast<uint32_t>(q));  // q == 128 is 2^-126
 }
 
 template <int S>
@@ -97,11 +139,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kt_end = min(p.k_tiles, kt_begin + p.tiles_per_split);
   const int nkt = max(0, kt_end - kt_begin);
   const int stages = p.stages;
+  const bool per_block = p.acc_blocks == 1;
 
-  const uint32_t bar_full = sbase + L.bars;
-  const uint32_t bar_empty = bar_full + 8u * stages;
-  const uint32_t bar_acc = bar_empty + 8u * stages;
-  const uint32_t bar_sfb = bar_acc + 8u;
+  const uint32_t bar_full = sbase + L.bars;                     // [stages]
+  const uint32_t bar_empty = bar_full + 8u * stages;            // [stages]
+  const uint32_t bar_acc_full = bar_empty + 8u * stages;        // [kAccRing]
+  const uint32_t bar_acc_empty = bar_acc_full + 8u * kAccRing;  // [kAccRing]
+  const uint32_t bar_sfb = bar_acc_empty + 8u * kAccRing;
   const uint32_t bar_recv = bar_sfb + 8u;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L.misc);  // [0] tmem base, [1] generation
 
@@ -112,14 +156,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar_full + 8u * s, 1);
       ptx::mbar_init(bar_empty + 8u * s, 1);
     }
-    ptx::mbar_init(bar_acc, 1);
+    for (int r = 0; r < kAccRing; ++r) {
+      ptx::mbar_init(bar_acc_full + 8u * r, 1);
+      ptx::mbar_init(bar_acc_empty + 8u * r, 128);
+    }
     ptx::mbar_init(bar_sfb, 128);
     ptx::mbar_init(bar_recv, 1);
     ptx::fence_mbarrier_init();
     ptx::fence_proxy_async_smem();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(sbase + L.misc, p.tmem_cols);
+    ptx::tmem_alloc(sbase + L.misc, p.tmem.cols);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -138,13 +185,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_stream = ptx::policy_evict_first();
       const uint64_t pol_keep = ptx::policy_evict_last();
       const int npre = min(stages, nkt);
+      // One 128 x 128-byte W tile: a contiguous 16 KB image from the tiled
+      // copy, or a 2-D TMA box (with the same 128-byte swizzle) of W in place.
+      auto load_w_tile = [&](uint32_t dst, int kt, uint32_t bar) {
+        if (p.w_tiled != nullptr)
+          ptx::bulk_load(dst, p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt) * kWTileBytes,
+                         kWTileBytes, bar, pol_stream);
+        else
+          ptx::tma_load_2d(dst, &tmap_w, kt * kTileK, tile * kBlockN, bar, pol_stream);
+      };
       // W and its scales do not depend on the previous kernel: start them now.
       for (int i = 0; i < npre; ++i) {
         const uint32_t full = bar_full + 8u * i;
         const int kt = kt_begin + i;
         ptx::mbar_arrive_expect_tx(full, kStageTxBytes);
-        ptx::tma_load_2d(sbase + L.w + i * kWTileBytes, &tmap_w, kt * kTileK, tile * kBlockN, full,
-                         pol_stream);
+        load_w_tile(sbase + L.w + i * kWTileBytes, kt, full);
         ptx::bulk_load(sbase + L.sfa + i * kSfChunkBytes,
                        p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt) * kSfChunkBytes,
                        kSfChunkBytes, full, pol_stream);
@@ -165,8 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t full = bar_full + 8u * s;
         const int kt = kt_begin + i;
         ptx::mbar_arrive_expect_tx(full, kStageTxBytes);
-        ptx::tma_load_2d(sbase + L.w + s * kWTileBytes, &tmap_w, kt * kTileK, tile * kBlockN, full,
-                         pol_stream);
+        load_w_tile(sbase + L.w + s * kWTileBytes, kt, full);
         ptx::bulk_load(sbase + L.sfa + s * kSfChunkBytes,
                        p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt) * kSfChunkBytes,
                        kSfChunkBytes, full, pol_stream);
@@ -189,34 +243,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) raise_flag(p.state, 0x2u);
         ptx::tc_fence_after();
       }
-      const uint32_t d_tmem = tmem;  // accumulator at column 0
       for (int i = 0; i < nkt && ok; ++i) {
         const int s = i % stages;
+        const int r = i % kAccRing;
         if (!ptx::mbar_wait(bar_full + 8u * s, static_cast<uint32_t>(i / stages) & 1u,
-                            p.wait_limit_ns)) {
+                            p.wait_limit_ns) ||
+            (i >= kAccRing &&
+             !ptx::mbar_wait(bar_acc_empty + 8u * r,
+                             (static_cast<uint32_t>(i / kAccRing) - 1u) & 1u, p.wait_limit_ns))) {
           raise_flag(p.state, 0x2u);
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t sfa_t = tmem + p.sfa_col + 4u * s;
-        const uint32_t sfb_t = tmem + p.sfb_col + 4u * s;
+        const uint32_t sfa_t = tmem + p.tmem.sfa + 4u * s;
+        const uint32_t sfb_t = tmem + p.tmem.sfb + 4u * s;
         ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::desc_rows16(sbase + L.sfa + s * kSfChunkBytes));
         ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::desc_rows16(sbase + L.sx + i * 128));
         const uint32_t a0 = sbase + L.w + s * kWTileBytes;
         const uint32_t b0 = sbase + L.x + s * kXTileBytes;
+        const uint32_t d0 = tmem + p.tmem.acc + p.tmem.acc_slot * static_cast<uint32_t>(r);
 #pragma unroll
         for (uint32_t kb = 0; kb < kSfPerTile; ++kb) {
-          ptx::mma_mxf8(d_tmem, ptx::desc_kmajor_sw128(a0 + 32u * kb),
-                        ptx::desc_kmajor_sw128(b0 + 32u * kb), idesc_for_block(kb),
-                        (i > 0 || kb > 0) ? 1u : 0u, sfa_t, sfb_t);
+          // One 8-column accumulator per block, or one per stage.
+          const uint32_t d = per_block ? d0 + 8u * kb : d0;
+          const uint32_t accumulate = per_block ? 0u : (kb > 0 ? 1u : 0u);
+          ptx::mma_mxf8(d, ptx::desc_kmajor_sw128(a0 + 32u * kb),
+                        ptx::desc_kmajor_sw128(b0 + 32u * kb), idesc_for_block(kb), accumulate,
+                        sfa_t, sfb_t);
         }
         ptx::mma_commit(bar_empty + 8u * s);
+        ptx::mma_commit(bar_acc_full + 8u * r);
       }
-      if (nkt > 0 && ok)
-        ptx::mma_commit(bar_acc);
-      else
-        ptx::mbar_arrive(bar_acc);
     }
   } else {
     // ------------------------------------------------------------- epilogue
@@ -250,26 +308,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_proxy_async_smem();  // the tensor-memory copy reads them
     ptx::mbar_arrive(bar_sfb);
 
-    if (!ptx::mbar_wait(bar_acc, 0, p.wait_limit_ns)) raise_flag(p.state, 0x2u);
-    ptx::tc_fence_after();
-    float acc[kRows];
-    if (nkt > 0) {
-      uint32_t r[8];
-      ptx::tmem_ld_32x32b_x8(tmem + lane_base, r);
-      ptx::tmem_wait_ld();
+    // Fold every completed accumulator slot into the compensated sums.
+    float hi[kRows], lo[kRows];
 #pragma unroll
-      for (int q = 0; q < kRows; ++q) acc[q] = __uint_as_float(r[q]);
-    } else {
-      // A split with no K tiles contributes zeros.
+    for (int t = 0; t < kRows; ++t) hi[t] = lo[t] = 0.0f;
+    for (int i = 0; i < nkt; ++i) {
+      const int r = i % kAccRing;
+      if (!ptx::mbar_wait(bar_acc_full + 8u * r, static_cast<uint32_t>(i / kAccRing) & 1u,
+                          p.wait_limit_ns)) {
+        raise_flag(p.state, 0x2u);
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t slot =
+          tmem + lane_base + p.tmem.acc + p.tmem.acc_slot * static_cast<uint32_t>(r);
+      if (per_block) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(slot, v);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_acc_empty + 8u * r);
 #pragma unroll
-      for (int q = 0; q < kRows; ++q) acc[q] = 0.0f;
+        for (int kb = 0; kb < kSfPerTile; ++kb)
+#pragma unroll
+          for (int t = 0; t < kRows; ++t)
+            two_sum_add(hi[t], lo[t], __uint_as_float(v[kb * 8 + t]));
+      } else {
+        uint32_t v[8];
+        ptx::tmem_ld_32x32b_x8(slot, v);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_acc_empty + 8u * r);
+#pragma unroll
+        for (int t = 0; t < kRows; ++t) two_sum_add(hi[t], lo[t], __uint_as_float(v[t]));
+      }
     }
 
-    constexpr int kShard = kRows / S;  // tokens this CTA reduces and stores
-    float owned[kShard];
+    // Split-K: every CTA sends the (hi, lo) pairs of the tokens it does not
+    // own to their owners, then sums the S pairs of its own tokens in K-slice
+    // order.  A split with no K tiles contributes zeros.
+    constexpr int kShard = kRows / S;
+    double owned[kShard];
     if constexpr (S > 1) {
       if (etid == 0)
-        ptx::mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>((S - 1) * kShard * kBlockN * 4));
+        ptx::mbar_arrive_expect_tx(bar_recv,
+                                   static_cast<uint32_t>((S - 1) * kShard * kBlockN * 8));
 #pragma unroll
       for (int peer = 0; peer < S; ++peer) {
         if (peer == static_cast<int>(split)) continue;
@@ -278,37 +361,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t remote_bar = ptx::map_to_rank(bar_recv, peer);
 #pragma unroll
         for (int jj = 0; jj < kShard; ++jj) {
-          const uint32_t local = sbase + L.recv + ((sender * kShard + jj) * kBlockN + col) * 4;
+          const uint32_t local =
+              sbase + L.recv + (((sender * kShard + jj) * kBlockN + col) * 2) * 4;
           ptx::st_async_remote(ptx::map_to_rank(local, peer),
-                               __float_as_uint(acc[peer * kShard + jj]), remote_bar);
+                               __float_as_uint(hi[peer * kShard + jj]), remote_bar);
+          ptx::st_async_remote(ptx::map_to_rank(local + 4, peer),
+                               __float_as_uint(lo[peer * kShard + jj]), remote_bar);
         }
       }
       if (!ptx::mbar_wait_cluster(bar_recv, 0, p.wait_limit_ns)) raise_flag(p.state, 0x2u);
       const float* recv = reinterpret_cast<const float*>(smem + L.recv);
 #pragma unroll
       for (int jj = 0; jj < kShard; ++jj) {
-        float total = 0.0f;
+        float sh = 0.0f, sl = 0.0f;
 #pragma unroll
         for (int src = 0; src < S; ++src) {
-          float v;
+          float vh, vl;
           if (src == static_cast<int>(split)) {
-            v = select(acc, static_cast<int>(split) * kShard + jj);
+            vh = 0.0f;
+            vl = 0.0f;
+#pragma unroll
+            for (int q = 0; q < kRows; ++q)
+              if (q == static_cast<int>(split) * kShard + jj) {
+                vh = hi[q];
+                vl = lo[q];
+              }
           } else {
             const int sidx = src < static_cast<int>(split) ? src : src - 1;
-            v = recv[(sidx * kShard + jj) * kBlockN + col];
+            const float* pair = recv + ((sidx * kShard + jj) * kBlockN + col) * 2;
+            vh = pair[0];
+            vl = pair[1];
           }
-          total = (src == 0) ? v : total + v;  // K-slice order, on every CTA
+          two_sum_add(sh, sl, vh);
+          sl = __fadd_rn(sl, vl);
         }
-        owned[jj] = total;
+        owned[jj] = static_cast<double>(sh) + static_cast<double>(sl);
       }
     } else {
 #pragma unroll
-      for (int jj = 0; jj < kShard; ++jj) owned[jj] = acc[jj];
+      for (int jj = 0; jj < kShard; ++jj)
+        owned[jj] = static_cast<double>(hi[jj]) + static_cast<double>(lo[jj]);
     }
 
     uint16_t* ctile = reinterpret_cast<uint16_t*>(smem + L.ctile);  // [kShard][128]
 #pragma unroll
-    for (int jj = 0; jj < kShard; ++jj) ctile[jj * kBlockN + col] = bf16_bits_rn(owned[jj]);
+    for (int jj = 0; jj < kShard; ++jj)
+      ctile[jj * kBlockN + col] = bf16_bits_from_double(owned[jj]);
     epilogue_barrier();
 
     const uint32_t g = misc[1];
@@ -346,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, p.tmem_cols);
+    ptx::tmem_dealloc(tmem, p.tmem.cols);
   }
 }
 
@@ -370,6 +468,30 @@ __global__ void relayout_w_scales_kernel(const uint8_t* __restrict__ w_scale,
     const int row = tile * kBlockN + r1 * 32 + r0;
     const int blk = kt * kSfPerTile + b;
     w_sf[idx] = blk < kblocks ? w_scale[static_cast<size_t>(row) * kblocks + blk] : 127;
+  }
+}
+
+// W [n][k] -> [n/128][k_tiles][16384]: each 16 KB block is the shared-memory
+// image of one 128-row x 128-byte tile in the 128-byte swizzle (row r at byte
+// r * 128, its 16-byte chunk c at position c ^ (r % 8)), so one bulk copy
+// lands it exactly as a swizzled TMA box would.  Bytes past K are zero.
+__global__ void tile_weights_kernel(const uint8_t* __restrict__ w, uint8_t* __restrict__ w_tiled,
+                                    int n, int k, int k_tiles) {
+  const size_t chunks = static_cast<size_t>(n / kBlockN) * k_tiles * (kWTileBytes / 16);
+  for (size_t q = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; q < chunks;
+       q += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t block = q / (kWTileBytes / 16);
+    const int within = static_cast<int>(q % (kWTileBytes / 16));
+    const int tile = static_cast<int>(block / k_tiles);
+    const int kt = static_cast<int>(block % k_tiles);
+    const int r = within / 8;
+    const int position = within % 8;
+    const int c = position ^ (r & 7);
+    const int k0 = kt * kTileK + c * 16;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (k0 < k)
+      v = *reinterpret_cast<const uint4*>(w + static_cast<size_t>(tile * kBlockN + r) * k + k0);
+    reinterpret_cast<uint4*>(w_tiled)[q] = v;
   }
 }
 
@@ -408,25 +530,25 @@ GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split) {
   L.ctile = L.sfa + stages * kSfChunkBytes;
   L.recv = L.ctile + kRows * kBlockN * 2;
   const uint32_t recv_bytes =
-      split_k > 1 ? static_cast<uint32_t>((split_k - 1) * (kRows / split_k) * kBlockN * 4) : 0u;
+      split_k > 1 ? static_cast<uint32_t>((split_k - 1) * (kRows / split_k) * kBlockN * 8) : 0u;
   L.sx = L.recv + recv_bytes;
   const uint32_t sx_bytes = static_cast<uint32_t>(tiles_per_split * 128 + 384);
   L.bars = (L.sx + sx_bytes + 7u) & ~7u;
-  L.misc = L.bars + static_cast<uint32_t>(2 * stages + 3) * 8u;
+  L.misc = L.bars + static_cast<uint32_t>(2 * stages + 2 * kAccRing + 2) * 8u;
   L.total = L.misc + 16u + 1024u;
   return L;
 }
 
-uint32_t gemm_tmem_columns(int stages, int tiles_per_split, uint32_t* sfb_col, uint32_t* sfa_col) {
-  (void)tiles_per_split;
-  const uint32_t sfa = 8u;
-  const uint32_t sfb = sfa + 4u * static_cast<uint32_t>(stages);
-  const uint32_t used = sfb + 4u * static_cast<uint32_t>(stages);
-  uint32_t cols = 32;
-  while (cols < used) cols <<= 1;
-  if (sfb_col) *sfb_col = sfb;
-  if (sfa_col) *sfa_col = sfa;
-  return cols;
+TmemPlan gemm_tmem_plan(int stages, int acc_blocks) {
+  TmemPlan t{};
+  t.acc = 0;
+  t.acc_slot = acc_blocks == 1 ? static_cast<uint32_t>(kSfPerTile * kRows) : kRows;
+  t.sfa = t.acc + t.acc_slot * kAccRing;
+  t.sfb = t.sfa + 4u * static_cast<uint32_t>(stages);
+  const uint32_t used = t.sfb + 4u * static_cast<uint32_t>(stages);
+  t.cols = 32;
+  while (t.cols < used) t.cols <<= 1;
+  return t;
 }
 
 cudaError_t set_gemm_smem_attribute(int split_k, int bytes) {
@@ -457,6 +579,16 @@ cudaError_t launch_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
     default:
       return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_tile_weights(const uint8_t* w, uint8_t* w_tiled, int n, int k,
+                                cudaStream_t stream) {
+  const int k_tiles = (k + kTileK - 1) / kTileK;
+  const size_t chunks = static_cast<size_t>(n / kBlockN) * k_tiles * (kWTileBytes / 16);
+  const int threads = 256;
+  const int blocks = static_cast<int>(std::min<size_t>((chunks + threads - 1) / threads, 8192));
+  tile_weights_kernel<<<blocks, threads, 0, stream>>>(w, w_tiled, n, k, k_tiles);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_relayout_w_scales(const uint8_t* w_scale, uint8_t* w_sf, int n, int k,

@@ -10,3 +10,18 @@ if str(ROOT) not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line(
         "markers", "gpu: needs a CUDA GPU (sm_103a); compares the CUDA path with the oracle")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(scope="session")
+def cuda():
+    """The CUDA device, with the library built; GPU tests fail loudly without one."""
+    import torch
+
+    from mxfp8_gemm_mailbox_gb300 import build
+
+    assert torch.cuda.is_available(), "the -m gpu tests need a CUDA GPU (sm_103a)"
+    build.build()
+    return torch.device("cuda")

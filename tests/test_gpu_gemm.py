@@ -1,0 +1,218 @@
+"""GPU parity of the publishing GEMM against the oracle, element by element,
+at sizes the oracle finishes in seconds: several tiles, ragged K, every m,
+every split-K cluster size, integer-valued inputs (bit-exact), N(0, 1)
+inputs (within 2 BF16 ULPs), the mailbox between GEMM and consume, the
+negative-zero clearing, and the fused vs unfused equivalence."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from mxfp8_gemm_mailbox_gb300 import ERR_STATE, OK, Mailbox, Mxfp8Error, PublishGemm
+from mxfp8_gemm_mailbox_gb300._lib import W_IN_PLACE, W_TILED
+from tests.gpu_util import (assert_bf16_close, bits, dev, mailbox_words, pack_words, sanitized,
+                            state_words)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_chain(w, ws, x, xs, split_k, capacity=8, stages=0, mailbox=None, acc_blocks=0,
+              w_layout=0):
+    """GEMM (C requested) -> snapshot of mailbox + state -> consume.  Returns
+    (C bits, mailbox words between the two kernels, state then, out bits,
+    mailbox words after, state after, handle config)."""
+    n = w.shape[0]
+    m = x.shape[0]
+    mb = mailbox or Mailbox(capacity, n)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=split_k, stages=stages, acc_blocks=acc_blocks,
+                    w_layout=w_layout)
+    c = torch.full((m, n), 0x7FFF, dtype=torch.int16, device="cuda")
+    g.run(dev(x), dev(xs), c)
+    torch.cuda.synchronize()
+    between = mailbox_words(mb).copy()
+    state_between = state_words(mb)
+    out = mb.consume(m)
+    torch.cuda.synchronize()
+    cfg = g.config()
+    g.close()
+    return (bits(c), between, state_between, bits(out), mailbox_words(mb).copy(),
+            state_words(mb), cfg)
+
+
+def check_published(between, state_between, c_bits, capacity, n, generation=0):
+    m = c_bits.shape[0]
+    assert state_between[1] == generation
+    expect = np.full((3, capacity, n // 2), oracle.SENTINEL, np.uint32)
+    expect[generation, :m] = pack_words(sanitized(c_bits))
+    assert (between == expect).all(), "mailbox between GEMM and consume"
+    lo, hi = between & 0xFFFF, between >> 16
+    pub = between[generation, :m]
+    assert not (pub == oracle.SENTINEL).any()
+    assert not ((pub & 0xFFFF) == 0x8000).any() and not ((pub >> 16) == 0x8000).any()
+    del lo, hi
+
+
+@pytest.mark.parametrize("w_layout", [W_IN_PLACE, W_TILED])
+@pytest.mark.parametrize("split_k", [1, 2, 4])
+@pytest.mark.parametrize("n,k,m", [(128, 128, 1), (384, 1024, 8), (256, 2048, 5), (512, 4096, 3),
+                                   (128, 96, 2), (256, 160, 7), (128, 32, 8), (256, 1152, 4)])
+def test_integer_inputs_bit_exact(cuda, n, k, m, split_k, w_layout):
+    w, ws, x, xs = synthetic.integer_operands(n, k, m, seed=n + k + m)
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    c, between, sb, out, after, state, cfg = run_chain(w, ws, x, xs, split_k, w_layout=w_layout)
+    assert cfg["split_k"] == split_k
+    assert cfg["w_layout"] == {W_IN_PLACE: "in_place", W_TILED: "tiled"}[w_layout]
+    assert (c == want).all(), f"{int((c != want).sum())} of {c.size} differ"
+    check_published(between, sb, c, 8, n)
+    assert (out == sanitized(c)).all()
+    assert (after == oracle.SENTINEL).all()
+    assert state == [1, 0, 0, 0]
+
+
+@pytest.mark.parametrize("w_layout", [W_IN_PLACE, W_TILED])
+@pytest.mark.parametrize("split_k", [1, 2, 4])
+@pytest.mark.parametrize("n,k,m,lo,hi", [(256, 256, 1, -3, 3), (1024, 4096, 8, -4, 2),
+                                         (640, 2048, 6, -6, 3), (384, 8192, 4, -4, 2),
+                                         (256, 1056, 3, -4, 2)])
+def test_normal_inputs_within_two_ulps(cuda, n, k, m, lo, hi, split_k, w_layout):
+    wl = synthetic.Workload("p", n, k, m, split_k, exp_lo=lo, exp_hi=hi, x_zero_fraction=0.01,
+                            seed=7 * n + k + m)
+    w, ws = synthetic.make_weights(wl)
+    x, xs = synthetic.make_activations(wl)
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    c, between, sb, out, after, state, _ = run_chain(w, ws, x, xs, split_k, w_layout=w_layout)
+    assert_bf16_close(c, want, f"N={n} K={k} m={m} S={split_k}")
+    check_published(between, sb, c, 8, n)
+    assert (out == sanitized(c)).all()
+    assert (after == oracle.SENTINEL).all()
+
+
+def test_split_k_results_agree(cuda):
+    wl = synthetic.Workload("s", 512, 4096, 8, exp_lo=-4, exp_hi=2, seed=3)
+    w, ws = synthetic.make_weights(wl)
+    x, xs = synthetic.make_activations(wl)
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    results = [run_chain(w, ws, x, xs, s)[0] for s in (1, 2, 4)]
+    for r in results:
+        assert_bf16_close(r, want)
+    wi, wsi, xi, xsi = synthetic.integer_operands(512, 4096, 8, seed=4)
+    ints = [run_chain(wi, wsi, xi, xsi, s)[0] for s in (1, 2, 4)]
+    assert (ints[0] == ints[1]).all() and (ints[0] == ints[2]).all()
+
+
+@pytest.mark.parametrize("stages", [2, 3, 7, 12])
+def test_every_ring_depth(cuda, stages):
+    w, ws, x, xs = synthetic.integer_operands(256, 4096, 8, seed=stages)
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    c, *_, cfg = run_chain(w, ws, x, xs, 1, stages=stages)
+    assert cfg["stages"] == stages
+    assert (c == want).all()
+
+
+def test_ring_too_deep_for_shared_memory_is_refused(cuda):
+    w, ws, x, xs = synthetic.integer_operands(256, 4096, 8, seed=1)
+    with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED"):
+        PublishGemm(dev(w), dev(ws), Mailbox(8, 256), split_k=1, stages=16)
+
+
+@pytest.mark.parametrize("acc_blocks", [1, 4])
+@pytest.mark.parametrize("split_k", [1, 4])
+def test_accumulation_granularity(cuda, acc_blocks, split_k):
+    w, ws, x, xs = synthetic.integer_operands(512, 4096, 8, seed=17)
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    c, between, sb, out, after, state, cfg = run_chain(w, ws, x, xs, split_k,
+                                                      acc_blocks=acc_blocks)
+    assert cfg["acc_blocks"] == acc_blocks
+    assert (c == want).all()
+    check_published(between, sb, c, 8, 512)
+    assert (out == sanitized(c)).all()
+
+
+def test_negative_zero_is_cleared_in_the_mailbox_only(cuda):
+    # Tiny negative sums round to -0 in BF16 (-2^-136 below half the smallest
+    # subnormal); other rows are exactly +0 / -0 products.
+    n, k, m = 256, 64, 4
+    w = np.full((n, k), 0x38, np.uint8)
+    ws = np.full((n, k // 32), 0x01, np.uint8)       # 2^-126
+    x = np.full((m, k), 0xB8, np.uint8)              # -1
+    xs = np.full((m, k // 32), 0x70, np.uint8)       # 2^-15
+    w[128:] = 0x80                                   # -0 weights
+    x[3] = 0x00
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    c, between, sb, out, after, state, _ = run_chain(w, ws, x, xs, 1)
+    assert_bf16_close(c, want)
+    pub = between[0, :m]
+    assert not ((pub & 0xFFFF) == 0x8000).any() and not ((pub >> 16) == 0x8000).any()
+    assert (out == sanitized(c)).all()
+    assert not (out == 0x8000).any()
+
+
+def test_capacity_and_row_limits(cuda):
+    w, ws, x, xs = synthetic.integer_operands(128, 256, 3, seed=1)
+    mb = Mailbox(3, 128)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=1)
+    g.precompile(3)
+    with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED"):
+        g.precompile(4)
+    x4 = dev(np.zeros((4, 256), np.uint8))
+    with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED"):
+        g.run(x4, dev(np.full((4, 8), 127, np.uint8)))
+    c = torch.empty((3, 128), dtype=torch.int16, device="cuda")
+    g.run(dev(x), dev(xs), c)
+    out = mb.consume(3)
+    torch.cuda.synchronize()
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    assert (bits(c) == want).all() and (bits(out) == sanitized(want)).all()
+    assert mb.status()[0] == OK
+
+
+def test_fused_equals_unfused_bit_for_bit(cuda):
+    # The unfused path: the GEMM writes only C, the standalone publish kernel
+    # reads it back; mailbox and consumer output must match the fused epilogue.
+    wl = synthetic.Workload("u", 1024, 2048, 7, 2, exp_lo=-6, exp_hi=3, signed_pairs=True, seed=11)
+    w, ws = synthetic.make_weights(wl)
+    x, xs = synthetic.make_activations(wl)
+    W, WS, X, XS = dev(w), dev(ws), dev(x), dev(xs)
+    fused_mb, unfused_mb = Mailbox(8, 1024), Mailbox(8, 1024)
+    gf = PublishGemm(W, WS, fused_mb, split_k=2)
+    gu = PublishGemm(W, WS, unfused_mb, split_k=2)
+    for call in range(4):  # walk the generations
+        cf = torch.empty((7, 1024), dtype=torch.int16, device="cuda")
+        cu = torch.empty((7, 1024), dtype=torch.int16, device="cuda")
+        gf.run(X, XS, cf)
+        gu.run_unfused(X, XS, cu)
+        unfused_mb.publish(cu)
+        torch.cuda.synchronize()
+        assert (bits(cf) == bits(cu)).all()
+        assert (mailbox_words(fused_mb) == mailbox_words(unfused_mb)).all()
+        assert state_words(fused_mb) == state_words(unfused_mb)
+        of = fused_mb.consume(7)
+        ou = unfused_mb.consume(7)
+        torch.cuda.synchronize()
+        assert (bits(of) == bits(ou)).all()
+        assert state_words(fused_mb) == state_words(unfused_mb) == [(call + 1) % 3, call % 3, 0, 0]
+    assert_bf16_close(bits(cf), oracle.gemm_bf16(w, ws, x, xs))
+
+
+def test_publish_without_c(cuda):
+    w, ws, x, xs = synthetic.integer_operands(256, 512, 8, seed=2)
+    mb = Mailbox(8, 256)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=2)
+    g.run(dev(x), dev(xs), None)
+    out = mb.consume(8)
+    torch.cuda.synchronize()
+    assert (bits(out) == sanitized(oracle.gemm_bf16(w, ws, x, xs))).all()
+
+
+def test_bad_next_generation_is_flagged(cuda):
+    w, ws, x, xs = synthetic.integer_operands(128, 256, 2, seed=5)
+    mb = Mailbox(8, 128)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=1)
+    mb.state[0] = 4
+    c = torch.empty((2, 128), dtype=torch.int16, device="cuda")
+    g.run(dev(x), dev(xs), c)
+    torch.cuda.synchronize()
+    assert (mailbox_words(mb) == oracle.SENTINEL).all()  # no publish into a bad generation
+    assert (bits(c) == oracle.gemm_bf16(w, ws, x, xs)).all()  # C is still written
+    assert mb.status()[0] == ERR_STATE
