@@ -19,7 +19,7 @@ constexpr int kGenerations = 3;
 constexpr uint32_t kSentinel = 0x80000000u;
 constexpr int kMaxStages = 16;
 constexpr int kMaxTilesPerSplit = 256;
-constexpr int kAccRing = 4;       // accumulator slots in tensor memory (in stages)
+constexpr int kMaxAccRing = 8;    // accumulator slots in tensor memory (one stage each)
 
 // Byte offsets inside the GEMM's dynamic shared memory (after aligning the
 // base to 1024 bytes), computed once on the host.
@@ -27,9 +27,9 @@ struct GemmSmemLayout {
   uint32_t w;         // stages x 16 KB W tiles
   uint32_t x;         // stages x 1 KB activation tiles
   uint32_t sfa;       // stages x 512 B W scale chunks
-  uint32_t ctile;     // 8 x 128 BF16 epilogue staging
-  uint32_t recv;      // split-K partials received from peers
-  uint32_t sx;        // x scale words of this CTA's K range
+  uint32_t ctile;     // 8 x 128 BF16 epilogue staging (inside the dead W ring)
+  uint32_t recv;      // split-K partials received from peers (inside the dead W ring)
+  uint32_t sx;        // x scale chunks of this CTA's K range
   uint32_t bars;      // mbarriers
   uint32_t misc;      // tensor-memory base, generation broadcast
   uint32_t total;     // bytes including the alignment slack
@@ -41,6 +41,7 @@ struct TmemPlan {
   uint32_t cols;       // allocated (a power of two >= 32)
   uint32_t acc;        // first accumulator column
   uint32_t acc_slot;   // columns per accumulator slot (one stage of MMAs)
+  uint32_t acc_ring;   // accumulator slots
   uint32_t sfa;        // first column of the W scale ring
   uint32_t sfb;        // first column of the x scale ring
 };

@@ -52,17 +52,16 @@ __global__ void __launch_bounds__(kConsumeThreads)
     mailbox_consume_kernel(uint16_t* __restrict__ mailbox, int32_t* __restrict__ state,
                            int capacity, int n, int m, uint16_t* __restrict__ out,
                            uint64_t timeout_ns) {
-  __shared__ uint32_t shared_generation;
   // The next kernel may launch now (its own grid wait covers this grid); the
   // GEMM (or publish kernel) before this one has completed and its stores
   // are visible after the grid wait.
   ptx::launch_dependents();
   ptx::grid_dependency_wait();
+  // The active generation is written only by the publisher, so every thread
+  // reads it; thread 0 of each CTA also counts the CTA in, and the last CTA
+  // to arrive advances the next generation and clears the count.
+  const uint32_t g = ptx::ld_volatile_u32(state + 1);
   if (threadIdx.x == 0) {
-    // One read of the generation per CTA, before the CTA counts itself, so
-    // the last CTA may advance it while the others still run.
-    const uint32_t g = ptx::ld_volatile_u32(state + 1);
-    shared_generation = g;
     const uint32_t before = ptx::atom_add_acq_rel(state + 2, 1u);
     if (before == gridDim.x - 1) {
       if (g < static_cast<uint32_t>(kGenerations)) {
@@ -73,8 +72,6 @@ __global__ void __launch_bounds__(kConsumeThreads)
       state[2] = 0;
     }
   }
-  __syncthreads();
-  const uint32_t g = shared_generation;
   if (g >= static_cast<uint32_t>(kGenerations)) return;  // nothing to address
 
   const int packs_per_row = n / 8;

@@ -29,7 +29,7 @@
 //               tokens) and folded into the compensated sums, split-K
 //               exchange, BF16 rounding, C store, publish.
 //
-// Tensor-memory columns: [acc, +4 * acc_slot) the accumulator ring (FP32,
+// Tensor-memory columns: [acc, +acc_ring * acc_slot) the accumulator ring (FP32,
 // lane = output column, column = block * 8 + token); then the W and x scale
 // rings, one 4-column slot per stage each, filled by tcgen05.cp (32x128b,
 // multicast to the four lane quarters) from 16-byte-row scale chunks in
@@ -119,6 +119,19 @@ __device__ __forceinline__ uint16_t bf16_bits_from_double(double v) {
   return static_cast<uint16_t>(sign | static_cast<uint32_t>(q));  // q == 128 is 2^-126
 }
 
+// Position in a ring of mbarrier-guarded slots: the slot and the parity of
+// its current use, advanced without divisions in the hot loops.
+struct RingCursor {
+  int slot;
+  uint32_t phase;
+  __device__ __forceinline__ void next(int size) {
+    if (++slot == size) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 template <int S>
 __global__ void __launch_bounds__(kThreads, 1)
     publish_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
@@ -143,9 +156,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t bar_full = sbase + L.bars;                     // [stages]
   const uint32_t bar_empty = bar_full + 8u * stages;            // [stages]
-  const uint32_t bar_acc_full = bar_empty + 8u * stages;        // [kAccRing]
-  const uint32_t bar_acc_empty = bar_acc_full + 8u * kAccRing;  // [kAccRing]
-  const uint32_t bar_sfb = bar_acc_empty + 8u * kAccRing;
+  const int acc_ring = static_cast<int>(p.tmem.acc_ring);
+  const uint32_t bar_acc_full = bar_empty + 8u * stages;          // [acc_ring]
+  const uint32_t bar_acc_empty = bar_acc_full + 8u * kMaxAccRing;  // [acc_ring]
+  const uint32_t bar_sfb = bar_acc_empty + 8u * kMaxAccRing;
   const uint32_t bar_recv = bar_sfb + 8u;
   uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L.misc);  // [0] tmem base, [1] generation
 
@@ -156,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar_full + 8u * s, 1);
       ptx::mbar_init(bar_empty + 8u * s, 1);
     }
-    for (int r = 0; r < kAccRing; ++r) {
+    for (int r = 0; r < acc_ring; ++r) {
       ptx::mbar_init(bar_acc_full + 8u * r, 1);
       ptx::mbar_init(bar_acc_empty + 8u * r, 128);
     }
@@ -210,10 +224,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_2d(sbase + L.x + i * kXTileBytes, &tmap_x, (kt_begin + i) * kTileK, 0,
                          bar_full + 8u * i, pol_keep);
       int issued = npre;
-      for (int i = npre; i < nkt; ++i) {
-        const int s = i % stages;
-        const uint32_t use = static_cast<uint32_t>(i / stages);
-        if (!ptx::mbar_wait(bar_empty + 8u * s, (use - 1u) & 1u, p.wait_limit_ns)) {
+      // From here every slot is on its second or later use: wait until the
+      // MMAs of its previous use released it.
+      RingCursor ring{0, 1u};
+      for (int i = npre; i < nkt; ++i, ring.next(stages)) {
+        const int s = ring.slot;
+        if (!ptx::mbar_wait(bar_empty + 8u * s, ring.phase ^ 1u, p.wait_limit_ns)) {
           raise_flag(p.state, 0x2u);
           break;
         }
@@ -243,14 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) raise_flag(p.state, 0x2u);
         ptx::tc_fence_after();
       }
-      for (int i = 0; i < nkt && ok; ++i) {
-        const int s = i % stages;
-        const int r = i % kAccRing;
-        if (!ptx::mbar_wait(bar_full + 8u * s, static_cast<uint32_t>(i / stages) & 1u,
-                            p.wait_limit_ns) ||
-            (i >= kAccRing &&
-             !ptx::mbar_wait(bar_acc_empty + 8u * r,
-                             (static_cast<uint32_t>(i / kAccRing) - 1u) & 1u, p.wait_limit_ns))) {
+      RingCursor stage{0, 0u}, acc{0, 0u};
+      for (int i = 0; i < nkt && ok; ++i, stage.next(stages), acc.next(acc_ring)) {
+        const int s = stage.slot;
+        const int r = acc.slot;
+        if (!ptx::mbar_wait(bar_full + 8u * s, stage.phase, p.wait_limit_ns) ||
+            (i >= acc_ring &&
+             !ptx::mbar_wait(bar_acc_empty + 8u * r, acc.phase ^ 1u, p.wait_limit_ns))) {
           raise_flag(p.state, 0x2u);
           ok = false;
           break;
@@ -276,6 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit(bar_acc_full + 8u * r);
       }
     }
+  }
+  if (warp < 2) {
+    __syncwarp();
+    if (S > 1) ptx::cluster_sync();  // matches the epilogue's barrier before the exchange
   } else {
     // ------------------------------------------------------------- epilogue
     const int etid = tid - 64;               // 0..127
@@ -286,24 +305,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (etid == 0) misc[1] = ptx::ld_volatile_u32(p.state + 0);
 
     // x scales of this CTA's K range as one 128-byte chunk per K tile: row r
-    // (< 8) of tile j at byte j * 128 + r * 16, its four E8M0 codes first.
-    // Rows >= m and blocks past K take 127 (a scale of 1; those x elements
-    // are zero).  The copy of a chunk reads 32 rows; rows 8..31 (the next
-    // chunks, or the zero tail) feed no output column.
+    // (< 8) of tile j at byte j * 128 + r * 16, its four E8M0 codes first and
+    // 12 zero bytes after.  Rows >= m and blocks past K take 127 (a scale of
+    // 1; those x elements are zero).  The copy of a chunk reads 32 rows; rows
+    // 8..31 (the next chunks, or the tail) feed no output column.  Each thread
+    // issues all its loads before any store, so the staging costs one L2 trip.
     uint8_t* sx = smem + L.sx;
     const int kblocks = p.k / 32;
-    const int sx_bytes = p.tiles_per_split * 128 + 384;
-    for (int b = etid; b < sx_bytes; b += 128) {
-      const int j = b / 128;
-      const int r = (b % 128) / 16;
-      const int q = b % 16;
-      uint8_t v = 0;
-      if (q < kSfPerTile && j < nkt) {
-        const int kb = (kt_begin + j) * kSfPerTile + q;
-        v = 127;
-        if (r < p.m && kb < kblocks) v = p.x_scale[static_cast<size_t>(r) * kblocks + kb];
+    const int words = kRows * nkt;
+    constexpr int kMaxWords = kRows * kMaxTilesPerSplit / 128;  // per thread
+#pragma unroll
+    for (int it = 0; it < kMaxWords; ++it) {
+      const int w = etid + it * 128;
+      if (w >= words) break;
+      const int r = w / nkt;
+      const int j = w - r * nkt;
+      uint32_t v = 0x7F7F7F7Fu;
+      if (r < p.m) {
+        const int kb0 = (kt_begin + j) * kSfPerTile;
+        const uint8_t* row = p.x_scale + static_cast<size_t>(r) * kblocks;
+        uint32_t b[kSfPerTile];
+#pragma unroll
+        for (int q = 0; q < kSfPerTile; ++q) b[q] = kb0 + q < kblocks ? row[kb0 + q] : 127u;
+        v = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
       }
-      sx[b] = v;
+      *reinterpret_cast<uint4*>(sx + j * 128 + r * 16) = make_uint4(v, 0u, 0u, 0u);
     }
     ptx::fence_proxy_async_smem();  // the tensor-memory copy reads them
     ptx::mbar_arrive(bar_sfb);
@@ -312,10 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float hi[kRows], lo[kRows];
 #pragma unroll
     for (int t = 0; t < kRows; ++t) hi[t] = lo[t] = 0.0f;
-    for (int i = 0; i < nkt; ++i) {
-      const int r = i % kAccRing;
-      if (!ptx::mbar_wait(bar_acc_full + 8u * r, static_cast<uint32_t>(i / kAccRing) & 1u,
-                          p.wait_limit_ns)) {
+    RingCursor acc{0, 0u};
+    for (int i = 0; i < nkt; ++i, acc.next(acc_ring)) {
+      const int r = acc.slot;
+      if (!ptx::mbar_wait(bar_acc_full + 8u * r, acc.phase, p.wait_limit_ns)) {
         raise_flag(p.state, 0x2u);
         break;
       }
@@ -350,6 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kShard = kRows / S;
     double owned[kShard];
     if constexpr (S > 1) {
+      // The receive buffer lives in the W ring, which is dead only once every
+      // CTA of the cluster has finished its main loop.
+      ptx::cluster_sync();
       if (etid == 0)
         ptx::mbar_arrive_expect_tx(bar_recv,
                                    static_cast<uint32_t>((S - 1) * kShard * kBlockN * 8));
@@ -523,18 +552,22 @@ cudaError_t launch_impl(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, co
 }  // namespace
 
 GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split) {
+  (void)split_k;
   GemmSmemLayout L{};
   L.w = 0;
   L.x = L.w + stages * kWTileBytes;
   L.sfa = L.x + stages * kXTileBytes;
-  L.ctile = L.sfa + stages * kSfChunkBytes;
-  L.recv = L.ctile + kRows * kBlockN * 2;
-  const uint32_t recv_bytes =
-      split_k > 1 ? static_cast<uint32_t>((split_k - 1) * (kRows / split_k) * kBlockN * 8) : 0u;
-  L.sx = L.recv + recv_bytes;
+  // Written only after the main loop: the epilogue's BF16 tile in W stage 0,
+  // the split-K partials from peers ((S-1) x 8/S x 128 x 8 bytes <= 6 KB) in
+  // W stage 1 (every ring has at least two stages).
+  L.ctile = L.w;
+  L.recv = L.w + kWTileBytes;
+  // One 128-byte x scale chunk per K tile, plus the 384 bytes the copy of the
+  // last chunk reads past it (rows that feed no output column).
+  L.sx = L.sfa + stages * kSfChunkBytes;
   const uint32_t sx_bytes = static_cast<uint32_t>(tiles_per_split * 128 + 384);
   L.bars = (L.sx + sx_bytes + 7u) & ~7u;
-  L.misc = L.bars + static_cast<uint32_t>(2 * stages + 2 * kAccRing + 2) * 8u;
+  L.misc = L.bars + static_cast<uint32_t>(2 * stages + 2 * kMaxAccRing + 2) * 8u;
   L.total = L.misc + 16u + 1024u;
   return L;
 }
@@ -543,7 +576,8 @@ TmemPlan gemm_tmem_plan(int stages, int acc_blocks) {
   TmemPlan t{};
   t.acc = 0;
   t.acc_slot = acc_blocks == 1 ? static_cast<uint32_t>(kSfPerTile * kRows) : kRows;
-  t.sfa = t.acc + t.acc_slot * kAccRing;
+  t.acc_ring = acc_blocks == 1 ? 4u : static_cast<uint32_t>(kMaxAccRing);
+  t.sfa = t.acc + t.acc_slot * t.acc_ring;
   t.sfb = t.sfa + 4u * static_cast<uint32_t>(stages);
   const uint32_t used = t.sfb + 4u * static_cast<uint32_t>(stages);
   t.cols = 32;
