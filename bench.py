@@ -291,18 +291,39 @@ def run_ours(args):
     us_per_call = seconds / steps * 1e6
     value = bytes_all / seconds / 1e9
 
-    # The dominant kernel alone: CUDA events around each GEMM launch.
-    n_gemm = min(2000, steps)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_gemm)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_gemm)]
+    # The dominant kernel, the publishing GEMM: launched back to back from a
+    # CUDA graph of GRAPH_STEPS launches over the same rotating weights, with
+    # its publish switched off (the same kernel; the mailbox protocol needs a
+    # consume after every publish), between CUDA events on its stream.
+    cbuf = torch.empty((wl.m, wl.n), dtype=torch.bfloat16, device=device)
+    gemm_graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
-        for i in range(n_gemm):
+        with torch.cuda.graph(gemm_graph, stream=stream):
+            for i in range(GRAPH_STEPS):
+                gemms[i % WEIGHT_COPIES].run_unfused(X, XS, cbuf)
+        for _ in range(warm):
+            gemm_graph.replay()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(replays):
+            gemm_graph.replay()
+        g1.record(stream)
+    stream.synchronize()
+    gemm_us = g0.elapsed_time(g1) * 1e3 / steps
+    # The same kernel launched alone (events around each launch: no overlap
+    # with its neighbours, so launch and ramp-up are included).
+    n_iso = min(300, steps)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_iso)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_iso)]
+    with torch.cuda.stream(stream):
+        for i in range(n_iso):
             starts[i].record(stream)
             gemms[i % WEIGHT_COPIES].run(X, XS)
             ends[i].record(stream)
             mb.consume(wl.m, out)
     stream.synchronize()
-    gemm_us = statistics.mean(s.elapsed_time(e) * 1e3 for s, e in zip(starts, ends))
+    iso_us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in zip(starts, ends))
     peak, peak_kind = measured_peak()
     achieved = wl.weight_bytes / (gemm_us * 1e-6) / 1e9
 
@@ -382,6 +403,8 @@ def run_ours(args):
                 "traffic": traffic,
                 "algorithmic_bytes_per_launch": wl.weight_bytes,
                 "launch_us": round(gemm_us, 3),
+                "launch_timing": f"{GRAPH_STEPS} back-to-back launches per CUDA graph, publish off",
+                "isolated_launch_us": round(iso_us, 3),
             },
             "cpu_baseline": cpu,
             "e2e": {
@@ -393,6 +416,8 @@ def run_ours(args):
                 "d2h_bytes_per_step": int(out.numel() * out.element_size()),
             },
             "gpu_launches": 2 * steps,
+            "tactic": {k: cfg[k] for k in ("split_k", "stages", "acc_blocks", "w_layout",
+                                            "l2_prefetch", "tmem_columns")},
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)

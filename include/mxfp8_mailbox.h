@@ -81,6 +81,8 @@ typedef struct mxfp8_gemm_desc {
   int32_t stages;     /* shared-memory ring depth: 2..16 (0 = choose)                */
   int32_t acc_blocks; /* K blocks per promoted partial sum: 1 or 4 (0 = 4)           */
   int32_t w_layout;   /* MXFP8_W_IN_PLACE or MXFP8_W_TILED (0 = choose)              */
+  int32_t l2_prefetch;/* W stages past the ring each CTA warms in L2 before its grid
+                         wait: 0..64 (0 = none, the measured best on GB300)           */
 } mxfp8_gemm_desc;
 
 /* Where the GEMM streams W from.  IN_PLACE: the caller's [N][K] buffer,

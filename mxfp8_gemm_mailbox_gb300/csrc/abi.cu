@@ -110,6 +110,8 @@ mxfp8_status check_desc(const mxfp8_gemm_desc* d) {
     return fail(MXFP8_ERR_UNSUPPORTED, "acc_blocks must be 1 or 4 (or 0 to choose)");
   if (d->w_layout != 0 && d->w_layout != MXFP8_W_IN_PLACE && d->w_layout != MXFP8_W_TILED)
     return fail(MXFP8_ERR_UNSUPPORTED, "w_layout must be MXFP8_W_IN_PLACE or MXFP8_W_TILED");
+  if (d->l2_prefetch < 0 || d->l2_prefetch > 64)
+    return fail(MXFP8_ERR_UNSUPPORTED, "l2_prefetch must be in 0..64");
   return MXFP8_OK;
 }
 
@@ -214,6 +216,7 @@ mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale,
   p.capacity = g->desc.capacity_m;
   p.publish = publish ? 1 : 0;
   p.acc_blocks = g->desc.acc_blocks;
+  p.l2_prefetch = g->desc.l2_prefetch;
   p.tmem = g->tmem;
   p.x_scale = static_cast<const uint8_t*>(x_scale);
   p.w_sf = g->w_sf;

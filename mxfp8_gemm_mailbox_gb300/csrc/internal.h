@@ -54,6 +54,7 @@ struct GemmParams {
   int32_t capacity;
   int32_t publish;          // 1: fused publish into the mailbox; 0: C only
   int32_t acc_blocks;       // 32-wide K blocks summed in TMEM per promoted partial: 1 or 4
+  int32_t l2_prefetch;      // stages past the ring warmed in L2 before the grid wait
   TmemPlan tmem;
   const uint8_t* x_scale;   // [m][k/32]
   const uint8_t* w_sf;      // [n/128][k_tiles][512] tiled W scales

@@ -59,8 +59,23 @@ __global__ void __launch_bounds__(kConsumeThreads)
   ptx::grid_dependency_wait();
   // The active generation is written only by the publisher, so every thread
   // reads it; thread 0 of each CTA also counts the CTA in, and the last CTA
-  // to arrive advances the next generation and clears the count.
+  // to arrive advances the next generation and clears the count.  Each
+  // thread loads its pack from all three generations alongside the state
+  // word (one memory round trip instead of two) and keeps the active one.
+  const int packs_per_row = n / 8;
+  const int pack = blockIdx.x * kConsumeThreads + threadIdx.x;
+  const bool active = pack < m * packs_per_row;
+  const int t = active ? pack / packs_per_row : 0;
+  const int c8 = active ? pack % packs_per_row : 0;
+  const size_t generation_stride = static_cast<size_t>(capacity) * n;
+  uint16_t* slot0 = mailbox + static_cast<size_t>(t) * n + c8 * 8;
   const uint32_t g = ptx::ld_volatile_u32(state + 1);
+  uint4 candidates[kGenerations];
+  if (active) {
+#pragma unroll
+    for (int gg = 0; gg < kGenerations; ++gg)
+      candidates[gg] = ptx::ld_volatile_v4(slot0 + gg * generation_stride);
+  }
   if (threadIdx.x == 0) {
     const uint32_t before = ptx::atom_add_acq_rel(state + 2, 1u);
     if (before == gridDim.x - 1) {
@@ -72,15 +87,10 @@ __global__ void __launch_bounds__(kConsumeThreads)
       state[2] = 0;
     }
   }
-  if (g >= static_cast<uint32_t>(kGenerations)) return;  // nothing to address
+  if (g >= static_cast<uint32_t>(kGenerations) || !active) return;
 
-  const int packs_per_row = n / 8;
-  const int pack = blockIdx.x * kConsumeThreads + threadIdx.x;
-  if (pack >= m * packs_per_row) return;
-  const int t = pack / packs_per_row;
-  const int c8 = pack % packs_per_row;
-  uint16_t* slot = mailbox + (static_cast<size_t>(g) * capacity + t) * n + c8 * 8;
-  uint4 v = ptx::ld_volatile_v4(slot);
+  uint16_t* slot = slot0 + g * generation_stride;
+  uint4 v = g == 0 ? candidates[0] : (g == 1 ? candidates[1] : candidates[2]);
   if (has_sentinel(v)) {
     const uint64_t start = ptx::globaltimer();
     for (;;) {

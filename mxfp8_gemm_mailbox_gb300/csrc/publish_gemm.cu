@@ -218,6 +218,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                        p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt) * kSfChunkBytes,
                        kSfChunkBytes, full, pol_stream);
       }
+      // Warm L2 with the stages that come after the ring, so HBM keeps
+      // streaming while the previous kernel finishes and the grid wait holds.
+      const int nwarm = min(nkt, npre + p.l2_prefetch);
+      if (nwarm > npre) {
+        if (p.w_tiled != nullptr) {
+          ptx::prefetch_l2(p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt_begin + npre) *
+                                           kWTileBytes,
+                           static_cast<uint32_t>(nwarm - npre) * kWTileBytes);
+        } else {
+          for (int i = npre; i < nwarm; ++i)
+            ptx::prefetch_l2_tile(&tmap_w, (kt_begin + i) * kTileK, tile * kBlockN);
+        }
+        ptx::prefetch_l2(p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt_begin + npre) *
+                                      kSfChunkBytes,
+                         static_cast<uint32_t>(nwarm - npre) * kSfChunkBytes);
+      }
       // The activations follow the programmatic grid wait.
       ptx::grid_dependency_wait();
       for (int i = 0; i < npre; ++i)
