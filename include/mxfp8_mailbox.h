@@ -202,6 +202,38 @@ mxfp8_status mxfp8_mailbox_status(const int32_t* stage_state, int32_t* words, vo
 /* Releases the handle (host memory only; the caller's buffers stay). */
 void mxfp8_publish_gemm_destroy(mxfp8_publish_gemm* gemm);
 
+/* Scratch bytes the library keeps in device memory for
+ * mxfp8_publish_gemm_run_noalloc: a static array that every GPU loading the
+ * library holds until the process exits. */
+#define MXFP8_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* The publishing GEMM in one call that allocates nothing.  The source pages
+ * have no counterpart: it exists for callers that cannot allocate -- code
+ * issuing work while a stream is captured into a CUDA graph (where a device
+ * allocation would break the capture), runtimes that hand all device memory
+ * to a fixed pool at start-up and forbid cudaMalloc afterwards, and plain C
+ * hosts without a device allocator of their own.  It needs no handle and no
+ * workspace: W is read in place (MXFP8_W_IN_PLACE; w_layout 0 means that
+ * here, MXFP8_W_TILED is refused), and W's scale factors are re-laid on every
+ * call into the library's static scratch array (MXFP8_NOALLOC_SCRATCH_BYTES),
+ * then the same GEMM kernel as mxfp8_publish_gemm_run runs on it.
+ *  desc:        as for mxfp8_publish_gemm_create; N/128 * ceil(K/128) * 512
+ *               bytes of scale chunks must fit the scratch, else
+ *               MXFP8_ERR_UNSUPPORTED (e.g. N = 8192 with K = 16384 fits).
+ *  w, w_scale:  device, as for mxfp8_publish_gemm_create (both read per call).
+ *  x, x_scale, m, c: as for mxfp8_publish_gemm_run.
+ *  mailbox, stage_state: device, as for mxfp8_mailbox_init.
+ * The first call on a device resolves the scratch array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Every call shares the one array and leaves its
+ * scale chunks there; calls that overlap on the GPU (on two streams, or two
+ * threads) race on it and must not be issued.  As after
+ * mxfp8_publish_gemm_run, one mailbox_consume must follow on the stream. */
+mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* desc, const void* w,
+                                            const void* w_scale, const void* x,
+                                            const void* x_scale, int32_t m, void* c,
+                                            void* mailbox, int32_t* stage_state, void* stream);
+
 /* Text of the calling thread's last error ("" if none). */
 const char* mxfp8_last_error(void);
 

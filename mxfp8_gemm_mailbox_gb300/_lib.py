@@ -21,6 +21,7 @@ FLAG_BAD_STATE = 0x4
 GENERATIONS = 3
 SENTINEL = 0x80000000
 MAX_ROWS = 8
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 # Every symbol the header declares, with (restype, argtypes).
 _vp = ctypes.c_void_p
@@ -51,6 +52,8 @@ SIGNATURES = {
     "mailbox_consume": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _vp, _u64, _vp]),
     "mxfp8_mailbox_status": (ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp]),
     "mxfp8_publish_gemm_destroy": (None, [_vp]),
+    "mxfp8_publish_gemm_run_noalloc": (ctypes.c_int, [ctypes.POINTER(GemmDesc), _vp, _vp, _vp, _vp,
+                                                      _i32, _vp, _vp, _vp, _vp]),
     "mxfp8_last_error": (ctypes.c_char_p, []),
 }
 

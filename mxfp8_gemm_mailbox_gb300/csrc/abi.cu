@@ -422,6 +422,117 @@ mxfp8_status mxfp8_mailbox_status(const int32_t* stage_state, int32_t* words, vo
 
 void mxfp8_publish_gemm_destroy(mxfp8_publish_gemm* gemm) { delete gemm; }
 
+}  // extern "C"
+
+// ------------------------------------------------ the allocation-free call
+// For callers that cannot allocate device memory: W's re-laid scale chunks go
+// into this file-scope array instead of a caller-provided workspace.  Its
+// name is a host-side stand-in in host code, so host code uses only the
+// device address resolved below, once per device, with that device current.
+namespace {
+
+__device__ __align__(256) uint8_t g_noalloc_scratch[MXFP8_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+uint8_t* g_noalloc_address[kMaxDevices] = {};
+
+mxfp8_status noalloc_scratch(int device, uint8_t** out) {
+  if (device < 0 || device >= kMaxDevices)
+    return fail(MXFP8_ERR_UNSUPPORTED, "device ordinal out of range for the scratch table");
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_address[device] == nullptr) {
+    void* address = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&address, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch array)");
+    g_noalloc_address[device] = static_cast<uint8_t*>(address);
+  }
+  *out = g_noalloc_address[device];
+  return MXFP8_OK;
+}
+
+}  // namespace
+
+extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* desc, const void* w,
+                                                       const void* w_scale, const void* x,
+                                                       const void* x_scale, int32_t m, void* c,
+                                                       void* mailbox, int32_t* stage_state,
+                                                       void* stream) {
+  mxfp8_status st = check_desc(desc);
+  if (st != MXFP8_OK) return st;
+  if (desc->w_layout == MXFP8_W_TILED)
+    return fail(MXFP8_ERR_UNSUPPORTED, "the allocation-free call reads W in place (no tiled copy)");
+  if (!w || !aligned(w, 16)) return fail(MXFP8_ERR_INVALID, "w must be a 16-byte aligned device pointer");
+  if (!w_scale) return fail(MXFP8_ERR_INVALID, "w_scale is NULL");
+  st = check_mailbox(mailbox, stage_state, desc->capacity_m, desc->n);
+  if (st != MXFP8_OK) return st;
+  const int limit = std::min(MXFP8_MAX_ROWS, static_cast<int>(desc->capacity_m));
+  if (m < 1 || m > limit)
+    return fail(MXFP8_ERR_UNSUPPORTED,
+                "m must be in 1.." + std::to_string(limit) + ", got " + std::to_string(m));
+  if (!x || !aligned(x, 16)) return fail(MXFP8_ERR_INVALID, "x must be a 16-byte aligned device pointer");
+  if (!x_scale) return fail(MXFP8_ERR_INVALID, "x_scale is NULL");
+  if (c && !aligned(c, 16)) return fail(MXFP8_ERR_INVALID, "c must be 16-byte aligned");
+  const size_t need = scale_chunk_bytes(desc->n, desc->k);
+  if (need > MXFP8_NOALLOC_SCRATCH_BYTES)
+    return fail(MXFP8_ERR_UNSUPPORTED,
+                "N=" + std::to_string(desc->n) + ", K=" + std::to_string(desc->k) + " needs " +
+                    std::to_string(need) + " scratch bytes; the allocation-free call holds " +
+                    std::to_string(MXFP8_NOALLOC_SCRATCH_BYTES));
+
+  mxfp8_gemm_desc d = *desc;
+  d.w_layout = MXFP8_W_IN_PLACE;
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceLimits lim;
+  st = device_limits(device, &lim);
+  if (st != MXFP8_OK) return st;
+  st = resolve_tactic(&d, lim);
+  if (st != MXFP8_OK) return st;
+  uint8_t* scratch = nullptr;
+  st = noalloc_scratch(device, &scratch);
+  if (st != MXFP8_OK) return st;
+
+  const int k_tiles = k_tiles_of(d.k);
+  const int tiles_per_split = (k_tiles + d.split_k - 1) / d.split_k;
+  CUtensorMap tmap_w, tmap_x;
+  st = encode_rows(&tmap_w, w, static_cast<uint64_t>(d.k), static_cast<uint64_t>(d.n), kBlockN);
+  if (st != MXFP8_OK) return st;
+  st = encode_rows(&tmap_x, x, static_cast<uint64_t>(d.k), static_cast<uint64_t>(m), kRows);
+  if (st != MXFP8_OK) return st;
+  GemmParams p{};
+  p.n = d.n;
+  p.k = d.k;
+  p.m = m;
+  p.k_tiles = k_tiles;
+  p.tiles_per_split = tiles_per_split;
+  p.stages = d.stages;
+  p.capacity = d.capacity_m;
+  p.publish = 1;
+  p.acc_blocks = d.acc_blocks;
+  p.l2_prefetch = d.l2_prefetch;
+  p.tmem = gemm_tmem_plan(d.stages, d.acc_blocks);
+  p.x_scale = static_cast<const uint8_t*>(x_scale);
+  p.w_sf = scratch;
+  p.w_tiled = nullptr;
+  p.c = static_cast<uint16_t*>(c);
+  p.mailbox = static_cast<uint16_t*>(mailbox);
+  p.state = stage_state;
+  p.wait_limit_ns = kGemmWaitLimitNs;
+  p.smem = gemm_smem_layout(d.stages, d.split_k, tiles_per_split);
+  e = set_gemm_smem_attribute(d.split_k, static_cast<int>(p.smem.total));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  e = launch_relayout_w_scales(static_cast<const uint8_t*>(w_scale), scratch, d.n, d.k, s);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the W scale re-layout");
+  e = launch_publish_gemm(tmap_w, tmap_x, p, d.split_k, s);
+  if (e != cudaSuccess) return cuda_fail(e, "launching the publishing GEMM");
+  return MXFP8_OK;
+}
+
+extern "C" {
+
 const char* mxfp8_last_error(void) { return g_last_error.c_str(); }
 
 }  // extern "C"
