@@ -208,11 +208,11 @@ void mxfp8_publish_gemm_destroy(mxfp8_publish_gemm* gemm);
 #define MXFP8_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 /* The publishing GEMM in one call that allocates nothing.  The source pages
- * have no counterpart: it exists for callers that cannot allocate -- code
- * issuing work while a stream is captured into a CUDA graph (where a device
- * allocation would break the capture), runtimes that hand all device memory
- * to a fixed pool at start-up and forbid cudaMalloc afterwards, and plain C
- * hosts without a device allocator of their own.  It needs no handle and no
+ * have no counterpart: it exists for callers that cannot allocate --
+ * runtimes that hand all device memory to a fixed pool at start-up and forbid
+ * cudaMalloc afterwards, latency-critical issue paths where an allocation
+ * (which may synchronise the device) is not allowed, and plain C hosts
+ * without a device allocator of their own.  It needs no handle and no
  * workspace: W is read in place (MXFP8_W_IN_PLACE; w_layout 0 means that
  * here, MXFP8_W_TILED is refused), and W's scale factors are re-laid on every
  * call into the library's static scratch array (MXFP8_NOALLOC_SCRATCH_BYTES),

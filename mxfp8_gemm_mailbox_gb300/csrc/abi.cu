@@ -431,7 +431,7 @@ void mxfp8_publish_gemm_destroy(mxfp8_publish_gemm* gemm) { delete gemm; }
 // device address resolved below, once per device, with that device current.
 namespace {
 
-__device__ __align__(256) uint8_t g_noalloc_scratch[MXFP8_NOALLOC_SCRATCH_BYTES];
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MXFP8_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;

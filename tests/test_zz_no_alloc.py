@@ -1,8 +1,9 @@
 """The allocation-free publishing GEMM against the handle-based one.
 
 Some callers cannot allocate device memory at the point they issue work
-(while a stream is being captured into a CUDA graph, inside a runtime that
-owns all device memory in a fixed pool, from a C host with no allocator), so
+(inside a runtime that owns all device memory in a fixed pool, on an issue
+path where an allocation could synchronise the device, from a C host with no
+allocator), so
 the library offers ``mxfp8_publish_gemm_run_noalloc``: no handle, no
 workspace, W read in place and its scale chunks re-laid into the library's
 own static scratch array on every call.  This file runs last in the suite;
