@@ -100,8 +100,11 @@ def _load(path: Path | None = None):
     lib.oracle_publish.argtypes = [u32p, i32p, i, i, i, u16p]
     lib.oracle_consume.argtypes = [u32p, i32p, i, i, i, u16p]
     lib.oracle_chain.argtypes = [i, i, i, u8p, u8p, u8p, u8p, u32p, i32p, i, u16p, u16p]
+    lib.oracle_gather_init.argtypes = [u32p, i32p, i]
+    lib.oracle_all_gather.argtypes = [u32p, i32p, i, u32p, i, u32p]
     for name in ("oracle_gemm_fp64", "oracle_gemm_bf16", "oracle_gemm_sample",
-                 "oracle_mailbox_init", "oracle_publish", "oracle_consume", "oracle_chain"):
+                 "oracle_mailbox_init", "oracle_publish", "oracle_consume", "oracle_chain",
+                 "oracle_gather_init", "oracle_all_gather"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -235,6 +238,32 @@ class Mailbox:
                                   _ptr(c, ctypes.c_uint16) if c is not None else None,
                                   _ptr(out, ctypes.c_uint16))
         return st, c, out
+
+
+class Gather:
+    """The oracle's one-rank Lamport all-gather: mailbox ``[3][capacity]``
+    uint32 words and state ``[generation, arrivals]``."""
+
+    def __init__(self, capacity_bytes: int):
+        if capacity_bytes <= 0 or capacity_bytes % 16:
+            raise ValueError("the capacity must be a positive multiple of 16 bytes")
+        self.capacity_words = capacity_bytes // 4
+        self.words = np.empty((GENERATIONS, self.capacity_words), dtype=np.uint32)
+        self.state = np.empty(2, dtype=np.int32)
+        st = _load().oracle_gather_init(_ptr(self.words, ctypes.c_uint32),
+                                        _ptr(self.state, ctypes.c_int32), self.capacity_words)
+        if st != OK:
+            raise ValueError(f"oracle_gather_init status {st}")
+
+    def __call__(self, inp: np.ndarray):
+        """(status, output words) for input words (uint32)."""
+        inp = np.ascontiguousarray(inp, dtype=np.uint32).reshape(-1)
+        out = np.empty_like(inp)
+        st = _load().oracle_all_gather(_ptr(self.words, ctypes.c_uint32),
+                                       _ptr(self.state, ctypes.c_int32), self.capacity_words,
+                                       _ptr(inp, ctypes.c_uint32), inp.size,
+                                       _ptr(out, ctypes.c_uint32))
+        return st, out
 
 
 def bf16_bits_to_float(bits: np.ndarray) -> np.ndarray:

@@ -253,3 +253,46 @@ int oracle_chain(int n, int k, int m, const uint8_t* w, const uint8_t* w_scale,
   if (!c) free(local);
   return status;
 }
+
+/* ------------------------------------------------------------------------
+ * The Lamport all-gather with one rank (page "vllm.models.deepseek_v41.
+ * nvidia.ops.cute_dsl.all_gather", module description steps 1-3 and
+ * _AllGatherKernel.kernel), word by word.  Its own mailbox is
+ * mailbox[generation][pack] = [3][capacity_words] 32-bit words; its state is
+ * int32[2]: [0] the call's generation, [1] the arrival count.
+ * ------------------------------------------------------------------------ */
+
+int oracle_gather_init(uint32_t* mailbox, int32_t* state, int capacity_words) {
+  if (capacity_words <= 0 || capacity_words % 4) return ORACLE_ERR_ARGS;
+  for (size_t i = 0; i < (size_t)ORACLE_GENERATIONS * capacity_words; ++i)
+    mailbox[i] = ORACLE_SENTINEL;
+  state[0] = 0;
+  state[1] = 0;
+  return ORACLE_OK;
+}
+
+/* One call on `words` input words (a positive multiple of 4, at most the
+ * capacity): (1) publish every word into this rank's slot of generation g,
+ * a word equal to the sentinel going out as 0; (2) collect: read the slot, a
+ * sentinel word there meaning the poll would not end (ORACLE_ERR_SENTINEL),
+ * write the word to the output, store the sentinel back; (3) advance the
+ * generation and clear the arrival count. */
+int oracle_all_gather(uint32_t* mailbox, int32_t* state, int capacity_words, const uint32_t* in,
+                      int words, uint32_t* out) {
+  if (capacity_words <= 0 || capacity_words % 4 || words <= 0 || words % 4 ||
+      words > capacity_words)
+    return ORACLE_ERR_ARGS;
+  int g = state[0];
+  if (g < 0 || g >= ORACLE_GENERATIONS) return ORACLE_ERR_STATE;
+  uint32_t* slot = mailbox + (size_t)g * capacity_words;
+  for (int i = 0; i < words; ++i) slot[i] = in[i] == ORACLE_SENTINEL ? 0u : in[i];
+  int status = ORACLE_OK;
+  for (int i = 0; i < words; ++i) {
+    if (slot[i] == ORACLE_SENTINEL) status = ORACLE_ERR_SENTINEL;
+    out[i] = slot[i];
+    slot[i] = ORACLE_SENTINEL;
+  }
+  state[0] = (g + 1) % ORACLE_GENERATIONS;
+  state[1] = 0;
+  return status;
+}

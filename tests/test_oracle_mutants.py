@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 import tests.test_oracle as pins
+import tests.test_oracle_gather as gather_pins
 
 SOURCE = Path(oracle.__file__).resolve().parent / "mxfp8_oracle.c"
 
@@ -59,6 +60,15 @@ MUTANTS = {
     "active generation not handed over": (
         "  state[1] = g;\n  return ORACLE_OK;",
         "  return ORACLE_OK;"),
+    "gather keeps the sentinel word": (
+        "slot[i] = in[i] == ORACLE_SENTINEL ? 0u : in[i];",
+        "slot[i] = in[i];"),
+    "gather leaves its slot": (
+        "    out[i] = slot[i];\n    slot[i] = ORACLE_SENTINEL;",
+        "    out[i] = slot[i];"),
+    "gather generation not advanced": (
+        "  state[0] = (g + 1) % ORACLE_GENERATIONS;\n  state[1] = 0;\n  return status;",
+        "  state[1] = 0;\n  return status;"),
 }
 
 PINS = [
@@ -73,6 +83,8 @@ PINS = [
     pins.test_gemm_constant_closed_form,
     pins.test_publish_layout_and_sanitisation,
     pins.test_chain_state_sequence_and_reset,
+    gather_pins.test_gather_worked_examples_golden,
+    gather_pins.test_gather_sequence_of_alternating_sizes,
 ]
 
 
