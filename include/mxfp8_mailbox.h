@@ -202,6 +202,39 @@ mxfp8_status mxfp8_mailbox_status(const int32_t* stage_state, int32_t* words, vo
 /* Releases the handle (host memory only; the caller's buffers stay). */
 void mxfp8_publish_gemm_destroy(mxfp8_publish_gemm* gemm);
 
+/* ------------------------------------------------------------------------
+ * The Lamport all-gather with one rank (page "vllm.models.deepseek_v41.
+ * nvidia.ops.cute_dsl.all_gather", module description steps 1-3), on its own
+ * mailbox: three generations of `capacity_bytes` (a positive multiple of 16,
+ * at most MXFP8_GATHER_MAX_CAPACITY) as 16-byte packs, and state words
+ * int32[4]: [0] the call's generation, [1] the arrival count, [2] unused,
+ * [3] error flags (the MXFP8_FLAG_* bits; mxfp8_mailbox_status reads them).
+ * ------------------------------------------------------------------------ */
+#define MXFP8_GATHER_MAX_CAPACITY (64u << 20)
+
+/* Mailbox bytes for a capacity (3 * capacity_bytes), 0 if it is invalid. */
+size_t lamport_gather_mailbox_bytes(size_t capacity_bytes);
+
+/* Arm a gather mailbox: every word the sentinel, the state zero
+ * (LamportAllGather.__init__).  mailbox: device, 16-byte aligned,
+ * lamport_gather_mailbox_bytes(capacity_bytes); state: device, 16-byte
+ * aligned int32[4].  One kernel on `stream`. */
+mxfp8_status lamport_gather_init(void* mailbox, int32_t* state, size_t capacity_bytes,
+                                 void* stream);
+
+/* One gather (_AllGatherKernel): in (device, 16-byte aligned, nbytes = 16 to
+ * capacity_bytes, a multiple of 16) is published with every 32-bit word equal
+ * to 0x80000000 cleared to 0 (LamportAllGather.__call__: FP32 negative zero
+ * arrives as positive zero), polled back from the rank's own slot, written to
+ * out (device, 16-byte aligned, nbytes), and the slot reset; the last CTA
+ * advances the generation.  Launched with programmatic stream serialisation;
+ * it triggers its dependents once it has published.  A poll still unsatisfied
+ * after timeout_ns (0 = one second) sets MXFP8_FLAG_POLL_TIMEOUT.  Calls on
+ * one mailbox must be ordered on one stream and must not overlap. */
+mxfp8_status lamport_all_gather(void* mailbox, int32_t* state, size_t capacity_bytes,
+                                const void* in, size_t nbytes, void* out, uint64_t timeout_ns,
+                                void* stream);
+
 /* Scratch bytes the library keeps in device memory for
  * mxfp8_publish_gemm_run_noalloc: a static array that every GPU loading the
  * library holds until the process exits. */

@@ -51,6 +51,9 @@ SIGNATURES = {
     "mailbox_publish": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _vp, _vp]),
     "mailbox_consume": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _vp, _u64, _vp]),
     "mxfp8_mailbox_status": (ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp]),
+    "lamport_gather_mailbox_bytes": (_sz, [_sz]),
+    "lamport_gather_init": (ctypes.c_int, [_vp, _vp, _sz, _vp]),
+    "lamport_all_gather": (ctypes.c_int, [_vp, _vp, _sz, _vp, _sz, _vp, _u64, _vp]),
     "mxfp8_publish_gemm_destroy": (None, [_vp]),
     "mxfp8_publish_gemm_run_noalloc": (ctypes.c_int, [ctypes.POINTER(GemmDesc), _vp, _vp, _vp, _vp,
                                                       _i32, _vp, _vp, _vp, _vp]),

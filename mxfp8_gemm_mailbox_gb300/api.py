@@ -145,3 +145,38 @@ class PublishGemm:
             self.close()
         except Exception:
             pass
+
+
+class LamportGather:
+    """The one-rank Lamport all-gather on its own mailbox of ``capacity_bytes``
+    (a multiple of 16): ``gather(x)`` returns x's words with 0x80000000 words
+    cleared, through the publish / poll / reset protocol."""
+
+    def __init__(self, capacity_bytes: int, device=None, stream=None):
+        lib = _lib.load()
+        nbytes = lib.lamport_gather_mailbox_bytes(capacity_bytes)
+        if nbytes == 0:
+            raise ValueError(f"invalid gather capacity {capacity_bytes}")
+        device = torch.device(device or "cuda")
+        self.capacity = capacity_bytes
+        self.words = torch.empty(nbytes // 4, dtype=torch.int32, device=device)
+        self.state = torch.zeros(4, dtype=torch.int32, device=device)
+        check(lib.lamport_gather_init(_ptr(self.words), _ptr(self.state), capacity_bytes,
+                                      _stream(stream)), "lamport_gather_init")
+
+    def accepts(self, inp: torch.Tensor) -> bool:
+        return 0 < inp.nbytes <= self.capacity and inp.nbytes % 16 == 0
+
+    def __call__(self, inp: torch.Tensor, out: torch.Tensor | None = None, timeout_ns: int = 0,
+                 stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty_like(inp)
+        check(_lib.load().lamport_all_gather(_ptr(self.words), _ptr(self.state), self.capacity,
+                                             _ptr(inp), inp.nbytes, _ptr(out), timeout_ns,
+                                             _stream(stream)), "lamport_all_gather")
+        return out
+
+    def status(self, stream=None):
+        words = (ctypes.c_int32 * 4)()
+        st = _lib.load().mxfp8_mailbox_status(_ptr(self.state), words, _stream(stream))
+        return st, list(words)

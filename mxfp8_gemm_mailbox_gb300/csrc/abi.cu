@@ -405,6 +405,50 @@ mxfp8_status mailbox_consume(void* mailbox, int32_t* stage_state, int32_t capaci
   return MXFP8_OK;
 }
 
+size_t lamport_gather_mailbox_bytes(size_t capacity_bytes) {
+  if (capacity_bytes == 0 || capacity_bytes % 16 || capacity_bytes > MXFP8_GATHER_MAX_CAPACITY)
+    return 0;
+  return static_cast<size_t>(MXFP8_MAILBOX_GENERATIONS) * capacity_bytes;
+}
+
+mxfp8_status lamport_gather_init(void* mailbox, int32_t* state, size_t capacity_bytes,
+                                 void* stream) {
+  if (lamport_gather_mailbox_bytes(capacity_bytes) == 0)
+    return fail(MXFP8_ERR_INVALID, "the capacity must be a positive multiple of 16 bytes, at most " +
+                                       std::to_string(MXFP8_GATHER_MAX_CAPACITY));
+  if (!mailbox || !aligned(mailbox, 16))
+    return fail(MXFP8_ERR_INVALID, "mailbox must be a 16-byte aligned device pointer");
+  if (!state || !aligned(state, 16))
+    return fail(MXFP8_ERR_INVALID, "state must be a 16-byte aligned device int32[4]");
+  cudaError_t e = launch_lamport_gather_init(mailbox, state, capacity_bytes,
+                                             static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the gather mailbox init");
+  return MXFP8_OK;
+}
+
+mxfp8_status lamport_all_gather(void* mailbox, int32_t* state, size_t capacity_bytes,
+                                const void* in, size_t nbytes, void* out, uint64_t timeout_ns,
+                                void* stream) {
+  if (lamport_gather_mailbox_bytes(capacity_bytes) == 0)
+    return fail(MXFP8_ERR_INVALID, "the capacity must be a positive multiple of 16 bytes, at most " +
+                                       std::to_string(MXFP8_GATHER_MAX_CAPACITY));
+  if (nbytes == 0 || nbytes % 16 || nbytes > capacity_bytes)
+    return fail(MXFP8_ERR_INVALID, "the gather takes 16-byte multiples of up to " +
+                                       std::to_string(capacity_bytes) + " bytes, not " +
+                                       std::to_string(nbytes));
+  if (!mailbox || !aligned(mailbox, 16))
+    return fail(MXFP8_ERR_INVALID, "mailbox must be a 16-byte aligned device pointer");
+  if (!state || !aligned(state, 16))
+    return fail(MXFP8_ERR_INVALID, "state must be a 16-byte aligned device int32[4]");
+  if (!in || !aligned(in, 16) || !out || !aligned(out, 16))
+    return fail(MXFP8_ERR_INVALID, "in and out must be 16-byte aligned device pointers");
+  cudaError_t e = launch_lamport_gather(in, out, mailbox, state, capacity_bytes, nbytes,
+                                        timeout_ns ? timeout_ns : kDefaultPollTimeoutNs,
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the gather");
+  return MXFP8_OK;
+}
+
 mxfp8_status mxfp8_mailbox_status(const int32_t* stage_state, int32_t* words, void* stream) {
   if (!stage_state || !words) return fail(MXFP8_ERR_INVALID, "stage_state and words are required");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

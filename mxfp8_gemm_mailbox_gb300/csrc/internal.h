@@ -81,6 +81,11 @@ cudaError_t launch_mailbox_init(uint16_t* mailbox, int32_t* state, int capacity,
                                 cudaStream_t stream);
 cudaError_t launch_mailbox_consume(uint16_t* mailbox, int32_t* state, int capacity, int n, int m,
                                    uint16_t* out, uint64_t timeout_ns, cudaStream_t stream);
+cudaError_t launch_lamport_gather_init(void* mailbox, int32_t* state, size_t capacity_bytes,
+                                       cudaStream_t stream);
+cudaError_t launch_lamport_gather(const void* in, void* out, void* mailbox, int32_t* state,
+                                  size_t capacity_bytes, size_t nbytes, uint64_t timeout_ns,
+                                  cudaStream_t stream);
 cudaError_t launch_mailbox_publish(uint16_t* mailbox, int32_t* state, int capacity, int n, int m,
                                    const uint16_t* c, cudaStream_t stream);
 

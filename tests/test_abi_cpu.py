@@ -21,7 +21,7 @@ def lib():
 def declared_functions():
     text = HEADER.read_text()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b((?:mxfp8|mailbox)_\w+)\s*\(", text, flags=re.M)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b((?:mxfp8|mailbox|lamport)_\w+)\s*\(", text, flags=re.M)
     return sorted(set(names))
 
 
@@ -122,3 +122,18 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         _lib.load()
+
+
+def test_gather_calls_reject_bad_arguments(lib):
+    mb, st, buf = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)
+    assert lib.lamport_gather_mailbox_bytes(4096) == 3 * 4096
+    for cap in (0, 20, (64 << 20) + 16):
+        assert lib.lamport_gather_mailbox_bytes(cap) == 0
+        assert lib.lamport_gather_init(mb, st, cap, None) == _lib.ERR_INVALID
+    assert lib.lamport_gather_init(ctypes.c_void_p(0x1008), st, 4096, None) == _lib.ERR_INVALID
+    for nbytes in (0, 24, 4112):
+        assert lib.lamport_all_gather(mb, st, 4096, buf, nbytes, buf, 0, None) == _lib.ERR_INVALID
+    assert lib.lamport_all_gather(mb, st, 4096, ctypes.c_void_p(0x3004), 16, buf, 0,
+                                  None) == _lib.ERR_INVALID
+    assert "16-byte multiples" in (lib.lamport_all_gather(mb, st, 64, buf, 80, buf, 0, None)
+                                   and lib.mxfp8_last_error().decode())
