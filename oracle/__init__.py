@@ -100,11 +100,15 @@ def _load(path: Path | None = None):
     lib.oracle_publish.argtypes = [u32p, i32p, i, i, i, u16p]
     lib.oracle_consume.argtypes = [u32p, i32p, i, i, i, u16p]
     lib.oracle_chain.argtypes = [i, i, i, u8p, u8p, u8p, u8p, u32p, i32p, i, u16p, u16p]
+    lib.oracle_tagged_init.argtypes = [u32p, i, i]
+    lib.oracle_tagged_publish.argtypes = [u32p, i, i, i, u16p, ctypes.c_uint32]
+    lib.oracle_tagged_consume.argtypes = [u32p, i, i, i, ctypes.c_uint32, u16p]
     lib.oracle_gather_init.argtypes = [u32p, i32p, i]
     lib.oracle_all_gather.argtypes = [u32p, i32p, i, u32p, i, u32p]
     for name in ("oracle_gemm_fp64", "oracle_gemm_bf16", "oracle_gemm_sample",
                  "oracle_mailbox_init", "oracle_publish", "oracle_consume", "oracle_chain",
-                 "oracle_gather_init", "oracle_all_gather"):
+                 "oracle_gather_init", "oracle_all_gather", "oracle_tagged_init",
+                 "oracle_tagged_publish", "oracle_tagged_consume"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -238,6 +242,29 @@ class Mailbox:
                                   _ptr(c, ctypes.c_uint16) if c is not None else None,
                                   _ptr(out, ctypes.c_uint16))
         return st, c, out
+
+
+class TaggedMailbox:
+    """The oracle's tagged-pair mailbox: ``pairs [capacity][N/2][2]`` uint32
+    (value word, tag); tag 0 is the armed state."""
+
+    def __init__(self, capacity: int, n: int):
+        self.capacity, self.n = capacity, n
+        self.pairs = np.empty((capacity, n // 2, 2), dtype=np.uint32)
+        st = _load().oracle_tagged_init(_ptr(self.pairs, ctypes.c_uint32), capacity, n)
+        if st != OK:
+            raise ValueError(f"oracle_tagged_init status {st}")
+
+    def publish(self, c: np.ndarray, tag: int) -> int:
+        c = np.ascontiguousarray(c, dtype=np.uint16)
+        return _load().oracle_tagged_publish(_ptr(self.pairs, ctypes.c_uint32), self.capacity,
+                                             self.n, c.shape[0], _ptr(c, ctypes.c_uint16), tag)
+
+    def consume(self, m: int, tag: int):
+        out = np.empty((m, self.n), dtype=np.uint16)
+        st = _load().oracle_tagged_consume(_ptr(self.pairs, ctypes.c_uint32), self.capacity,
+                                           self.n, m, tag, _ptr(out, ctypes.c_uint16))
+        return st, out
 
 
 class Gather:

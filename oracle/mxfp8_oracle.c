@@ -296,3 +296,51 @@ int oracle_all_gather(uint32_t* mailbox, int32_t* state, int capacity_words, con
   state[1] = 0;
   return status;
 }
+
+/* ------------------------------------------------------------------------
+ * The tagged-pair mailbox (page "vllm.models.deepseek_v41.amd.mono.common.
+ * sync", Mailbox: every 32-bit value stored next to the launch's tag, a
+ * consumer polls until all tags match, nothing is reset).  Pairs are
+ * pairs[t][w] = (word, tag) for t < capacity, w < N/2, word w holding BF16
+ * columns 2w (low half) and 2w + 1; tag 0 is the armed state, never live.
+ * ------------------------------------------------------------------------ */
+
+int oracle_tagged_init(uint32_t* pairs, int capacity, int n) {
+  if (capacity <= 0 || n <= 0 || n % 8) return ORACLE_ERR_ARGS;
+  memset(pairs, 0, sizeof(uint32_t) * 2 * (size_t)capacity * (size_t)(n / 2));
+  return ORACLE_OK;
+}
+
+/* put: C [m][N] (BF16 bits, moved unchanged) with `tag`. */
+int oracle_tagged_publish(uint32_t* pairs, int capacity, int n, int m, const uint16_t* c,
+                          uint32_t tag) {
+  if (capacity <= 0 || n <= 0 || n % 8 || m <= 0 || m > capacity || tag == 0)
+    return ORACLE_ERR_ARGS;
+  int half_n = n / 2;
+  for (int t = 0; t < m; ++t)
+    for (int w = 0; w < half_n; ++w) {
+      size_t at = 2 * ((size_t)t * half_n + w);
+      pairs[at] = (uint32_t)c[(size_t)t * n + 2 * w] | ((uint32_t)c[(size_t)t * n + 2 * w + 1] << 16);
+      pairs[at + 1] = tag;
+    }
+  return ORACLE_OK;
+}
+
+/* poll: the value words of rows t < m once every tag equals `tag`; a stale
+ * tag means the poll would not end (ORACLE_ERR_SENTINEL; the words are still
+ * copied).  Nothing is reset. */
+int oracle_tagged_consume(const uint32_t* pairs, int capacity, int n, int m, uint32_t tag,
+                          uint16_t* out) {
+  if (capacity <= 0 || n <= 0 || n % 8 || m <= 0 || m > capacity || tag == 0)
+    return ORACLE_ERR_ARGS;
+  int half_n = n / 2;
+  int status = ORACLE_OK;
+  for (int t = 0; t < m; ++t)
+    for (int w = 0; w < half_n; ++w) {
+      size_t at = 2 * ((size_t)t * half_n + w);
+      if (pairs[at + 1] != tag) status = ORACLE_ERR_SENTINEL;
+      out[(size_t)t * n + 2 * w] = (uint16_t)(pairs[at] & 0xFFFF);
+      out[(size_t)t * n + 2 * w + 1] = (uint16_t)(pairs[at] >> 16);
+    }
+  return status;
+}

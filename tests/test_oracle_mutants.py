@@ -14,6 +14,7 @@ import pytest
 import oracle
 import tests.test_oracle as pins
 import tests.test_oracle_gather as gather_pins
+import tests.test_oracle_tagged as tagged_pins
 
 SOURCE = Path(oracle.__file__).resolve().parent / "mxfp8_oracle.c"
 
@@ -66,6 +67,12 @@ MUTANTS = {
     "gather leaves its slot": (
         "    out[i] = slot[i];\n    slot[i] = ORACLE_SENTINEL;",
         "    out[i] = slot[i];"),
+    "tagged pair without its tag": (
+        "      pairs[at + 1] = tag;\n",
+        "      pairs[at + 1] = 1u;\n"),
+    "tagged poll ignores stale tags": (
+        "      if (pairs[at + 1] != tag) status = ORACLE_ERR_SENTINEL;\n",
+        "\n"),
     "gather generation not advanced": (
         "  state[0] = (g + 1) % ORACLE_GENERATIONS;\n  state[1] = 0;\n  return status;",
         "  state[1] = 0;\n  return status;"),
@@ -85,6 +92,8 @@ PINS = [
     pins.test_chain_state_sequence_and_reset,
     gather_pins.test_gather_worked_examples_golden,
     gather_pins.test_gather_sequence_of_alternating_sizes,
+    tagged_pins.test_pair_layout_and_unchanged_bits,
+    tagged_pins.test_stale_tag_and_no_reset,
 ]
 
 
