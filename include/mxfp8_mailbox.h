@@ -235,6 +235,37 @@ mxfp8_status lamport_all_gather(void* mailbox, int32_t* state, size_t capacity_b
                                 const void* in, size_t nbytes, void* out, uint64_t timeout_ns,
                                 void* stream);
 
+/* ------------------------------------------------------------------------
+ * The tagged-pair mailbox (page "vllm.models.deepseek_v41.amd.mono.common.
+ * sync", Mailbox: each 32-bit value stored next to the launch's tag, a
+ * consumer polls until every tag matches, nothing is reset), as an
+ * alternative protocol for the projection's output.  pairs: device, 16-byte
+ * aligned, tagged_mailbox_bytes(capacity_m, n): [capacity_m][n/2] pairs of
+ * uint32 (value word holding BF16 columns 2w | 2w+1 << 16, tag).  Tag 0 is the
+ * armed state and is refused; the caller gives every call a new tag (an
+ * epoch) and calls on one mailbox are ordered on one stream.  The BF16 bits
+ * move unchanged (no sentinel, so negative zero is kept).
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of a tagged mailbox: capacity_m * n * 4 (0 for an invalid shape:
+ * capacity_m not in 1..8, n not a positive multiple of 8). */
+size_t tagged_mailbox_bytes(int32_t capacity_m, int32_t n);
+
+/* Arm: every pair zero (tag 0). */
+mxfp8_status tagged_mailbox_init(void* pairs, int32_t capacity_m, int32_t n, void* stream);
+
+/* put: C [m][n] BF16 (device, 16-byte aligned) with `tag`, each value in one
+ * 16-byte store with its tag.  PDL launch. */
+mxfp8_status tagged_publish(void* pairs, int32_t capacity_m, int32_t n, int32_t m,
+                            const void* c, uint32_t tag, void* stream);
+
+/* poll: out [m][n] BF16 (device, 16-byte aligned) once every tag of rows
+ * t < m equals `tag`; nothing is reset.  A poll unsatisfied after timeout_ns
+ * (0 = one second) gives up, copies what is there and, if flags (device
+ * int32) is not NULL, sets MXFP8_FLAG_POLL_TIMEOUT in it.  PDL launch. */
+mxfp8_status tagged_consume(void* pairs, int32_t capacity_m, int32_t n, int32_t m, uint32_t tag,
+                            void* out, uint64_t timeout_ns, int32_t* flags, void* stream);
+
 /* Scratch bytes the library keeps in device memory for
  * mxfp8_publish_gemm_run_noalloc: a static array that every GPU loading the
  * library holds until the process exits. */

@@ -7,8 +7,8 @@ The compute path is the CUDA library ``libmxfp8_mailbox.so`` (C ABI in
 from . import _lib
 from ._lib import (ERR_CUDA, ERR_INVALID, ERR_STATE, ERR_TIMEOUT, ERR_UNSUPPORTED,
                    FLAG_BAD_STATE, FLAG_GEMM_TIMEOUT, FLAG_POLL_TIMEOUT, OK, Mxfp8Error)
-from .api import LamportGather, Mailbox, PublishGemm
+from .api import LamportGather, Mailbox, PublishGemm, TaggedMailbox
 
-__all__ = ["LamportGather", "Mailbox", "PublishGemm", "Mxfp8Error", "OK", "ERR_INVALID", "ERR_UNSUPPORTED",
+__all__ = ["LamportGather", "Mailbox", "TaggedMailbox", "PublishGemm", "Mxfp8Error", "OK", "ERR_INVALID", "ERR_UNSUPPORTED",
            "ERR_CUDA", "ERR_TIMEOUT", "ERR_STATE", "FLAG_POLL_TIMEOUT", "FLAG_GEMM_TIMEOUT",
            "FLAG_BAD_STATE"]

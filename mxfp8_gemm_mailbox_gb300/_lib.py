@@ -52,6 +52,11 @@ SIGNATURES = {
     "mailbox_consume": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _vp, _u64, _vp]),
     "mxfp8_mailbox_status": (ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp]),
     "lamport_gather_mailbox_bytes": (_sz, [_sz]),
+    "tagged_mailbox_bytes": (_sz, [_i32, _i32]),
+    "tagged_mailbox_init": (ctypes.c_int, [_vp, _i32, _i32, _vp]),
+    "tagged_publish": (ctypes.c_int, [_vp, _i32, _i32, _i32, _vp, ctypes.c_uint32, _vp]),
+    "tagged_consume": (ctypes.c_int, [_vp, _i32, _i32, _i32, ctypes.c_uint32, _vp, _u64, _vp,
+                                      _vp]),
     "lamport_gather_init": (ctypes.c_int, [_vp, _vp, _sz, _vp]),
     "lamport_all_gather": (ctypes.c_int, [_vp, _vp, _sz, _vp, _sz, _vp, _u64, _vp]),
     "mxfp8_publish_gemm_destroy": (None, [_vp]),

@@ -180,3 +180,35 @@ class LamportGather:
         words = (ctypes.c_int32 * 4)()
         st = _lib.load().mxfp8_mailbox_status(_ptr(self.state), words, _stream(stream))
         return st, list(words)
+
+
+class TaggedMailbox:
+    """The tagged-pair mailbox ``[capacity_m][n/2]`` of (value word, tag):
+    ``publish(c, tag)`` stores C with a nonzero tag; ``consume(m, tag)`` reads
+    it back once every tag matches.  Nothing is reset; BF16 bits move
+    unchanged."""
+
+    def __init__(self, capacity_m: int, n: int, device=None, stream=None):
+        lib = _lib.load()
+        nbytes = lib.tagged_mailbox_bytes(capacity_m, n)
+        if nbytes == 0:
+            raise ValueError(f"invalid tagged mailbox shape capacity_m={capacity_m}, n={n}")
+        device = torch.device(device or "cuda")
+        self.capacity, self.n = capacity_m, n
+        self.pairs = torch.empty(nbytes // 4, dtype=torch.int32, device=device)
+        self.flags = torch.zeros(1, dtype=torch.int32, device=device)
+        check(lib.tagged_mailbox_init(_ptr(self.pairs), capacity_m, n, _stream(stream)),
+              "tagged_mailbox_init")
+
+    def publish(self, c: torch.Tensor, tag: int, stream=None) -> None:
+        check(_lib.load().tagged_publish(_ptr(self.pairs), self.capacity, self.n, c.shape[0],
+                                         _ptr(c), tag, _stream(stream)), "tagged_publish")
+
+    def consume(self, m: int, tag: int, out: torch.Tensor | None = None, timeout_ns: int = 0,
+                stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty((m, self.n), dtype=torch.bfloat16, device=self.pairs.device)
+        check(_lib.load().tagged_consume(_ptr(self.pairs), self.capacity, self.n, m, tag,
+                                         _ptr(out), timeout_ns, _ptr(self.flags),
+                                         _stream(stream)), "tagged_consume")
+        return out

@@ -405,6 +405,51 @@ mxfp8_status mailbox_consume(void* mailbox, int32_t* stage_state, int32_t capaci
   return MXFP8_OK;
 }
 
+size_t tagged_mailbox_bytes(int32_t capacity_m, int32_t n) {
+  if (capacity_m < 1 || capacity_m > MXFP8_MAX_ROWS || n <= 0 || n % 8) return 0;
+  return static_cast<size_t>(capacity_m) * n * 4;
+}
+
+mxfp8_status tagged_mailbox_init(void* pairs, int32_t capacity_m, int32_t n, void* stream) {
+  const size_t bytes = tagged_mailbox_bytes(capacity_m, n);
+  if (bytes == 0) return fail(MXFP8_ERR_INVALID, "capacity_m must be in 1..8 and n a multiple of 8");
+  if (!pairs || !aligned(pairs, 16))
+    return fail(MXFP8_ERR_INVALID, "pairs must be a 16-byte aligned device pointer");
+  cudaError_t e = launch_tagged_init(pairs, bytes, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the tagged mailbox init");
+  return MXFP8_OK;
+}
+
+mxfp8_status tagged_publish(void* pairs, int32_t capacity_m, int32_t n, int32_t m, const void* c,
+                            uint32_t tag, void* stream) {
+  if (tagged_mailbox_bytes(capacity_m, n) == 0)
+    return fail(MXFP8_ERR_INVALID, "capacity_m must be in 1..8 and n a multiple of 8");
+  if (m < 1 || m > capacity_m) return fail(MXFP8_ERR_UNSUPPORTED, "m must be in 1..capacity_m");
+  if (tag == 0) return fail(MXFP8_ERR_INVALID, "tag 0 is the armed state; use a nonzero epoch");
+  if (!pairs || !aligned(pairs, 16) || !c || !aligned(c, 16))
+    return fail(MXFP8_ERR_INVALID, "pairs and c must be 16-byte aligned device pointers");
+  cudaError_t e = launch_tagged_publish(pairs, n, m, static_cast<const uint16_t*>(c), tag,
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the tagged publish");
+  return MXFP8_OK;
+}
+
+mxfp8_status tagged_consume(void* pairs, int32_t capacity_m, int32_t n, int32_t m, uint32_t tag,
+                            void* out, uint64_t timeout_ns, int32_t* flags, void* stream) {
+  if (tagged_mailbox_bytes(capacity_m, n) == 0)
+    return fail(MXFP8_ERR_INVALID, "capacity_m must be in 1..8 and n a multiple of 8");
+  if (m < 1 || m > capacity_m) return fail(MXFP8_ERR_UNSUPPORTED, "m must be in 1..capacity_m");
+  if (tag == 0) return fail(MXFP8_ERR_INVALID, "tag 0 is the armed state; use a nonzero epoch");
+  if (!pairs || !aligned(pairs, 16) || !out || !aligned(out, 16))
+    return fail(MXFP8_ERR_INVALID, "pairs and out must be 16-byte aligned device pointers");
+  if (flags && !aligned(flags, 4)) return fail(MXFP8_ERR_INVALID, "flags must be 4-byte aligned");
+  cudaError_t e = launch_tagged_consume(pairs, n, m, tag, static_cast<uint16_t*>(out),
+                                        timeout_ns ? timeout_ns : kDefaultPollTimeoutNs, flags,
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launching the tagged consume");
+  return MXFP8_OK;
+}
+
 size_t lamport_gather_mailbox_bytes(size_t capacity_bytes) {
   if (capacity_bytes == 0 || capacity_bytes % 16 || capacity_bytes > MXFP8_GATHER_MAX_CAPACITY)
     return 0;

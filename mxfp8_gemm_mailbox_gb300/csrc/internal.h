@@ -86,6 +86,11 @@ cudaError_t launch_lamport_gather_init(void* mailbox, int32_t* state, size_t cap
 cudaError_t launch_lamport_gather(const void* in, void* out, void* mailbox, int32_t* state,
                                   size_t capacity_bytes, size_t nbytes, uint64_t timeout_ns,
                                   cudaStream_t stream);
+cudaError_t launch_tagged_init(void* pairs, size_t bytes, cudaStream_t stream);
+cudaError_t launch_tagged_publish(void* pairs, int n, int m, const uint16_t* c, uint32_t tag,
+                                  cudaStream_t stream);
+cudaError_t launch_tagged_consume(const void* pairs, int n, int m, uint32_t tag, uint16_t* out,
+                                  uint64_t timeout_ns, int32_t* flags, cudaStream_t stream);
 cudaError_t launch_mailbox_publish(uint16_t* mailbox, int32_t* state, int capacity, int n, int m,
                                    const uint16_t* c, cudaStream_t stream);
 

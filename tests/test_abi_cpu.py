@@ -21,7 +21,7 @@ def lib():
 def declared_functions():
     text = HEADER.read_text()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b((?:mxfp8|mailbox|lamport)_\w+)\s*\(", text, flags=re.M)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b((?:mxfp8|mailbox|lamport|tagged)_\w+)\s*\(", text, flags=re.M)
     return sorted(set(names))
 
 
@@ -137,3 +137,15 @@ def test_gather_calls_reject_bad_arguments(lib):
                                   None) == _lib.ERR_INVALID
     assert "16-byte multiples" in (lib.lamport_all_gather(mb, st, 64, buf, 80, buf, 0, None)
                                    and lib.mxfp8_last_error().decode())
+
+
+def test_tagged_calls_reject_bad_arguments(lib):
+    pairs, buf = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000)
+    assert lib.tagged_mailbox_bytes(8, 7168) == 8 * 7168 * 4
+    assert lib.tagged_mailbox_bytes(0, 128) == 0 and lib.tagged_mailbox_bytes(8, 12) == 0
+    assert lib.tagged_publish(pairs, 8, 128, 1, buf, 0, None) == _lib.ERR_INVALID  # tag 0
+    assert lib.tagged_publish(pairs, 8, 128, 9, buf, 1, None) == _lib.ERR_UNSUPPORTED
+    assert lib.tagged_consume(pairs, 8, 128, 1, 0, buf, 0, None, None) == _lib.ERR_INVALID
+    assert lib.tagged_consume(pairs, 8, 128, 1, 1, ctypes.c_void_p(0x2008), 0, None,
+                              None) == _lib.ERR_INVALID
+    assert lib.tagged_mailbox_init(ctypes.c_void_p(0x1004), 8, 128, None) == _lib.ERR_INVALID
