@@ -51,6 +51,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="budget of the oracle CPU-baseline sample")
+    p.add_argument("--path", choices=("chain", "protocols"), default="chain",
+                   help="chain: the headline (default); protocols: the output hand-off "
+                        "protocols on their own (sentinel mailbox, tagged pairs, all-gather)")
     return p.parse_args(argv)
 
 
@@ -482,10 +485,98 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- protocol rows
+def run_protocols(args):
+    """Each hand-off protocol on its own, at the headline's output size
+    (m = 8 rows x N = 7168 BF16 columns), timed from CUDA graphs of
+    GRAPH_STEPS calls between CUDA events: the sentinel mailbox (publish +
+    consume), the tagged-pair mailbox (publish + consume), and the one-rank
+    Lamport all-gather at payloads up to a few hundred kilobytes."""
+    import numpy as np
+    import torch
+
+    import mxfp8_gemm_mailbox_gb300 as mx
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    wl = workload()
+    rng = np.random.default_rng(5)
+    c = torch.from_numpy(rng.integers(-2**15, 2**15, size=(wl.m, wl.n)).astype(np.int16)).to(device)
+    stream = torch.cuda.Stream(device=device)
+
+    def per_call_us(fn, calls_per_step=1):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            stream.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(GRAPH_STEPS):
+                    fn()
+            for _ in range(3):
+                graph.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            replays = max(1, args.steps // GRAPH_STEPS)
+            e0.record(stream)
+            for _ in range(replays):
+                graph.replay()
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (replays * GRAPH_STEPS * calls_per_step)
+
+    results = {}
+    mb = mx.Mailbox(wl.capacity, wl.n, device=device)
+    out = torch.empty((wl.m, wl.n), dtype=torch.bfloat16, device=device)
+
+    def sentinel():
+        mb.publish(c)
+        mb.consume(wl.m, out)
+    results["sentinel_mailbox_us"] = round(per_call_us(sentinel), 3)
+    status, words = mb.status(stream)
+    if status != mx.OK:
+        raise RuntimeError(f"sentinel mailbox status {status}: {words}")
+    tm = mx.TaggedMailbox(wl.capacity, wl.n, device=device)
+
+    def tagged():
+        tm.publish(c, 7)
+        tm.consume(wl.m, 7, out)
+    results["tagged_pairs_us"] = round(per_call_us(tagged), 3)
+    gather_us = {}
+    for nbytes in (16, 65536, 262144):
+        g = mx.LamportGather(262144, device=device)
+        src = torch.zeros(nbytes // 4, dtype=torch.int32, device=device)
+        dst = torch.empty_like(src)
+        gather_us[str(nbytes)] = round(per_call_us(lambda: g(src, dst)), 3)
+        status, words = g.status(stream)
+        if status != mx.OK:
+            raise RuntimeError(f"gather status {status}: {words}")
+    results["lamport_all_gather_us"] = gather_us
+    payload = wl.m * wl.n * 2
+    line = {
+        "metric": "us/call of the output hand-off protocols (one GPU)",
+        "value": results["sentinel_mailbox_us"],
+        "unit": "us",
+        "n_gpus": 1,
+        "steps": max(1, args.steps // GRAPH_STEPS) * GRAPH_STEPS,
+        "higher_is_better": False,
+        "dtype": "bf16 bits",
+        "data": "synthetic",
+        "config": {"workload": f"hand-off of m={wl.m} x N={wl.n} BF16 ({payload} bytes)",
+                   "timing": f"CUDA graphs of {GRAPH_STEPS} calls"},
+        "results": results,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.path == "protocols":
+        run_protocols(args)
     else:
         run_ours(args)
 

@@ -167,6 +167,16 @@ mxfp8_status mxfp8_publish_gemm_precompile(mxfp8_publish_gemm* gemm, int32_t m);
 mxfp8_status mxfp8_publish_gemm_run(mxfp8_publish_gemm* gemm, const void* x,
                                     const void* x_scale, int32_t m, void* c, void* stream);
 
+/* mxfp8_publish_gemm_run with a global scale (publishing_gemm page,
+ * epilog_warp with use_scale: the accumulator times mScale[0] before the
+ * conversion to BF16): C = alpha * sum_k W x, published as in
+ * mxfp8_publish_gemm_run.  alpha: device, 4-byte aligned FP32 scalar, read
+ * after the grid wait (so the previous kernel may write it), or NULL for 1.
+ * The product is formed on the compensated sum and rounded once. */
+mxfp8_status mxfp8_publish_gemm_run_scaled(mxfp8_publish_gemm* gemm, const void* x,
+                                           const void* x_scale, int32_t m, const float* alpha,
+                                           void* c, void* stream);
+
 /* The same GEMM without the publish (the unfused path of the publishing_gemm
  * page's module description: the plain GEMM writes C, a separate publish
  * kernel reads it back).  c is required. */

@@ -48,6 +48,7 @@ SIGNATURES = {
     "mxfp8_publish_gemm_precompile": (ctypes.c_int, [_vp, _i32]),
     "mxfp8_publish_gemm_run": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, _vp]),
     "mxfp8_gemm_run_unfused": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, _vp]),
+    "mxfp8_publish_gemm_run_scaled": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, _vp, _vp]),
     "mailbox_publish": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _vp, _vp]),
     "mailbox_consume": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _vp, _u64, _vp]),
     "mxfp8_mailbox_status": (ctypes.c_int, [_vp, ctypes.POINTER(_i32), _vp]),

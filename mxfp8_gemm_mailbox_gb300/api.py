@@ -129,6 +129,17 @@ class PublishGemm:
                                                  _ptr(c), _stream(stream)), "mxfp8_publish_gemm_run")
         return c
 
+    def run_scaled(self, x: torch.Tensor, x_scale: torch.Tensor, alpha: torch.Tensor | None,
+                   c: torch.Tensor | None = None, stream=None) -> torch.Tensor | None:
+        """``run`` with C = alpha * (W x); alpha a one-element float32 CUDA tensor."""
+        if alpha is not None and (alpha.dtype != torch.float32 or not alpha.is_cuda):
+            raise TypeError("alpha must be a float32 CUDA tensor")
+        check(_lib.load().mxfp8_publish_gemm_run_scaled(self._handle, _ptr(x), _ptr(x_scale),
+                                                        x.shape[0], _ptr(alpha), _ptr(c),
+                                                        _stream(stream)),
+              "mxfp8_publish_gemm_run_scaled")
+        return c
+
     def run_unfused(self, x: torch.Tensor, x_scale: torch.Tensor, c: torch.Tensor,
                     stream=None) -> torch.Tensor:
         check(_lib.load().mxfp8_gemm_run_unfused(self._handle, _ptr(x), _ptr(x_scale), x.shape[0],

@@ -192,7 +192,7 @@ mxfp8_status check_rows(const mxfp8_publish_gemm* g, int32_t m) {
 }
 
 mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale, int32_t m,
-                      void* c, void* stream, bool publish) {
+                      void* c, void* stream, bool publish, const float* alpha = nullptr) {
   if (!g) return fail(MXFP8_ERR_INVALID, "gemm handle is NULL");
   mxfp8_status st = check_rows(g, m);
   if (st != MXFP8_OK) return st;
@@ -222,6 +222,7 @@ mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale,
   p.w_sf = g->w_sf;
   p.w_tiled = g->w_tiled;
   p.c = static_cast<uint16_t*>(c);
+  p.alpha = alpha;
   p.mailbox = g->mailbox;
   p.state = g->state;
   p.wait_limit_ns = kGemmWaitLimitNs;
@@ -371,6 +372,13 @@ mxfp8_status mxfp8_publish_gemm_precompile(mxfp8_publish_gemm* gemm, int32_t m) 
 mxfp8_status mxfp8_publish_gemm_run(mxfp8_publish_gemm* gemm, const void* x, const void* x_scale,
                                     int32_t m, void* c, void* stream) {
   return run_gemm(gemm, x, x_scale, m, c, stream, true);
+}
+
+mxfp8_status mxfp8_publish_gemm_run_scaled(mxfp8_publish_gemm* gemm, const void* x,
+                                           const void* x_scale, int32_t m, const float* alpha,
+                                           void* c, void* stream) {
+  if (alpha && !aligned(alpha, 4)) return fail(MXFP8_ERR_INVALID, "alpha must be 4-byte aligned");
+  return run_gemm(gemm, x, x_scale, m, c, stream, true, alpha);
 }
 
 mxfp8_status mxfp8_gemm_run_unfused(mxfp8_publish_gemm* gemm, const void* x, const void* x_scale,

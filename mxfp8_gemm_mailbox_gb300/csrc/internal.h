@@ -60,6 +60,7 @@ struct GemmParams {
   const uint8_t* w_sf;      // [n/128][k_tiles][512] tiled W scales
   const uint8_t* w_tiled;   // [n/128][k_tiles][16384] shared-memory images of W, or nullptr
   uint16_t* c;              // [m][n] BF16 or nullptr
+  const float* alpha;       // global scale of C (device scalar) or nullptr for 1
   uint16_t* mailbox;        // [3][capacity][n] BF16
   int32_t* state;           // int32[4]
   uint64_t wait_limit_ns;

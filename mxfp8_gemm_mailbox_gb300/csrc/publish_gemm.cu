@@ -448,6 +448,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         owned[jj] = static_cast<double>(hi[jj]) + static_cast<double>(lo[jj]);
     }
 
+    // The global scale (gemm page, epilog_warp with use_scale: the
+    // accumulator times mScale[0]) multiplies the compensated sum before its
+    // one rounding.  It is read after the grid wait like x.
+    if (p.alpha != nullptr) {
+      const double a = static_cast<double>(*p.alpha);
+#pragma unroll
+      for (int jj = 0; jj < kShard; ++jj) owned[jj] *= a;
+    }
+
     uint16_t* ctile = reinterpret_cast<uint16_t*>(smem + L.ctile);  // [kShard][128]
 #pragma unroll
     for (int jj = 0; jj < kShard; ++jj)

@@ -95,6 +95,7 @@ def _load(path: Path | None = None):
     lib.oracle_clear_negative_zero.restype = ctypes.c_uint16
     lib.oracle_gemm_fp64.argtypes = [i, i, i, u8p, u8p, u8p, u8p, f64p]
     lib.oracle_gemm_bf16.argtypes = [i, i, i, u8p, u8p, u8p, u8p, u16p]
+    lib.oracle_gemm_bf16_scaled.argtypes = [i, i, i, u8p, u8p, u8p, u8p, ctypes.c_float, u16p]
     lib.oracle_gemm_sample.argtypes = [i, i, i, u8p, u8p, u8p, u8p, i, i32p, i32p, u16p]
     lib.oracle_mailbox_init.argtypes = [u32p, i32p, i, i]
     lib.oracle_publish.argtypes = [u32p, i32p, i, i, i, u16p]
@@ -105,7 +106,8 @@ def _load(path: Path | None = None):
     lib.oracle_tagged_consume.argtypes = [u32p, i, i, i, ctypes.c_uint32, u16p]
     lib.oracle_gather_init.argtypes = [u32p, i32p, i]
     lib.oracle_all_gather.argtypes = [u32p, i32p, i, u32p, i, u32p]
-    for name in ("oracle_gemm_fp64", "oracle_gemm_bf16", "oracle_gemm_sample",
+    for name in ("oracle_gemm_fp64", "oracle_gemm_bf16", "oracle_gemm_bf16_scaled",
+                 "oracle_gemm_sample",
                  "oracle_mailbox_init", "oracle_publish", "oracle_consume", "oracle_chain",
                  "oracle_gather_init", "oracle_all_gather", "oracle_tagged_init",
                  "oracle_tagged_publish", "oracle_tagged_consume"):
@@ -176,6 +178,20 @@ def gemm_bf16(w, ws, x, xs) -> np.ndarray:
                                   _ptr(c, ctypes.c_uint16))
     if st != OK:
         raise ValueError(f"oracle_gemm_bf16 status {st}")
+    return c
+
+
+def gemm_bf16_scaled(w, ws, x, xs, alpha: float) -> np.ndarray:
+    """C = BF16(alpha * sum), alpha an FP32 value (rounded once from FP64)."""
+    w, ws, x, xs = map(_u8, (w, ws, x, xs))
+    n, k, m = _check_shapes(w, ws, x, xs)
+    c = np.empty((m, n), dtype=np.uint16)
+    st = _load().oracle_gemm_bf16_scaled(n, k, m, _ptr(w, ctypes.c_uint8),
+                                         _ptr(ws, ctypes.c_uint8), _ptr(x, ctypes.c_uint8),
+                                         _ptr(xs, ctypes.c_uint8), float(np.float32(alpha)),
+                                         _ptr(c, ctypes.c_uint16))
+    if st != OK:
+        raise ValueError(f"oracle_gemm_bf16_scaled status {st}")
     return c
 
 

@@ -168,6 +168,20 @@ int oracle_gemm_bf16(int n, int k, int m, const uint8_t* w, const uint8_t* w_sca
   return status;
 }
 
+/* C = BF16(alpha * sum_k W x): the global scale of the gemm page's
+ * epilog_warp (use_scale), applied to the FP64 sum before the one rounding. */
+int oracle_gemm_bf16_scaled(int n, int k, int m, const uint8_t* w, const uint8_t* w_scale,
+                            const uint8_t* x, const uint8_t* x_scale, float alpha, uint16_t* c) {
+  double* acc = (double*)malloc(sizeof(double) * (size_t)m * (size_t)n);
+  if (!acc) return ORACLE_ERR_ARGS;
+  int status = oracle_gemm_fp64(n, k, m, w, w_scale, x, x_scale, acc);
+  if (status == ORACLE_OK)
+    for (size_t i = 0; i < (size_t)m * (size_t)n; ++i)
+      c[i] = oracle_bf16_rne((double)alpha * acc[i]);
+  free(acc);
+  return status;
+}
+
 /* Selected outputs only: out[i] = BF16(sum_k W[cols[i], k] x[rows[i], k]).
  * Used to check full-size runs at sampled positions. */
 int oracle_gemm_sample(int n, int k, int m, const uint8_t* w, const uint8_t* w_scale,

@@ -216,3 +216,32 @@ def test_bad_next_generation_is_flagged(cuda):
     assert (mailbox_words(mb) == oracle.SENTINEL).all()  # no publish into a bad generation
     assert (bits(c) == oracle.gemm_bf16(w, ws, x, xs)).all()  # C is still written
     assert mb.status()[0] == ERR_STATE
+
+
+@pytest.mark.parametrize("alpha,split_k", [(0.25, 1), (-1.7, 2), (3.0e-3, 4), (1.0, 4)])
+def test_global_scale(cuda, alpha, split_k):
+    wl = synthetic.Workload("alpha", 768, 4096, 6, split_k, exp_lo=-4, exp_hi=2, seed=91)
+    w, ws = synthetic.make_weights(wl)
+    x, xs = synthetic.make_activations(wl)
+    want = oracle.gemm_bf16_scaled(w, ws, x, xs, alpha)
+    mb = Mailbox(8, 768)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=split_k)
+    a = torch.tensor([alpha], dtype=torch.float32, device="cuda")
+    c = torch.empty((6, 768), dtype=torch.bfloat16, device="cuda")
+    g.run_scaled(dev(x), dev(xs), a, c)
+    out = mb.consume(6)
+    torch.cuda.synchronize()
+    assert_bf16_close(bits(c), want, f"alpha={alpha}")
+    assert (bits(out) == sanitized(bits(c))).all()
+    # integer inputs with a power-of-two scale stay exact
+    wi, wsi, xi, xsi = synthetic.integer_operands(768, 4096, 6, seed=3)
+    g2 = PublishGemm(dev(wi), dev(wsi), Mailbox(8, 768), split_k=split_k)
+    a2 = torch.tensor([0.5], dtype=torch.float32, device="cuda")
+    g2.run_scaled(dev(xi), dev(xsi), a2, c)
+    g2.mailbox.consume(6)
+    torch.cuda.synchronize()
+    assert (bits(c) == oracle.gemm_bf16_scaled(wi, wsi, xi, xsi, 0.5)).all()
+    g.run_scaled(dev(x), dev(xs), None, c)  # NULL alpha is the plain run
+    mb.consume(6)
+    torch.cuda.synchronize()
+    assert_bf16_close(bits(c), oracle.gemm_bf16(w, ws, x, xs))

@@ -277,3 +277,21 @@ def test_bad_generation_is_rejected():
     assert st == oracle.ERR_STATE
     mb.state[0] = 3
     assert mb.publish(np.zeros((1, 128), np.uint16)) == oracle.ERR_STATE
+
+
+def test_scaled_gemm_closed_forms():
+    # alpha = 1 is the unscaled product; a power of two scales exactly; any
+    # alpha equals the rounding of alpha times the FP64 sum.
+    wl = synthetic.Workload("scaled", 256, 512, 3, exp_lo=-4, exp_hi=2, seed=12)
+    w, ws = synthetic.make_weights(wl)
+    x, xs = synthetic.make_activations(wl)
+    assert (oracle.gemm_bf16_scaled(w, ws, x, xs, 1.0) == oracle.gemm_bf16(w, ws, x, xs)).all()
+    c = oracle.gemm_bf16(w, ws, x, xs)
+    c4 = oracle.gemm_bf16_scaled(w, ws, x, xs, 0.25)
+    v, v4 = oracle.bf16_bits_to_float(c), oracle.bf16_bits_to_float(c4)
+    assert (v4 == v * 0.25).all()
+    acc = oracle.gemm_fp64(w, ws, x, xs)
+    a = float(np.float32(-1.7))
+    want = np.array([[_exact_bf16_rne(Fraction(a) * Fraction(float(u))) for u in row] for row in acc],
+                    dtype=np.uint16)
+    assert (oracle.gemm_bf16_scaled(w, ws, x, xs, a) == want).all()

@@ -67,6 +67,9 @@ MUTANTS = {
     "gather leaves its slot": (
         "    out[i] = slot[i];\n    slot[i] = ORACLE_SENTINEL;",
         "    out[i] = slot[i];"),
+    "global scale dropped": (
+        "c[i] = oracle_bf16_rne((double)alpha * acc[i]);",
+        "c[i] = oracle_bf16_rne(acc[i]);"),
     "tagged pair without its tag": (
         "      pairs[at + 1] = tag;\n",
         "      pairs[at + 1] = 1u;\n"),
@@ -90,6 +93,7 @@ PINS = [
     pins.test_gemm_constant_closed_form,
     pins.test_publish_layout_and_sanitisation,
     pins.test_chain_state_sequence_and_reset,
+    pins.test_scaled_gemm_closed_forms,
     gather_pins.test_gather_worked_examples_golden,
     gather_pins.test_gather_sequence_of_alternating_sizes,
     tagged_pins.test_pair_layout_and_unchanged_bits,
