@@ -159,6 +159,8 @@ mxfp8_status mxfp8_publish_gemm_precompile(mxfp8_publish_gemm* gemm, int32_t m);
  *  m:       1..min(8, capacity_m), else MXFP8_ERR_UNSUPPORTED.
  *  c:       device, 16-byte aligned, [m][N] BF16, or NULL to skip C.  C keeps
  *           negative zero; the mailbox copy clears it.
+ * The device current when the handle was created must be current (else
+ * MXFP8_ERR_INVALID); a handle is used by one host thread at a time.
  * Publishes into generation g = stage_state[0] and sets stage_state[1] = g.
  * Launched with programmatic stream serialisation: weight loads may start
  * before the previous kernel on `stream` finishes; x, x_scale and the state

@@ -200,6 +200,10 @@ mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale,
   if (!x_scale) return fail(MXFP8_ERR_INVALID, "x_scale is NULL");
   if (c && !aligned(c, 16)) return fail(MXFP8_ERR_INVALID, "c must be 16-byte aligned");
   if (!publish && !c) return fail(MXFP8_ERR_INVALID, "the unfused GEMM needs c");
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess || device != g->device)
+    return fail(MXFP8_ERR_INVALID, "the handle was created on device " + std::to_string(g->device) +
+                                       ", the current device is " + std::to_string(device));
   if (g->x_cached != x || g->m_cached != m) {
     st = encode_rows(&g->tmap_x, x, static_cast<uint64_t>(g->desc.k), static_cast<uint64_t>(m), kRows);
     if (st != MXFP8_OK) return st;
