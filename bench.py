@@ -51,9 +51,10 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="budget of the oracle CPU-baseline sample")
-    p.add_argument("--path", choices=("chain", "protocols"), default="chain",
+    p.add_argument("--path", choices=("chain", "protocols", "sweep"), default="chain",
                    help="chain: the headline (default); protocols: the output hand-off "
-                        "protocols on their own (sentinel mailbox, tagged pairs, all-gather)")
+                        "protocols on their own (sentinel mailbox, tagged pairs, all-gather); "
+                        "sweep: the chain on every m x N x K x S case of the sweep")
     return p.parse_args(argv)
 
 
@@ -618,12 +619,119 @@ def run_protocols(args):
         print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------- sweep table
+L2_BYTES = 129 * 2**20
+
+
+def run_sweep(args):
+    """The chain (publishing GEMM + PDL consumer) on every case of the sweep,
+    m 1..8 x N {2048, 4096, 7168} x K {2048, 4096, 8192, 16384} x S {1, 2, 4},
+    with the default tactic for each (N, K, S).  Each (N, K, S) gets enough
+    handles (each with its own tiled weight copy) that the copies rotated
+    through exceed twice the L2, so every call streams its weight from HBM;
+    per case one CUDA graph of at least GRAPH_STEPS calls is replayed between
+    CUDA events.  Prints one JSON line with a row per case."""
+    import math
+
+    import torch
+
+    import mxfp8_gemm_mailbox_gb300 as mx
+    import synthetic
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    peak, peak_kind = measured_peak()
+    stream = torch.cuda.Stream(device=device)
+    rows = []
+    calls_target = max(GRAPH_STEPS, args.steps)
+    for n in synthetic.SWEEP_N:
+        for k in synthetic.SWEEP_K:
+            base = synthetic.sweep_workload(8, n, k, 1)
+            w, ws = synthetic.make_weights(base)
+            W = torch.from_numpy(w).to(device)
+            WS = torch.from_numpy(ws).to(device)
+            weight_bytes = n * k + n * k // 32
+            copies = max(3, math.ceil(2.2 * L2_BYTES / weight_bytes))
+            for s in synthetic.SWEEP_S:
+                mb = mx.Mailbox(8, n, device=device)
+                gemms = [mx.PublishGemm(W, WS, mb, split_k=s, stream=stream)
+                         for _ in range(copies)]
+                cfg = gemms[0].config()
+                out = torch.empty((8, n), dtype=torch.bfloat16, device=device)
+                calls = copies * math.ceil(GRAPH_STEPS / copies)
+                for m in synthetic.SWEEP_M:
+                    wl = synthetic.sweep_workload(m, n, k, s)
+                    x, xs = synthetic.make_activations(wl)
+                    X = torch.from_numpy(x).to(device)
+                    XS = torch.from_numpy(xs).to(device)
+                    for g in gemms:
+                        g.precompile(m)
+                    with torch.cuda.stream(stream):
+                        for i in range(calls):
+                            gemms[i % copies].run(X, XS)
+                            mb.consume(m, out)
+                        stream.synchronize()
+                        graph = torch.cuda.CUDAGraph()
+                        with torch.cuda.graph(graph, stream=stream):
+                            for i in range(calls):
+                                gemms[i % copies].run(X, XS)
+                                mb.consume(m, out)
+                        for _ in range(max(3, args.warmup // calls)):
+                            graph.replay()
+                        replays = max(1, calls_target // calls)
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        for _ in range(replays):
+                            graph.replay()
+                        e1.record(stream)
+                    stream.synchronize()
+                    status, words = mb.status(stream)
+                    if status != mx.OK:
+                        raise RuntimeError(f"mailbox status {status} ({words}) at m={m} N={n} "
+                                           f"K={k} S={s}")
+                    us = e0.elapsed_time(e1) * 1e3 / (replays * calls)
+                    gbs = weight_bytes / (us * 1e-6) / 1e9
+                    rows.append({"m": m, "n": n, "k": k, "split_k": s, "us_per_call": round(us, 3),
+                                 "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                                 "stages": cfg["stages"], "grid_ctas": cfg["grid_ctas"],
+                                 "copies": copies})
+                    del graph
+                for g in gemms:
+                    g.close()
+                del gemms
+                torch.cuda.synchronize(device)
+                torch.cuda.empty_cache()
+    best = max(rows, key=lambda r: r["gbs"])
+    line = {
+        "metric": "us/call and weight-stream HBM GB/s of the chain, every sweep case",
+        "value": best["gbs"],
+        "unit": UNIT,
+        "n_gpus": 1,
+        "higher_is_better": True,
+        "dtype": "e4m3",
+        "data": "synthetic (sweep recipe: signed x row pairs, duplicated and zero W rows, "
+                "scale exponents in [-6, 3])",
+        "config": {"workload": "sweep m 1..8 x N {2048, 4096, 7168} x K {2048, 4096, 8192, "
+                               "16384} x S {1, 2, 4}",
+                   "timing": "one CUDA graph of >= 30 chained calls per case, rotating weight "
+                             "copies > 2 x L2"},
+        "peak": peak, "peak_kind": peak_kind,
+        "rows": rows,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
     elif args.path == "protocols":
         run_protocols(args)
+    elif args.path == "sweep":
+        run_sweep(args)
     else:
         run_ours(args)
 

@@ -11,13 +11,17 @@ constexpr int kBlockN = 128;      // output columns per CTA: the MMA's M
 constexpr int kRows = 8;          // activation rows per tile: the MMA's N
 constexpr int kTileK = 128;       // K elements per stage: one 128-byte swizzle row
 constexpr int kSfPerTile = 4;     // scale blocks of 32 per stage
-constexpr int kThreads = 192;     // warp 0 loads, warp 1 issues MMAs, warps 2-5 epilogue
+// Warp 0 loads, warps 1 and 6 issue MMAs (even and odd stages), warps 2-5
+// run the epilogue.
+constexpr int kMmaIssuers = 2;
+constexpr int kThreads = 192 + 32 * (kMmaIssuers - 1);
 constexpr int kSfChunkBytes = 512;
 constexpr int kWTileBytes = kBlockN * kTileK;  // 16384
 constexpr int kXTileBytes = kRows * kTileK;    // 1024
 constexpr int kGenerations = 3;
 constexpr uint32_t kSentinel = 0x80000000u;
 constexpr int kMaxStages = 16;
+constexpr int kProducerLanes = 2;  // lanes of the producer warp issuing stage copies
 constexpr int kMaxTilesPerSplit = 256;
 constexpr int kMaxAccRing = 8;    // accumulator slots in tensor memory (one stage each)
 

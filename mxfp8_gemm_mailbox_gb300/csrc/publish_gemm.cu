@@ -18,12 +18,14 @@
 // compensated FP32 pair (hi + lo, Knuth's TwoSum) as soon as it completes.
 // The pair is widened to FP64 and rounded once to BF16.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: W tile + W scale chunk per stage (started
-//               before the programmatic grid wait), x tile (after it).
-//   warp 1      tensor-memory allocation; one thread issues, per stage,
-//               tcgen05.cp of the W and x scale chunks and one block-scaled
-//               tcgen05.mma per 32-wide K block.
+// Warp roles (224 threads):
+//   warp 0      TMA producer: two lanes, alternate stages; per stage the W
+//               tile + W scale chunk (started before the programmatic grid
+//               wait) and the x tile (after it).
+//   warps 1, 6  MMA issuers, alternate stages (warp 1 also allocates tensor
+//               memory): one thread each issues, per stage, tcgen05.cp of the
+//               W and x scale chunks and one block-scaled tcgen05.mma per
+//               32-wide K block.
 //   warps 2-5   epilogue: x scales staged for the copies, partial sums read
 //               back (tcgen05.ld 32x32b: thread = output column, registers =
 //               tokens) and folded into the compensated sums, split-K
@@ -45,6 +47,10 @@ namespace mxfp8 {
 namespace {
 
 constexpr uint32_t kStageTxBytes = kWTileBytes + kXTileBytes + kSfChunkBytes;
+static_assert(kMaxAccRing % kMmaIssuers == 0 && 4 % kMmaIssuers == 0,
+              "each accumulator slot must belong to one MMA issuer");
+static_assert(kThreads == 192 + 32 * (kMmaIssuers - 1) && kMmaIssuers <= 2,
+              "warps 1 and 6 are the MMA issuers; warps 2-5 the epilogue");
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling: A and B E4M3
 // (format 0), both K-major, N = 8 (bits 17-22: N >> 3), E8M0 scales (bit 23),
@@ -193,9 +199,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = misc[0];
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
-      ptx::launch_dependents();
+    // -------------------------------------------------------------- producer
+    // The bulk copies one thread issues are served one after another (about
+    // 43 GB/s from HBM per issuing thread, whatever the ring depth), so the
+    // stages are dealt round robin to kProducerLanes lanes: lane l issues the
+    // W tile, W scale chunk and x tile of stages l, l + P, l + 2P, ...
+    const int producers = min(kProducerLanes, stages);
+    if (lane == 0) ptx::launch_dependents();
+    if (lane < producers) {
       const uint64_t pol_stream = ptx::policy_evict_first();
       const uint64_t pol_keep = ptx::policy_evict_last();
       const int npre = min(stages, nkt);
@@ -209,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tma_load_2d(dst, &tmap_w, kt * kTileK, tile * kBlockN, bar, pol_stream);
       };
       // W and its scales do not depend on the previous kernel: start them now.
-      for (int i = 0; i < npre; ++i) {
+      for (int i = lane; i < npre; i += producers) {
         const uint32_t full = bar_full + 8u * i;
         const int kt = kt_begin + i;
         ptx::mbar_arrive_expect_tx(full, kStageTxBytes);
@@ -221,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Warm L2 with the stages that come after the ring, so HBM keeps
       // streaming while the previous kernel finishes and the grid wait holds.
       const int nwarm = min(nkt, npre + p.l2_prefetch);
-      if (nwarm > npre) {
+      if (lane == 0 && nwarm > npre) {
         if (p.w_tiled != nullptr) {
           ptx::prefetch_l2(p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt_begin + npre) *
                                            kWTileBytes,
@@ -236,14 +247,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // The activations follow the programmatic grid wait.
       ptx::grid_dependency_wait();
-      for (int i = 0; i < npre; ++i)
+      for (int i = lane; i < npre; i += producers)
         ptx::tma_load_2d(sbase + L.x + i * kXTileBytes, &tmap_x, (kt_begin + i) * kTileK, 0,
                          bar_full + 8u * i, pol_keep);
-      int issued = npre;
       // From here every slot is on its second or later use: wait until the
-      // MMAs of its previous use released it.
-      RingCursor ring{0, 1u};
-      for (int i = npre; i < nkt; ++i, ring.next(stages)) {
+      // MMAs of its previous use released it.  This lane's stages advance the
+      // ring by `producers` slots at a time.
+      int issued = -1;  // the last stage this lane issued
+      for (int i = lane; i < npre; i += producers) issued = i;
+      const int first = npre + ((lane - npre % producers) % producers + producers) % producers;
+      RingCursor ring{first - npre, 1u};  // npre == stages whenever this loop runs
+      for (int i = first; i < nkt; i += producers) {
         const int s = ring.slot;
         if (!ptx::mbar_wait(bar_empty + 8u * s, ring.phase ^ 1u, p.wait_limit_ns)) {
           raise_flag(p.state, 0x2u);
@@ -257,17 +271,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                        p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt) * kSfChunkBytes,
                        kSfChunkBytes, full, pol_stream);
         ptx::tma_load_2d(sbase + L.x + s * kXTileBytes, &tmap_x, kt * kTileK, 0, full, pol_keep);
-        issued = i + 1;
+        issued = i;
+        ring.slot += producers;
+        if (ring.slot >= stages) {
+          ring.slot -= stages;
+          ring.phase ^= 1u;
+        }
       }
-      // Copies still in flight land before the CTA leaves (immediate when the
-      // MMA consumed them, which is the normal case).
-      for (int i = max(0, issued - stages); i < issued; ++i)
+      // This lane's copies still in flight land before the CTA leaves
+      // (immediate when the MMAs consumed them, which is the normal case):
+      // its stages among the last `stages` of the split, the latest use of
+      // their slots (no stage past nkt - 1 reuses them, so each wait is on
+      // the phase of this lane's own copy).
+      for (int i = issued; i >= max(0, nkt - stages); i -= producers)
         ptx::mbar_wait(bar_full + 8u * (i % stages), static_cast<uint32_t>(i / stages) & 1u,
                        p.wait_limit_ns);
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp >= 6) {
     if (lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
+      // --------------------------------------------------------- MMA issuers
+      // tcgen05 instructions cost their issuing thread a fixed time each
+      // (about 65 ns per stage of 2 copies, 4 MMAs and 2 commits), which caps
+      // one thread near 65 GB/s of weight, so two warps share the stages:
+      // issuer j takes stages j, j + kMmaIssuers, ...  Accumulator slots
+      // alternate with the stages (the ring size is even), so each slot has
+      // one issuer; a scale slot may pass between issuers, ordered by its
+      // stage's empty/full barriers.
+      const int issuer = warp == 1 ? 0 : warp - 5;
       ptx::grid_dependency_wait();
       bool ok = true;
       if (nkt > 0) {
@@ -276,7 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
       }
       RingCursor stage{0, 0u}, acc{0, 0u};
-      for (int i = 0; i < nkt && ok; ++i, stage.next(stages), acc.next(acc_ring)) {
+      for (int q = 0; q < issuer; ++q) {
+        stage.next(stages);
+        acc.next(acc_ring);
+      }
+      for (int i = issuer; i < nkt && ok; i += kMmaIssuers) {
         const int s = stage.slot;
         const int r = acc.slot;
         if (!ptx::mbar_wait(bar_full + 8u * s, stage.phase, p.wait_limit_ns) ||
@@ -305,10 +339,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mma_commit(bar_empty + 8u * s);
         ptx::mma_commit(bar_acc_full + 8u * r);
+        for (int q = 0; q < kMmaIssuers; ++q) {
+          stage.next(stages);
+          acc.next(acc_ring);
+        }
       }
     }
   }
-  if (warp < 2) {
+  if (warp < 2 || warp >= 6) {
     __syncwarp();
     if (S > 1) ptx::cluster_sync();  // matches the epilogue's barrier before the exchange
   } else {
