@@ -231,10 +231,28 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::
           : "memory");
 }
+// The two halves of a cluster barrier, for a wait placed well after the
+// arrival (every thread of every CTA of the cluster arrives once per phase).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
+}
+// Store 16 bytes (16-byte aligned) into a peer CTA's shared memory; the byte
+// count completes on the peer's mbarrier.
+__device__ __forceinline__ void st_async_remote_v4(uint32_t remote_addr, uint4 v,
+                                                   uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(remote_addr),
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+      : "memory");
 }
 // Store one word into a peer CTA's shared memory; the byte count completes on
 // the peer's mbarrier.

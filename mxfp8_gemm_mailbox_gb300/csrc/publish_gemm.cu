@@ -16,7 +16,8 @@
 // early: each MMA (or each group of acc_blocks MMAs) writes a fresh
 // accumulator slot of a ring, and the epilogue warps fold every slot into a
 // compensated FP32 pair (hi + lo, Knuth's TwoSum) as soon as it completes.
-// The pair is widened to FP64 and rounded once to BF16.
+// The pair is rounded once to BF16 (hi + lo taken exactly, from its FP32
+// bits).
 //
 // Warp roles (224 threads):
 //   warp 0      TMA producer: two lanes, alternate stages; per stage the W
@@ -90,39 +91,31 @@ __device__ __forceinline__ void two_sum_add(float& hi, float& lo, float v) {
   lo = __fadd_rn(lo, err);
 }
 
-// A double rounded once to BF16 bits, to nearest with ties to even, from the
-// two formats' bit layouts (BF16: 8 exponent bits, bias 127, 7 stored
-// mantissa bits; subnormal quantum 2^-133).
-__device__ __forceinline__ uint16_t bf16_bits_from_double(double v) {
-  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(v));
-  const uint32_t sign = static_cast<uint32_t>(b >> 63) << 15;
-  const int exp = static_cast<int>((b >> 52) & 0x7FF);
-  const unsigned long long mant = b & ((1ull << 52) - 1);
-  if (exp == 0x7FF) return static_cast<uint16_t>(sign | (mant ? 0x7FC0u : 0x7F80u));
-  if (exp == 0) return static_cast<uint16_t>(sign);  // below 2^-1022: rounds to zero
-  int e = exp - 1023;
-  if (e >= -126) {
-    unsigned long long keep = mant >> 45;
-    const unsigned long long rest = mant & ((1ull << 45) - 1);
-    const unsigned long long half = 1ull << 44;
-    if (rest > half || (rest == half && (keep & 1ull))) ++keep;
-    if (keep == 128) {
-      keep = 0;
-      ++e;
-    }
-    if (e > 127) return static_cast<uint16_t>(sign | 0x7F80u);
-    return static_cast<uint16_t>(sign | (static_cast<uint32_t>(e + 127) << 7) |
-                                 static_cast<uint32_t>(keep));
-  }
-  // Subnormal in BF16: units of 2^-133 = significand * 2^(e + 81).
-  const unsigned long long sig = mant | (1ull << 52);
-  const int drop = -(e + 81);  // >= 46
-  if (drop > 54) return static_cast<uint16_t>(sign);
-  unsigned long long q = sig >> drop;
-  const unsigned long long rest = sig & ((1ull << drop) - 1);
-  const unsigned long long half = 1ull << (drop - 1);
-  if (rest > half || (rest == half && (q & 1ull))) ++q;
-  return static_cast<uint16_t>(sign | static_cast<uint32_t>(q));  // q == 128 is 2^-126
+// BF16 bits of the exact value hi + lo, rounded once to nearest with ties to
+// even.  TwoSum gives s = fl(hi + lo) and the exact remainder e with
+// |e| <= ulp(s) / 2.  A BF16 midpoint has low 16 bits 0x8000 in FP32, and
+// every other FP32 value lies at least one FP32 ulp from the nearest midpoint,
+// so s + e rounds as s does unless s is itself a midpoint; there the sign of
+// e decides (towards it: away from the midpoint in that direction), and e = 0
+// is a true tie.  BF16 being the upper half of FP32, this covers subnormals
+// and overflow to infinity alike.
+__device__ __forceinline__ uint16_t bf16_bits_from_pair(float hi, float lo) {
+  const float s = __fadd_rn(hi, lo);
+  const float bp = __fsub_rn(s, hi);
+  const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(lo, bp));
+  const uint32_t b = __float_as_uint(s);
+  if ((b & 0x7F800000u) == 0x7F800000u)  // infinity, or NaN (kept quiet)
+    return static_cast<uint16_t>((b >> 16) | ((b & 0x007FFFFFu) != 0u ? 0x0040u : 0u));
+  const uint32_t low = b & 0xFFFFu;
+  const uint32_t keep = b >> 16;  // sign, exponent and the 7 kept mantissa bits
+  bool up;
+  if (low != 0x8000u)
+    up = low > 0x8000u;
+  else if (e == 0.0f)
+    up = (keep & 1u) != 0u;
+  else
+    up = (__float_as_uint(e) >> 31) == (b >> 31);  // e points away from zero
+  return static_cast<uint16_t>(keep + (up ? 1u : 0u));  // magnitude + 1 ulp
 }
 
 // Position in a ring of mbarrier-guarded slots: the slot and the parity of
@@ -348,7 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp < 2 || warp >= 6) {
     __syncwarp();
-    if (S > 1) ptx::cluster_sync();  // matches the epilogue's barrier before the exchange
+    if (S > 1) {
+      ptx::cluster_sync();    // matches the epilogue's barrier before the exchange
+      ptx::cluster_arrive();  // these warps address no peer: the final barrier's arrival
+    }
   } else {
     // ------------------------------------------------------------- epilogue
     const int etid = tid - 64;               // 0..127
@@ -426,34 +422,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Split-K: every CTA sends the (hi, lo) pairs of the tokens it does not
     // own to their owners, then sums the S pairs of its own tokens in K-slice
-    // order.  A split with no K tiles contributes zeros.
+    // order.  A split with no K tiles contributes zeros.  The receive buffer
+    // is [sender][column][token][hi, lo]: one CTA's pairs for one column are
+    // 8 * kShard contiguous bytes, sent as 16-byte stores.
     constexpr int kShard = kRows / S;
-    double owned[kShard];
+    static_assert(S == 1 || kShard % 2 == 0, "pairs travel two tokens per 16-byte store");
+    float own_hi[kShard], own_lo[kShard];
     if constexpr (S > 1) {
+      constexpr int kPairBytes = kShard * 8;
       // The receive buffer lives in the W ring, which is dead only once every
       // CTA of the cluster has finished its main loop.
       ptx::cluster_sync();
       if (etid == 0)
         ptx::mbar_arrive_expect_tx(bar_recv,
-                                   static_cast<uint32_t>((S - 1) * kShard * kBlockN * 8));
+                                   static_cast<uint32_t>((S - 1) * kBlockN * kPairBytes));
 #pragma unroll
       for (int peer = 0; peer < S; ++peer) {
         if (peer == static_cast<int>(split)) continue;
         const int sender = static_cast<int>(split) < peer ? static_cast<int>(split)
                                                           : static_cast<int>(split) - 1;
         const uint32_t remote_bar = ptx::map_to_rank(bar_recv, peer);
+        const uint32_t remote =
+            ptx::map_to_rank(sbase + L.recv + (sender * kBlockN + col) * kPairBytes, peer);
 #pragma unroll
-        for (int jj = 0; jj < kShard; ++jj) {
-          const uint32_t local =
-              sbase + L.recv + (((sender * kShard + jj) * kBlockN + col) * 2) * 4;
-          ptx::st_async_remote(ptx::map_to_rank(local, peer),
-                               __float_as_uint(hi[peer * kShard + jj]), remote_bar);
-          ptx::st_async_remote(ptx::map_to_rank(local + 4, peer),
-                               __float_as_uint(lo[peer * kShard + jj]), remote_bar);
-        }
+        for (int jj = 0; jj < kShard; jj += 2)
+          ptx::st_async_remote_v4(
+              remote + jj * 8,
+              make_uint4(__float_as_uint(hi[peer * kShard + jj]),
+                         __float_as_uint(lo[peer * kShard + jj]),
+                         __float_as_uint(hi[peer * kShard + jj + 1]),
+                         __float_as_uint(lo[peer * kShard + jj + 1])),
+              remote_bar);
       }
+      // This thread addresses no peer after its sends: its half of the final
+      // cluster barrier, whose wait comes before the CTA exits.
+      ptx::cluster_arrive();
       if (!ptx::mbar_wait_cluster(bar_recv, 0, p.wait_limit_ns)) raise_flag(p.state, 0x2u);
-      const float* recv = reinterpret_cast<const float*>(smem + L.recv);
+      const uint8_t* recv = smem + L.recv;
 #pragma unroll
       for (int jj = 0; jj < kShard; ++jj) {
         float sh = 0.0f, sl = 0.0f;
@@ -471,34 +476,44 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
           } else {
             const int sidx = src < static_cast<int>(split) ? src : src - 1;
-            const float* pair = recv + ((sidx * kShard + jj) * kBlockN + col) * 2;
-            vh = pair[0];
-            vl = pair[1];
+            const float2 pair = *reinterpret_cast<const float2*>(
+                recv + (sidx * kBlockN + col) * kPairBytes + jj * 8);
+            vh = pair.x;
+            vl = pair.y;
           }
           two_sum_add(sh, sl, vh);
           sl = __fadd_rn(sl, vl);
         }
-        owned[jj] = static_cast<double>(sh) + static_cast<double>(sl);
+        own_hi[jj] = sh;
+        own_lo[jj] = sl;
       }
     } else {
 #pragma unroll
-      for (int jj = 0; jj < kShard; ++jj)
-        owned[jj] = static_cast<double>(hi[jj]) + static_cast<double>(lo[jj]);
+      for (int jj = 0; jj < kShard; ++jj) {
+        own_hi[jj] = hi[jj];
+        own_lo[jj] = lo[jj];
+      }
     }
 
     // The global scale (gemm page, epilog_warp with use_scale: the
     // accumulator times mScale[0]) multiplies the compensated sum before its
-    // one rounding.  It is read after the grid wait like x.
+    // one rounding: alpha * hi exactly as a product and its FMA error, plus
+    // alpha * lo.  It is read after the grid wait like x.
     if (p.alpha != nullptr) {
-      const double a = static_cast<double>(*p.alpha);
+      const float a = *p.alpha;
 #pragma unroll
-      for (int jj = 0; jj < kShard; ++jj) owned[jj] *= a;
+      for (int jj = 0; jj < kShard; ++jj) {
+        const float ph = __fmul_rn(a, own_hi[jj]);
+        const float pe = __fmaf_rn(a, own_hi[jj], -ph);
+        own_lo[jj] = __fmaf_rn(a, own_lo[jj], pe);
+        own_hi[jj] = ph;
+      }
     }
 
     uint16_t* ctile = reinterpret_cast<uint16_t*>(smem + L.ctile);  // [kShard][128]
 #pragma unroll
     for (int jj = 0; jj < kShard; ++jj)
-      ctile[jj * kBlockN + col] = bf16_bits_from_double(owned[jj]);
+      ctile[jj * kBlockN + col] = bf16_bits_from_pair(own_hi[jj], own_lo[jj]);
     epilogue_barrier();
 
     const uint32_t g = misc[1];
@@ -531,8 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   if (S > 1) {
+    // No CTA leaves while a peer may still address it: every thread arrived
+    // after its last remote store, and this CTA's own receive barrier
+    // completed, so the wait is normally immediate.
     __syncwarp();
-    ptx::cluster_sync();  // no CTA leaves while a peer may still address it
+    ptx::cluster_wait();
   }
   if (warp == 1) {
     ptx::tc_fence_after();
