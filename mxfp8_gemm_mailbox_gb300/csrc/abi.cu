@@ -145,8 +145,8 @@ mxfp8_status device_limits(int device, DeviceLimits* out) {
 }
 
 // Fill split_k, cta_k and stages: split_k so the grid has about one or two
-// CTAs per SM; the deepest ring that still lets the intended number of CTAs
-// share an SM.
+// CTAs per SM; the deepest even ring (two producer lanes and two MMA issuers
+// need an even one) that still lets the intended number of CTAs share an SM.
 mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
   const int tiles = d->n / kBlockN;
   const int k_tiles = k_tiles_of(d->k);
@@ -174,6 +174,8 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
       if (s >= tps) break;  // more stages than K tiles buy nothing
     }
     if (best == 0) return fail(MXFP8_ERR_UNSUPPORTED, "no stage count fits in shared memory");
+    // An even ring runs two producer lanes and two MMA issuers.
+    if (best > 2 && best % 2 != 0) --best;
     d->stages = best;
   }
   if (static_cast<int>(gemm_smem_layout(d->stages, d->split_k, tps).total) > lim.smem_optin)

@@ -62,6 +62,10 @@ __global__ void __launch_bounds__(kConsumeThreads)
   // to arrive advances the next generation and clears the count.  Each
   // thread loads its pack from all three generations alongside the state
   // word (one memory round trip instead of two) and keeps the active one.
+  // No CTA of this grid reads the word the last one advances (state[0] is
+  // read by the next publisher, after this grid completes), so the count
+  // needs atomicity only: a relaxed add, issued with the loads instead of
+  // after them.
   const int packs_per_row = n / 8;
   const int pack = blockIdx.x * kConsumeThreads + threadIdx.x;
   const bool active = pack < m * packs_per_row;
@@ -69,6 +73,8 @@ __global__ void __launch_bounds__(kConsumeThreads)
   const int c8 = active ? pack % packs_per_row : 0;
   const size_t generation_stride = static_cast<size_t>(capacity) * n;
   uint16_t* slot0 = mailbox + static_cast<size_t>(t) * n + c8 * 8;
+  uint32_t before = 0;
+  if (threadIdx.x == 0) before = ptx::atom_add_relaxed(state + 2, 1u);
   const uint32_t g = ptx::ld_volatile_u32(state + 1);
   uint4 candidates[kGenerations];
   if (active) {
@@ -77,7 +83,6 @@ __global__ void __launch_bounds__(kConsumeThreads)
       candidates[gg] = ptx::ld_volatile_v4(slot0 + gg * generation_stride);
   }
   if (threadIdx.x == 0) {
-    const uint32_t before = ptx::atom_add_acq_rel(state + 2, 1u);
     if (before == gridDim.x - 1) {
       if (g < static_cast<uint32_t>(kGenerations)) {
         state[0] = static_cast<int32_t>((g + 1u) % kGenerations);

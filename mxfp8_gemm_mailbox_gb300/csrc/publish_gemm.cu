@@ -20,13 +20,13 @@
 // bits).
 //
 // Warp roles (224 threads):
-//   warp 0      TMA producer: two lanes, alternate stages; per stage the W
-//               tile + W scale chunk (started before the programmatic grid
-//               wait) and the x tile (after it).
-//   warps 1, 6  MMA issuers, alternate stages (warp 1 also allocates tensor
-//               memory): one thread each issues, per stage, tcgen05.cp of the
-//               W and x scale chunks and one block-scaled tcgen05.mma per
-//               32-wide K block.
+//   warp 0      TMA producer: two lanes taking alternate stages (one lane on
+//               an odd ring); per stage the W tile + W scale chunk (started
+//               before the programmatic grid wait) and the x tile (after it).
+//   warps 1, 6  MMA issuers taking alternate stages (warp 1 alone on an odd
+//               ring; it also allocates tensor memory): one thread each
+//               issues, per stage, tcgen05.cp of the W and x scale chunks and
+//               one block-scaled tcgen05.mma per 32-wide K block.
 //   warps 2-5   epilogue: x scales staged for the copies, partial sums read
 //               back (tcgen05.ld 32x32b: thread = output column, registers =
 //               tokens) and folded into the compensated sums, split-K
@@ -48,8 +48,8 @@ namespace mxfp8 {
 namespace {
 
 constexpr uint32_t kStageTxBytes = kWTileBytes + kXTileBytes + kSfChunkBytes;
-static_assert(kMaxAccRing % kMmaIssuers == 0 && 4 % kMmaIssuers == 0,
-              "each accumulator slot must belong to one MMA issuer");
+static_assert(kMaxAccRing % 2 == 0 && kMmaIssuers == 2 && kProducerLanes == 2,
+              "stage i belongs to producer lane and MMA issuer i % 2 on even rings");
 static_assert(kThreads == 192 + 32 * (kMmaIssuers - 1) && kMmaIssuers <= 2,
               "warps 1 and 6 are the MMA issuers; warps 2-5 the epilogue");
 
@@ -152,6 +152,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkt = max(0, kt_end - kt_begin);
   const int stages = p.stages;
   const bool per_block = p.acc_blocks == 1;
+  // Two producer lanes and two MMA issuers share the ring only when it has an
+  // even number of slots: then stage i, its slot i % stages, its scale slots
+  // and its accumulator slot (the accumulator ring is even too) all belong to
+  // lane / issuer i % 2, so every mbarrier is waited on by one thread in use
+  // order.  With an odd ring a slot would alternate between issuers, and one
+  // could wait on use u + 1 of a slot before use u completed, when the phase
+  // parity it tests still shows the phase before (the parity aliases).
+  const int pipes = (stages % 2 == 0) ? 2 : 1;
 
   const uint32_t bar_full = sbase + L.bars;                     // [stages]
   const uint32_t bar_empty = bar_full + 8u * stages;            // [stages]
@@ -194,10 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // -------------------------------------------------------------- producer
     // The bulk copies one thread issues are served one after another (about
-    // 43 GB/s from HBM per issuing thread, whatever the ring depth), so the
-    // stages are dealt round robin to kProducerLanes lanes: lane l issues the
-    // W tile, W scale chunk and x tile of stages l, l + P, l + 2P, ...
-    const int producers = min(kProducerLanes, stages);
+    // 43 GB/s from HBM per issuing thread, whatever the ring depth), so on an
+    // even ring lane l of two issues the W tile, W scale chunk and x tile of
+    // stages l, l + 2, l + 4, ...
+    const int producers = min(kProducerLanes, pipes);
     if (lane == 0) ptx::launch_dependents();
     if (lane < producers) {
       const uint64_t pol_stream = ptx::policy_evict_first();
@@ -281,16 +289,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                        p.wait_limit_ns);
     }
   } else if (warp == 1 || warp >= 6) {
-    if (lane == 0) {
+    const int issuer = warp == 1 ? 0 : warp - 5;
+    if (lane == 0 && issuer < pipes) {
       // --------------------------------------------------------- MMA issuers
       // tcgen05 instructions cost their issuing thread a fixed time each
       // (about 65 ns per stage of 2 copies, 4 MMAs and 2 commits), which caps
-      // one thread near 65 GB/s of weight, so two warps share the stages:
-      // issuer j takes stages j, j + kMmaIssuers, ...  Accumulator slots
-      // alternate with the stages (the ring size is even), so each slot has
-      // one issuer; a scale slot may pass between issuers, ordered by its
-      // stage's empty/full barriers.
-      const int issuer = warp == 1 ? 0 : warp - 5;
+      // one thread near 65 GB/s of weight, so with an even ring two warps
+      // share the stages: issuer j takes stages j, j + 2, ...
       ptx::grid_dependency_wait();
       bool ok = true;
       if (nkt > 0) {
@@ -303,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         stage.next(stages);
         acc.next(acc_ring);
       }
-      for (int i = issuer; i < nkt && ok; i += kMmaIssuers) {
+      for (int i = issuer; i < nkt && ok; i += pipes) {
         const int s = stage.slot;
         const int r = acc.slot;
         if (!ptx::mbar_wait(bar_full + 8u * s, stage.phase, p.wait_limit_ns) ||
@@ -332,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mma_commit(bar_empty + 8u * s);
         ptx::mma_commit(bar_acc_full + 8u * r);
-        for (int q = 0; q < kMmaIssuers; ++q) {
+        for (int q = 0; q < pipes; ++q) {
           stage.next(stages);
           acc.next(acc_ring);
         }

@@ -110,6 +110,38 @@ def test_every_ring_depth(cuda, stages):
     assert (c == want).all()
 
 
+@pytest.mark.parametrize("stages", [2, 4, 5, 7, 10])
+def test_short_rings_over_a_long_k_loop(cuda, stages):
+    """128 K tiles per CTA through a short ring, ten chained calls: even
+    rings run two producer lanes and two MMA issuers (each slot owned by
+    one of each), odd rings one of each; every call bit-exact."""
+    n, k = 1024, 16384
+    w, ws, x, xs = synthetic.integer_operands(n, k, 8, seed=100 + stages)
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    mb = Mailbox(8, n)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=1, stages=stages)
+    assert g.config()["stages"] == stages
+    X, XS = dev(x), dev(xs)
+    for call in range(10):
+        c = torch.full((8, n), 0x7FFF, dtype=torch.int16, device="cuda")
+        g.run(X, XS, c)
+        out = mb.consume(8)
+        torch.cuda.synchronize()
+        assert (bits(c) == want).all(), f"C, call {call}"
+        assert (bits(out) == sanitized(want)).all(), f"consumer output, call {call}"
+    assert mb.status()[0] == OK and state_words(mb) == [10 % 3, 9 % 3, 0, 0]
+    g.close()
+
+
+def test_default_rings_are_even(cuda):
+    for n, k, split in [(2048, 16384, 1), (4096, 4096, 1), (7168, 8192, 2), (7168, 16384, 4)]:
+        w = torch.zeros((n, k), dtype=torch.uint8, device="cuda")
+        ws = torch.full((n, k // 32), 127, dtype=torch.uint8, device="cuda")
+        g = PublishGemm(w, ws, Mailbox(8, n), split_k=split)
+        assert g.config()["stages"] % 2 == 0
+        g.close()
+
+
 def test_ring_too_deep_for_shared_memory_is_refused(cuda):
     w, ws, x, xs = synthetic.integer_operands(256, 4096, 8, seed=1)
     with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED"):
