@@ -468,7 +468,7 @@ def run_ours(args):
             },
             "gpu_launches": 2 * steps,
             "tactic": {k: cfg[k] for k in ("split_k", "stages", "acc_blocks", "w_layout",
-                                            "l2_prefetch", "tmem_columns")},
+                                            "l2_prefetch", "pipes", "tmem_columns")},
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)

@@ -83,6 +83,12 @@ typedef struct mxfp8_gemm_desc {
   int32_t w_layout;   /* MXFP8_W_IN_PLACE or MXFP8_W_TILED (0 = choose)              */
   int32_t l2_prefetch;/* W stages past the ring each CTA warms in L2 before its grid
                          wait: 0..64 (0 = none, the measured best on GB300)           */
+  int32_t pipes;      /* producer lanes and MMA-issuing warps sharing the ring: 1, 2
+                         or 4, dividing `stages` (stage i and its ring slots belong to
+                         pipe i % pipes).  0 = choose: 4 when the grid has at most one
+                         CTA per SM and 4 divides the ring, else 2 on an even ring, else
+                         1.  One thread's bulk copies and tensor-core instructions are
+                         served one after another, so few-CTA grids need several.     */
 } mxfp8_gemm_desc;
 
 /* Where the GEMM streams W from.  IN_PLACE: the caller's [N][K] buffer,

@@ -112,6 +112,8 @@ mxfp8_status check_desc(const mxfp8_gemm_desc* d) {
     return fail(MXFP8_ERR_UNSUPPORTED, "w_layout must be MXFP8_W_IN_PLACE or MXFP8_W_TILED");
   if (d->l2_prefetch < 0 || d->l2_prefetch > 64)
     return fail(MXFP8_ERR_UNSUPPORTED, "l2_prefetch must be in 0..64");
+  if (d->pipes != 0 && d->pipes != 1 && d->pipes != 2 && d->pipes != 4)
+    return fail(MXFP8_ERR_UNSUPPORTED, "pipes must be 1, 2 or 4 (or 0 to choose)");
   return MXFP8_OK;
 }
 
@@ -144,9 +146,11 @@ mxfp8_status device_limits(int device, DeviceLimits* out) {
   return MXFP8_OK;
 }
 
-// Fill split_k, cta_k and stages: split_k so the grid has about one or two
-// CTAs per SM; the deepest even ring (two producer lanes and two MMA issuers
-// need an even one) that still lets the intended number of CTAs share an SM.
+// Fill split_k, cta_k, stages and pipes: split_k so the grid has about one or
+// two CTAs per SM; the deepest ring that still lets the intended number of
+// CTAs share an SM, rounded so the pipes divide it: with at most one CTA per
+// SM each CTA must stream fast, so 4 pipes (ring a multiple of 4); with two,
+// HBM is the limit and 2 pipes suffice (more in flight measured slower).
 mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
   const int tiles = d->n / kBlockN;
   const int k_tiles = k_tiles_of(d->k);
@@ -174,14 +178,20 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
       if (s >= tps) break;  // more stages than K tiles buy nothing
     }
     if (best == 0) return fail(MXFP8_ERR_UNSUPPORTED, "no stage count fits in shared memory");
-    // An even ring runs two producer lanes and two MMA issuers.
-    if (best > 2 && best % 2 != 0) --best;
+    const int unit = (per_sm == 1 && best >= 4) ? 4 : (best >= 2 ? 2 : 1);
+    best -= best % unit;
     d->stages = best;
   }
   if (static_cast<int>(gemm_smem_layout(d->stages, d->split_k, tps).total) > lim.smem_optin)
     return fail(MXFP8_ERR_UNSUPPORTED, "the requested stages do not fit in shared memory");
   if (gemm_tmem_plan(d->stages, d->acc_blocks).cols > 512)
     return fail(MXFP8_ERR_UNSUPPORTED, "the requested stages do not fit in tensor memory");
+  if (d->pipes == 0) {
+    d->pipes = (per_sm == 1 && d->stages % 4 == 0) ? 4 : (d->stages % 2 == 0 ? 2 : 1);
+  } else if (d->stages % d->pipes != 0) {
+    return fail(MXFP8_ERR_UNSUPPORTED, "pipes must divide stages (stage i and its ring slots "
+                                       "belong to pipe i % pipes)");
+  }
   return MXFP8_OK;
 }
 
@@ -223,6 +233,7 @@ mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale,
   p.publish = publish ? 1 : 0;
   p.acc_blocks = g->desc.acc_blocks;
   p.l2_prefetch = g->desc.l2_prefetch;
+  p.pipes = g->desc.pipes;
   p.tmem = g->tmem;
   p.x_scale = static_cast<const uint8_t*>(x_scale);
   p.w_sf = g->w_sf;
@@ -615,6 +626,7 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
   p.publish = 1;
   p.acc_blocks = d.acc_blocks;
   p.l2_prefetch = d.l2_prefetch;
+  p.pipes = d.pipes;
   p.tmem = gemm_tmem_plan(d.stages, d.acc_blocks);
   p.x_scale = static_cast<const uint8_t*>(x_scale);
   p.w_sf = scratch;

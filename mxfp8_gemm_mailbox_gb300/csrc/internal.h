@@ -11,17 +11,17 @@ constexpr int kBlockN = 128;      // output columns per CTA: the MMA's M
 constexpr int kRows = 8;          // activation rows per tile: the MMA's N
 constexpr int kTileK = 128;       // K elements per stage: one 128-byte swizzle row
 constexpr int kSfPerTile = 4;     // scale blocks of 32 per stage
-// Warp 0 loads, warps 1 and 6 issue MMAs (even and odd stages), warps 2-5
-// run the epilogue.
-constexpr int kMmaIssuers = 2;
-constexpr int kThreads = 192 + 32 * (kMmaIssuers - 1);
+// Warp 0 loads (one lane per pipe), warp 1 and warps 6.. issue MMAs (one
+// warp per pipe), warps 2-5 run the epilogue.
+constexpr int kMaxPipes = 4;
+constexpr int kMaxThreads = 192 + 32 * (kMaxPipes - 1);
+constexpr int threads_for_pipes(int pipes) { return 160 + 32 * pipes; }
 constexpr int kSfChunkBytes = 512;
 constexpr int kWTileBytes = kBlockN * kTileK;  // 16384
 constexpr int kXTileBytes = kRows * kTileK;    // 1024
 constexpr int kGenerations = 3;
 constexpr uint32_t kSentinel = 0x80000000u;
 constexpr int kMaxStages = 16;
-constexpr int kProducerLanes = 2;  // lanes of the producer warp issuing stage copies
 constexpr int kMaxTilesPerSplit = 256;
 constexpr int kMaxAccRing = 8;    // accumulator slots in tensor memory (one stage each)
 
@@ -59,6 +59,7 @@ struct GemmParams {
   int32_t publish;          // 1: fused publish into the mailbox; 0: C only
   int32_t acc_blocks;       // 32-wide K blocks summed in TMEM per promoted partial: 1 or 4
   int32_t l2_prefetch;      // stages past the ring warmed in L2 before the grid wait
+  int32_t pipes;            // producer lanes = MMA-issuing warps (1, 2, 4; divides stages)
   TmemPlan tmem;
   const uint8_t* x_scale;   // [m][k/32]
   const uint8_t* w_sf;      // [n/128][k_tiles][512] tiled W scales

@@ -19,14 +19,14 @@
 // The pair is rounded once to BF16 (hi + lo taken exactly, from its FP32
 // bits).
 //
-// Warp roles (224 threads):
-//   warp 0      TMA producer: two lanes taking alternate stages (one lane on
-//               an odd ring); per stage the W tile + W scale chunk (started
-//               before the programmatic grid wait) and the x tile (after it).
-//   warps 1, 6  MMA issuers taking alternate stages (warp 1 alone on an odd
-//               ring; it also allocates tensor memory): one thread each
-//               issues, per stage, tcgen05.cp of the W and x scale chunks and
-//               one block-scaled tcgen05.mma per 32-wide K block.
+// Warp roles (pipes = 1, 2 or 4 per launch):
+//   warp 0      TMA producer: one lane per pipe, lane l taking stages
+//               l, l + pipes, ...; per stage the W tile + W scale chunk
+//               (started before the programmatic grid wait) and the x tile.
+//   warp 1, 6.. MMA issuers, one warp per pipe (warp 1 also allocates tensor
+//               memory): one thread each issues, per stage, tcgen05.cp of the
+//               W and x scale chunks and one block-scaled tcgen05.mma per
+//               32-wide K block.  Blocks have 160 + 32 * pipes threads.
 //   warps 2-5   epilogue: x scales staged for the copies, partial sums read
 //               back (tcgen05.ld 32x32b: thread = output column, registers =
 //               tokens) and folded into the compensated sums, split-K
@@ -48,10 +48,10 @@ namespace mxfp8 {
 namespace {
 
 constexpr uint32_t kStageTxBytes = kWTileBytes + kXTileBytes + kSfChunkBytes;
-static_assert(kMaxAccRing % 2 == 0 && kMmaIssuers == 2 && kProducerLanes == 2,
-              "stage i belongs to producer lane and MMA issuer i % 2 on even rings");
-static_assert(kThreads == 192 + 32 * (kMmaIssuers - 1) && kMmaIssuers <= 2,
-              "warps 1 and 6 are the MMA issuers; warps 2-5 the epilogue");
+static_assert(kMaxAccRing % kMaxPipes == 0 && 4 % kMaxPipes == 0,
+              "every accumulator slot belongs to one pipe");
+static_assert(threads_for_pipes(kMaxPipes) == kMaxThreads && threads_for_pipes(1) == 192,
+              "warps 0-5 always, one more MMA-issuing warp per pipe past the first");
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling: A and B E4M3
 // (format 0), both K-major, N = 8 (bits 17-22: N >> 3), E8M0 scales (bit 23),
@@ -132,7 +132,7 @@ struct RingCursor {
 };
 
 template <int S>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kMaxThreads, 1)
     publish_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_x,
                         const __grid_constant__ GemmParams p) {
@@ -152,14 +152,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkt = max(0, kt_end - kt_begin);
   const int stages = p.stages;
   const bool per_block = p.acc_blocks == 1;
-  // Two producer lanes and two MMA issuers share the ring only when it has an
-  // even number of slots: then stage i, its slot i % stages, its scale slots
-  // and its accumulator slot (the accumulator ring is even too) all belong to
-  // lane / issuer i % 2, so every mbarrier is waited on by one thread in use
-  // order.  With an odd ring a slot would alternate between issuers, and one
-  // could wait on use u + 1 of a slot before use u completed, when the phase
-  // parity it tests still shows the phase before (the parity aliases).
-  const int pipes = (stages % 2 == 0) ? 2 : 1;
+  // `pipes` producer lanes and MMA issuers share the ring, and pipes divides
+  // the ring size: then stage i, its slot i % stages, its scale slots and its
+  // accumulator slot (the accumulator ring is a multiple of 4) all belong to
+  // lane / issuer i % pipes, so every mbarrier is waited on by one thread in
+  // use order.  Were a slot to pass between issuers, one could wait on use
+  // u + 1 of it before use u completed, while the phase parity it tests still
+  // shows the phase before (the parity aliases) and the wait returns at once.
+  const int pipes = p.pipes;
 
   const uint32_t bar_full = sbase + L.bars;                     // [stages]
   const uint32_t bar_empty = bar_full + 8u * stages;            // [stages]
@@ -202,10 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // -------------------------------------------------------------- producer
     // The bulk copies one thread issues are served one after another (about
-    // 43 GB/s from HBM per issuing thread, whatever the ring depth), so on an
-    // even ring lane l of two issues the W tile, W scale chunk and x tile of
-    // stages l, l + 2, l + 4, ...
-    const int producers = min(kProducerLanes, pipes);
+    // 43 GB/s from HBM per issuing thread, whatever the ring depth), so lane
+    // l < pipes issues the W tile, W scale chunk and x tile of stages l,
+    // l + pipes, l + 2 * pipes, ...
+    const int producers = pipes;
     if (lane == 0) ptx::launch_dependents();
     if (lane < producers) {
       const uint64_t pol_stream = ptx::policy_evict_first();
@@ -294,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // --------------------------------------------------------- MMA issuers
       // tcgen05 instructions cost their issuing thread a fixed time each
       // (about 65 ns per stage of 2 copies, 4 MMAs and 2 commits), which caps
-      // one thread near 65 GB/s of weight, so with an even ring two warps
-      // share the stages: issuer j takes stages j, j + 2, ...
+      // one thread near 65 GB/s of weight, so issuer j < pipes takes stages
+      // j, j + pipes, ...
       ptx::grid_dependency_wait();
       bool ok = true;
       if (nkt > 0) {
@@ -615,7 +615,7 @@ cudaError_t launch_impl(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, co
                         cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((p.n / kBlockN) * S), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads_for_pipes(p.pipes)), 1, 1);
   cfg.dynamicSmemBytes = p.smem.total;
   cfg.stream = stream;
   cudaLaunchAttribute attrs[2];

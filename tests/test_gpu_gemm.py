@@ -112,9 +112,9 @@ def test_every_ring_depth(cuda, stages):
 
 @pytest.mark.parametrize("stages", [2, 4, 5, 7, 10])
 def test_short_rings_over_a_long_k_loop(cuda, stages):
-    """128 K tiles per CTA through a short ring, ten chained calls: even
-    rings run two producer lanes and two MMA issuers (each slot owned by
-    one of each), odd rings one of each; every call bit-exact."""
+    """128 K tiles per CTA through a short ring, ten chained calls, with the
+    default pipes for the ring (4, 2 or 1: each slot owned by one producer
+    lane and one MMA issuer); every call bit-exact."""
     n, k = 1024, 16384
     w, ws, x, xs = synthetic.integer_operands(n, k, 8, seed=100 + stages)
     want = oracle.gemm_bf16(w, ws, x, xs)
@@ -133,13 +133,45 @@ def test_short_rings_over_a_long_k_loop(cuda, stages):
     g.close()
 
 
-def test_default_rings_are_even(cuda):
-    for n, k, split in [(2048, 16384, 1), (4096, 4096, 1), (7168, 8192, 2), (7168, 16384, 4)]:
+def test_default_pipes_divide_the_ring(cuda):
+    """Grids of at most one CTA per SM get 4 pipes on a ring that is a
+    multiple of 4; the headline's two CTAs per SM get 2."""
+    for n, k, split, pipes in [(2048, 16384, 1, 4), (4096, 4096, 1, 4), (7168, 8192, 2, 4),
+                               (7168, 16384, 4, 2)]:
         w = torch.zeros((n, k), dtype=torch.uint8, device="cuda")
         ws = torch.full((n, k // 32), 127, dtype=torch.uint8, device="cuda")
         g = PublishGemm(w, ws, Mailbox(8, n), split_k=split)
-        assert g.config()["stages"] % 2 == 0
+        cfg = g.config()
+        assert cfg["pipes"] == pipes and cfg["stages"] % pipes == 0, cfg
         g.close()
+
+
+@pytest.mark.parametrize("stages,pipes", [(8, 4), (4, 4), (8, 2), (6, 2), (5, 1), (8, 1)])
+def test_every_pipe_count_over_a_long_k_loop(cuda, stages, pipes):
+    """Each pipe count (producer lanes = MMA-issuing warps) on a ring it
+    divides, 128 K tiles per CTA, five chained calls, bit-exact."""
+    n, k = 1024, 16384
+    w, ws, x, xs = synthetic.integer_operands(n, k, 8, seed=200 + stages * 8 + pipes)
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    mb = Mailbox(8, n)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=1, stages=stages, pipes=pipes)
+    assert (g.config()["stages"], g.config()["pipes"]) == (stages, pipes)
+    X, XS = dev(x), dev(xs)
+    for call in range(5):
+        c = torch.full((8, n), 0x7FFF, dtype=torch.int16, device="cuda")
+        g.run(X, XS, c)
+        out = mb.consume(8)
+        torch.cuda.synchronize()
+        assert (bits(c) == want).all(), f"C, call {call}"
+        assert (bits(out) == sanitized(want)).all(), f"consumer output, call {call}"
+    assert mb.status()[0] == OK
+    g.close()
+
+
+def test_pipes_that_do_not_divide_the_ring_are_refused(cuda):
+    w, ws, x, xs = synthetic.integer_operands(256, 4096, 8, seed=1)
+    with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED"):
+        PublishGemm(dev(w), dev(ws), Mailbox(8, 256), split_k=1, stages=6, pipes=4)
 
 
 def test_ring_too_deep_for_shared_memory_is_refused(cuda):
