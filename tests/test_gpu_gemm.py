@@ -168,6 +168,28 @@ def test_every_pipe_count_over_a_long_k_loop(cuda, stages, pipes):
     g.close()
 
 
+@pytest.mark.parametrize("w_layout", [W_IN_PLACE, W_TILED])
+@pytest.mark.parametrize("l2_prefetch", [-1, 0, 3, 40])
+def test_l2_prefetch_leaves_results_unchanged(cuda, l2_prefetch, w_layout):
+    """Warming later W stages in L2 before the grid wait (the default, 6
+    stages; none; a few; more than the CTA has) is bit-exact."""
+    n, k = 512, 8192
+    w, ws, x, xs = synthetic.integer_operands(n, k, 8, seed=300 + l2_prefetch)
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    for split in (1, 4):
+        mb = Mailbox(8, n)
+        g = PublishGemm(dev(w), dev(ws), mb, split_k=split, w_layout=w_layout,
+                        l2_prefetch=l2_prefetch)
+        assert g.config()["l2_prefetch"] == (6 if l2_prefetch == 0 else l2_prefetch)
+        c = torch.full((8, n), 0x7FFF, dtype=torch.int16, device="cuda")
+        g.run(dev(x), dev(xs), c)
+        out = mb.consume(8)
+        torch.cuda.synchronize()
+        assert (bits(c) == want).all() and (bits(out) == sanitized(want)).all()
+        assert mb.status()[0] == OK
+        g.close()
+
+
 def test_pipes_that_do_not_divide_the_ring_are_refused(cuda):
     w, ws, x, xs = synthetic.integer_operands(256, 4096, 8, seed=1)
     with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED"):
