@@ -92,6 +92,12 @@ typedef struct mxfp8_gemm_desc {
                          CTA per SM and 4 divides the ring, else 2 on an even ring, else
                          1.  One thread's bulk copies and tensor-core instructions are
                          served one after another, so few-CTA grids need several.     */
+  int32_t tmem_load;  /* how the epilogue reads accumulators out of tensor memory:
+                         MXFP8_TMEM_LOAD_32X32B (0 = this: thread = output column) or
+                         MXFP8_TMEM_LOAD_16X256B (the gemm page's default shape, with
+                         column_lanes = 1 being the 32x32b case: a thread holds 4
+                         columns x 2 tokens and one warp-local transpose follows the
+                         main loop).  The two give identical bits.                     */
 } mxfp8_gemm_desc;
 
 /* Where the GEMM streams W from.  IN_PLACE: the caller's [N][K] buffer,
@@ -101,6 +107,11 @@ typedef struct mxfp8_gemm_desc {
  * contiguous 16 KB read; the caller's w is not read after create. */
 #define MXFP8_W_IN_PLACE 1
 #define MXFP8_W_TILED 2
+
+/* Accumulator read-out shapes (tcgen05.ld), publishing_gemm page,
+ * epilog_warp (16x256b, or 32x32b when column_lanes == 1). */
+#define MXFP8_TMEM_LOAD_32X32B 1
+#define MXFP8_TMEM_LOAD_16X256B 2
 
 typedef struct mxfp8_publish_gemm mxfp8_publish_gemm; /* opaque */
 

@@ -15,6 +15,8 @@ STATUS_NAMES = {OK: "OK", ERR_INVALID: "ERR_INVALID", ERR_UNSUPPORTED: "ERR_UNSU
                 ERR_CUDA: "ERR_CUDA", ERR_TIMEOUT: "ERR_TIMEOUT", ERR_STATE: "ERR_STATE"}
 W_IN_PLACE = 1
 W_TILED = 2
+TMEM_LOAD_32X32B = 1
+TMEM_LOAD_16X256B = 2
 FLAG_POLL_TIMEOUT = 0x1
 FLAG_GEMM_TIMEOUT = 0x2
 FLAG_BAD_STATE = 0x4
@@ -33,7 +35,7 @@ _u64 = ctypes.c_uint64
 class GemmDesc(ctypes.Structure):
     _fields_ = [("n", _i32), ("k", _i32), ("capacity_m", _i32), ("split_k", _i32),
                 ("cta_k", _i32), ("stages", _i32), ("acc_blocks", _i32), ("w_layout", _i32),
-                ("l2_prefetch", _i32), ("pipes", _i32)]
+                ("l2_prefetch", _i32), ("pipes", _i32), ("tmem_load", _i32)]
 
 
 SIGNATURES = {

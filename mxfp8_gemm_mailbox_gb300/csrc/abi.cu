@@ -117,6 +117,10 @@ mxfp8_status check_desc(const mxfp8_gemm_desc* d) {
     return fail(MXFP8_ERR_UNSUPPORTED, "l2_prefetch must be in 1..64, -1 (none) or 0 (choose)");
   if (d->pipes != 0 && d->pipes != 1 && d->pipes != 2 && d->pipes != 4)
     return fail(MXFP8_ERR_UNSUPPORTED, "pipes must be 1, 2 or 4 (or 0 to choose)");
+  if (d->tmem_load != 0 && d->tmem_load != MXFP8_TMEM_LOAD_32X32B &&
+      d->tmem_load != MXFP8_TMEM_LOAD_16X256B)
+    return fail(MXFP8_ERR_UNSUPPORTED,
+                "tmem_load must be MXFP8_TMEM_LOAD_32X32B or MXFP8_TMEM_LOAD_16X256B");
   return MXFP8_OK;
 }
 
@@ -166,6 +170,7 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
   d->cta_k = kTileK;
   if (d->acc_blocks == 0) d->acc_blocks = 4;
   if (d->l2_prefetch == 0) d->l2_prefetch = kDefaultL2Prefetch;
+  if (d->tmem_load == 0) d->tmem_load = MXFP8_TMEM_LOAD_32X32B;
   d->w_layout = resolved_w_layout(d->w_layout);
   const int tps = (k_tiles + d->split_k - 1) / d->split_k;
   if (tps > kMaxTilesPerSplit)
@@ -238,6 +243,7 @@ mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale,
   p.acc_blocks = g->desc.acc_blocks;
   p.l2_prefetch = std::max(0, static_cast<int>(g->desc.l2_prefetch));
   p.pipes = g->desc.pipes;
+  p.tmem_load = g->desc.tmem_load;
   p.tmem = g->tmem;
   p.x_scale = static_cast<const uint8_t*>(x_scale);
   p.w_sf = g->w_sf;
@@ -631,6 +637,7 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
   p.acc_blocks = d.acc_blocks;
   p.l2_prefetch = std::max(0, static_cast<int>(d.l2_prefetch));
   p.pipes = d.pipes;
+  p.tmem_load = d.tmem_load;
   p.tmem = gemm_tmem_plan(d.stages, d.acc_blocks);
   p.x_scale = static_cast<const uint8_t*>(x_scale);
   p.w_sf = scratch;

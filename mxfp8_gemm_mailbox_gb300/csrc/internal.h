@@ -5,6 +5,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "mxfp8_mailbox.h"
+
 namespace mxfp8 {
 
 constexpr int kBlockN = 128;      // output columns per CTA: the MMA's M
@@ -60,6 +62,7 @@ struct GemmParams {
   int32_t acc_blocks;       // 32-wide K blocks summed in TMEM per promoted partial: 1 or 4
   int32_t l2_prefetch;      // stages past the ring warmed in L2 before the grid wait
   int32_t pipes;            // producer lanes = MMA-issuing warps (1, 2, 4; divides stages)
+  int32_t tmem_load;        // MXFP8_TMEM_LOAD_32X32B or MXFP8_TMEM_LOAD_16X256B
   TmemPlan tmem;
   const uint8_t* x_scale;   // [m][k/32]
   const uint8_t* w_sf;      // [n/128][k_tiles][512] tiled W scales

@@ -48,6 +48,12 @@ namespace mxfp8 {
 namespace {
 
 constexpr uint32_t kStageTxBytes = kWTileBytes + kXTileBytes + kSfChunkBytes;
+// The 16x256b load's transpose buffer inside W stage 0: 4 warps x 32 columns
+// x 8 tokens x 8 bytes, after the BF16 tile (at most 8 x 128 x 2 bytes).
+constexpr uint32_t kTransposeOffset = 4096;
+static_assert(kTransposeOffset >= kRows * kBlockN * 2 &&
+                  kTransposeOffset + 4 * 32 * kRows * 8 <= kWTileBytes,
+              "the transpose buffer lies in W stage 0, past the BF16 tile");
 static_assert(kMaxAccRing % kMaxPipes == 0 && 4 % kMaxPipes == 0,
               "every accumulator slot belongs to one pipe");
 static_assert(threads_for_pipes(kMaxPipes) == kMaxThreads && threads_for_pipes(1) == 192,
@@ -131,7 +137,9 @@ struct RingCursor {
   }
 };
 
-template <int S>
+// kWideLoad: accumulators read with tcgen05.ld 16x256b (else 32x32b); a
+// template parameter so each read-out compiles to its own kernel.
+template <int S, bool kWideLoad>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     publish_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_x,
@@ -389,7 +397,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     ptx::fence_proxy_async_smem();  // the tensor-memory copy reads them
     ptx::mbar_arrive(bar_sfb);
 
-    // Fold every completed accumulator slot into the compensated sums.
+    // Fold every completed accumulator slot into the compensated sums.  With
+    // the 32x32b load thread = output column and hi[t] / lo[t] hold token t;
+    // with the 16x256b load (two per slot, lane halves 0-15 and 16-31 of the
+    // warp's quarter) element a = 4 h + r of a thread holds column
+    // 16 h + 8 (r / 2) + lane / 4 of the quarter and token 2 (lane % 4) +
+    // r % 2, and one warp-local transpose after the loop brings back the
+    // column-per-thread layout.  Each element sees the same values in the same
+    // order either way, so the two loads give identical bits.
+    constexpr bool wide_load = kWideLoad;
     float hi[kRows], lo[kRows];
 #pragma unroll
     for (int t = 0; t < kRows; ++t) hi[t] = lo[t] = 0.0f;
@@ -403,7 +419,36 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       ptx::tc_fence_after();
       const uint32_t slot =
           tmem + lane_base + p.tmem.acc + p.tmem.acc_slot * static_cast<uint32_t>(r);
-      if (per_block) {
+      if constexpr (wide_load) {
+        constexpr uint32_t kHalf = 16u << 16;  // lane offset of the second half
+        if (per_block) {
+          uint32_t v0[16], v1[16];
+          ptx::tmem_ld_16x256b_x4(slot, v0);
+          ptx::tmem_ld_16x256b_x4(slot + kHalf, v1);
+          ptx::tmem_wait_ld();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_acc_empty + 8u * r);
+#pragma unroll
+          for (int kb = 0; kb < kSfPerTile; ++kb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              two_sum_add(hi[e], lo[e], __uint_as_float(v0[kb * 4 + e]));
+              two_sum_add(hi[4 + e], lo[4 + e], __uint_as_float(v1[kb * 4 + e]));
+            }
+        } else {
+          uint32_t v0[4], v1[4];
+          ptx::tmem_ld_16x256b_x1(slot, v0);
+          ptx::tmem_ld_16x256b_x1(slot + kHalf, v1);
+          ptx::tmem_wait_ld();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_acc_empty + 8u * r);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            two_sum_add(hi[e], lo[e], __uint_as_float(v0[e]));
+            two_sum_add(hi[4 + e], lo[4 + e], __uint_as_float(v1[e]));
+          }
+        }
+      } else if (per_block) {
         uint32_t v[32];
         ptx::tmem_ld_32x32b_x32(slot, v);
         ptx::tmem_wait_ld();
@@ -422,6 +467,25 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         ptx::mbar_arrive(bar_acc_empty + 8u * r);
 #pragma unroll
         for (int t = 0; t < kRows; ++t) two_sum_add(hi[t], lo[t], __uint_as_float(v[t]));
+      }
+    }
+
+    if constexpr (wide_load) {
+      // Transpose through this warp's 2 KB of the dead W stage 0 (past the
+      // BF16 tile): [column of the quarter][token] pairs.
+      float2* pairs = reinterpret_cast<float2*>(smem + L.w + kTransposeOffset) + quarter * 32 * kRows;
+#pragma unroll
+      for (int a = 0; a < kRows; ++a) {
+        const int c = (a / 4) * 16 + ((a % 4) / 2) * 8 + lane / 4;
+        const int t = 2 * (lane % 4) + (a % 2);
+        pairs[c * kRows + t] = make_float2(hi[a], lo[a]);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int t = 0; t < kRows; ++t) {
+        const float2 v = pairs[lane * kRows + t];
+        hi[t] = v.x;
+        lo[t] = v.y;
       }
     }
 
@@ -610,7 +674,7 @@ __global__ void tile_weights_kernel(const uint8_t* __restrict__ w, uint8_t* __re
   }
 }
 
-template <int S>
+template <int S, bool kWideLoad>
 cudaError_t launch_impl(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, const GemmParams& p,
                         cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -632,7 +696,7 @@ cudaError_t launch_impl(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, co
   }
   cfg.attrs = attrs;
   cfg.numAttrs = count;
-  return cudaLaunchKernelEx(&cfg, publish_gemm_kernel<S>, tmap_w, tmap_x, p);
+  return cudaLaunchKernelEx(&cfg, publish_gemm_kernel<S, kWideLoad>, tmap_w, tmap_x, p);
 }
 
 }  // namespace
@@ -672,16 +736,20 @@ TmemPlan gemm_tmem_plan(int stages, int acc_blocks) {
 }
 
 cudaError_t set_gemm_smem_attribute(int split_k, int bytes) {
+  auto set = [bytes](auto kernel) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  };
+  cudaError_t e = cudaSuccess;
   switch (split_k) {
     case 1:
-      return cudaFuncSetAttribute(publish_gemm_kernel<1>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if ((e = set(publish_gemm_kernel<1, false>)) != cudaSuccess) return e;
+      return set(publish_gemm_kernel<1, true>);
     case 2:
-      return cudaFuncSetAttribute(publish_gemm_kernel<2>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if ((e = set(publish_gemm_kernel<2, false>)) != cudaSuccess) return e;
+      return set(publish_gemm_kernel<2, true>);
     case 4:
-      return cudaFuncSetAttribute(publish_gemm_kernel<4>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if ((e = set(publish_gemm_kernel<4, false>)) != cudaSuccess) return e;
+      return set(publish_gemm_kernel<4, true>);
     default:
       return cudaErrorInvalidValue;
   }
@@ -689,13 +757,17 @@ cudaError_t set_gemm_smem_attribute(int split_k, int bytes) {
 
 cudaError_t launch_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
                                 const GemmParams& p, int split_k, cudaStream_t stream) {
+  const bool wide = p.tmem_load == MXFP8_TMEM_LOAD_16X256B;
   switch (split_k) {
     case 1:
-      return launch_impl<1>(tmap_w, tmap_x, p, stream);
+      return wide ? launch_impl<1, true>(tmap_w, tmap_x, p, stream)
+                  : launch_impl<1, false>(tmap_w, tmap_x, p, stream);
     case 2:
-      return launch_impl<2>(tmap_w, tmap_x, p, stream);
+      return wide ? launch_impl<2, true>(tmap_w, tmap_x, p, stream)
+                  : launch_impl<2, false>(tmap_w, tmap_x, p, stream);
     case 4:
-      return launch_impl<4>(tmap_w, tmap_x, p, stream);
+      return wide ? launch_impl<4, true>(tmap_w, tmap_x, p, stream)
+                  : launch_impl<4, false>(tmap_w, tmap_x, p, stream);
     default:
       return cudaErrorInvalidValue;
   }

@@ -85,6 +85,7 @@ def _create(lib, desc, w=0x1000, ws=0x2000, mb=0x3000, st=0x4000, work=0x5000, n
     ((256, 256, 8, 1, 0, 0, 0, 0, 65), _lib.ERR_UNSUPPORTED, "l2_prefetch"),
     ((256, 256, 8, 1, 0, 0, 0, 0, -2), _lib.ERR_UNSUPPORTED, "l2_prefetch"),
     ((256, 256, 8, 1, 0, 0, 0, 0, 0, 3), _lib.ERR_UNSUPPORTED, "pipes"),
+    ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 3), _lib.ERR_UNSUPPORTED, "tmem_load"),
 ])
 def test_create_rejects_bad_descriptors(lib, desc, expect, needle):
     status, out, msg = _create(lib, _lib.GemmDesc(*desc))

@@ -10,7 +10,8 @@ import torch
 import oracle
 import synthetic
 from mxfp8_gemm_mailbox_gb300 import ERR_STATE, OK, Mailbox, Mxfp8Error, PublishGemm
-from mxfp8_gemm_mailbox_gb300._lib import W_IN_PLACE, W_TILED
+from mxfp8_gemm_mailbox_gb300._lib import (TMEM_LOAD_16X256B, TMEM_LOAD_32X32B, W_IN_PLACE,
+                                            W_TILED)
 from tests.gpu_util import (assert_bf16_close, bits, dev, mailbox_words, pack_words, sanitized,
                             state_words)
 
@@ -188,6 +189,44 @@ def test_l2_prefetch_leaves_results_unchanged(cuda, l2_prefetch, w_layout):
         assert (bits(c) == want).all() and (bits(out) == sanitized(want)).all()
         assert mb.status()[0] == OK
         g.close()
+
+
+@pytest.mark.parametrize("acc_blocks", [1, 4])
+@pytest.mark.parametrize("split_k", [1, 2, 4])
+def test_tmem_load_shapes_give_identical_bits(cuda, split_k, acc_blocks):
+    """The 16x256b accumulator read-out (the gemm page's default shape) and
+    the 32x32b one (its column_lanes = 1 case) fold each element's partial
+    sums in the same order: C, the mailbox and the consumer output agree bit
+    for bit, and both match the oracle (bit-exact on integer inputs, within
+    2 ULP on N(0, 1) inputs)."""
+    wl = synthetic.Workload("loads", 768, 6144, 7, split_k, exp_lo=-5, exp_hi=3, seed=41)
+    w, ws = synthetic.make_weights(wl)
+    x, xs = synthetic.make_activations(wl)
+    wi, wsi, xi, xsi = synthetic.integer_operands(768, 6144, 8, seed=42)
+    for (ww, wws, xx, xxs, exact) in ((w, ws, x, xs, False), (wi, wsi, xi, xsi, True)):
+        got = {}
+        for load in (TMEM_LOAD_32X32B, TMEM_LOAD_16X256B):
+            mb = Mailbox(8, 768)
+            g = PublishGemm(dev(ww), dev(wws), mb, split_k=split_k, acc_blocks=acc_blocks,
+                            tmem_load=load)
+            assert g.config()["tmem_load"] == {1: "32x32b", 2: "16x256b"}[load]
+            m = xx.shape[0]
+            c = torch.full((m, 768), 0x7FFF, dtype=torch.int16, device="cuda")
+            g.run(dev(xx), dev(xxs), c)
+            torch.cuda.synchronize()
+            words = mailbox_words(mb).copy()
+            out = mb.consume(m)
+            torch.cuda.synchronize()
+            got[load] = (bits(c), words, bits(out))
+            assert mb.status()[0] == OK
+            g.close()
+        a, b = got[TMEM_LOAD_32X32B], got[TMEM_LOAD_16X256B]
+        assert (a[0] == b[0]).all() and (a[1] == b[1]).all() and (a[2] == b[2]).all()
+        want = oracle.gemm_bf16(ww, wws, xx, xxs)
+        if exact:
+            assert (b[0] == want).all()
+        else:
+            assert_bf16_close(b[0], want)
 
 
 def test_pipes_that_do_not_divide_the_ring_are_refused(cuda):
