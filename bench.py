@@ -34,6 +34,7 @@ METRIC = "us/call and weight-stream HBM GB/s (% of GB300 peak), MXFP8 GEMM m<=8"
 UNIT = "GB/s"
 WEIGHT_COPIES = 3
 GRAPH_STEPS = 30  # calls per captured graph (a multiple of WEIGHT_COPIES)
+E2E_BATCH = 5     # end-to-end steps per wait on the input copies (divides GRAPH_STEPS)
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("mxfp8_gemm_mailbox_gb300/csrc/publish_gemm.cu",
                   "mxfp8_gemm_mailbox_gb300/csrc/ptx.cuh")
@@ -331,48 +332,62 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     achieved = wl.weight_bytes / (gemm_us * 1e-6) / 1e9
 
-    # End to end through the public API from pinned host buffers, double
-    # buffered: a copy stream moves step i+1's x and x scales in, and step
-    # i's output out, while the compute stream runs step i's GEMM + consumer.
+    # End to end through the public API from pinned host buffers.  Every
+    # step copies its own x and x scales in (one stream) and its output out
+    # (another stream).  An event edge inside the chain of kernels cuts the
+    # programmatic launch between a consumer and the next GEMM (about 6 us
+    # per step, measured), so the compute stream waits on the input copies
+    # once per batch of E2E_BATCH steps: batch j+1's inputs land while batch
+    # j computes, each step's output copy forks off right after its consumer.
     hx = torch.from_numpy(x).pin_memory()
     hxs = torch.from_numpy(xs).pin_memory()
-    houts = [torch.empty((wl.m, wl.n), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    dXs = [torch.empty_like(X) for _ in range(2)]
-    dXSs = [torch.empty_like(XS) for _ in range(2)]
-    outs = [torch.empty_like(out) for _ in range(2)]
-    copy_stream = torch.cuda.Stream(device=device)
+    nbuf = 2 * E2E_BATCH
+    houts = [torch.empty((wl.m, wl.n), dtype=torch.bfloat16).pin_memory() for _ in range(nbuf)]
+    dXs = [torch.empty_like(X) for _ in range(nbuf)]
+    dXSs = [torch.empty_like(XS) for _ in range(nbuf)]
+    outs = [torch.empty_like(out) for _ in range(nbuf)]
+    h2d_stream = torch.cuda.Stream(device=device)
+    d2h_stream = torch.cuda.Stream(device=device)
     n_e2e = min(3000, steps)
 
     def e2e_steps(count):
-        loaded = [torch.cuda.Event() for _ in range(2)]
-        done = [torch.cuda.Event() for _ in range(2)]
-        read = [torch.cuda.Event() for _ in range(2)]
+        k = E2E_BATCH
+        nbatch = (count + k - 1) // k
+        loaded = [torch.cuda.Event() for _ in range(nbatch)]
+        computed = [torch.cuda.Event() for _ in range(nbatch)]
+        read = [torch.cuda.Event() for _ in range(nbatch)]
+        step_done = [torch.cuda.Event() for _ in range(count)]
 
-        def load(i):
-            b = i % 2
-            with torch.cuda.stream(copy_stream):
-                if i >= 2:
-                    copy_stream.wait_event(done[b])  # step i-2 no longer reads this buffer
-                dXs[b].copy_(hx, non_blocking=True)
-                dXSs[b].copy_(hxs, non_blocking=True)
-                loaded[b].record(copy_stream)
+        def load(j):  # the inputs of batch j, one copy pair per step
+            with torch.cuda.stream(h2d_stream):
+                if j >= 2:
+                    h2d_stream.wait_event(computed[j - 2])  # batch j-2 no longer reads them
+                for i in range(j * k, min(count, (j + 1) * k)):
+                    dXs[i % nbuf].copy_(hx, non_blocking=True)
+                    dXSs[i % nbuf].copy_(hxs, non_blocking=True)
+                loaded[j].record(h2d_stream)
 
         load(0)
-        for i in range(count):
-            b = i % 2
-            if i + 1 < count:
-                load(i + 1)
+        for j in range(nbatch):
+            if j + 1 < nbatch:
+                load(j + 1)
             with torch.cuda.stream(stream):
-                stream.wait_event(loaded[b])
-                if i >= 2:
-                    stream.wait_event(read[b])  # step i-2's output has left the device
-                gemms[i % WEIGHT_COPIES].run(dXs[b], dXSs[b])
-                mb.consume(wl.m, outs[b])
-                done[b].record(stream)
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(done[b])
-                houts[b].copy_(outs[b], non_blocking=True)
-                read[b].record(copy_stream)
+                stream.wait_event(loaded[j])
+                if j >= 2:
+                    stream.wait_event(read[j - 2])  # batch j-2's outputs have left the device
+            for i in range(j * k, min(count, (j + 1) * k)):
+                b = i % nbuf
+                with torch.cuda.stream(stream):
+                    gemms[i % WEIGHT_COPIES].run(dXs[b], dXSs[b])
+                    mb.consume(wl.m, outs[b])
+                    step_done[i].record(stream)
+                with torch.cuda.stream(d2h_stream):
+                    d2h_stream.wait_event(step_done[i])
+                    houts[b].copy_(outs[b], non_blocking=True)
+            with torch.cuda.stream(stream):
+                computed[j].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                read[j].record(d2h_stream)
 
     # The per-step host work (about twenty launches and stream operations)
     # would dominate, so the pipeline of GRAPH_STEPS steps is captured once
@@ -382,9 +397,11 @@ def run_ours(args):
     torch.cuda.synchronize(device)
     e2e_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(e2e_graph, stream=stream):
-        copy_stream.wait_stream(stream)
+        h2d_stream.wait_stream(stream)
+        d2h_stream.wait_stream(stream)
         e2e_steps(GRAPH_STEPS)
-        stream.wait_stream(copy_stream)
+        stream.wait_stream(h2d_stream)
+        stream.wait_stream(d2h_stream)
     e2e_replays = max(1, n_e2e // GRAPH_STEPS)
     n_e2e = e2e_replays * GRAPH_STEPS
     with torch.cuda.stream(stream):
@@ -399,7 +416,7 @@ def run_ours(args):
             e2e_graph.replay()
         f1.record(stream)
     stream.synchronize()
-    if not torch.equal(houts[(n_e2e - 1) % 2], outs[(n_e2e - 1) % 2].cpu()):
+    if not torch.equal(houts[(GRAPH_STEPS - 1) % nbuf], outs[(GRAPH_STEPS - 1) % nbuf].cpu()):
         raise RuntimeError("the end-to-end output read back differs from the device copy")
     e2e_s, e2e_bytes = aggregate(f0.elapsed_time(f1) / 1e3, float(n_e2e * wl.weight_bytes), group)
     status, words = mb.status(stream)
@@ -461,9 +478,11 @@ def run_ours(args):
                 "us_per_call": round(e2e_s / n_e2e * 1e6, 3),
                 "steps": n_e2e,
                 "h2d_bytes_per_step": int(X.numel() + XS.numel()),
-                "pipelining": "double-buffered: inputs of step i+1 and output of step i "
-                              "copied on a second stream while step i computes; "
-                              f"{GRAPH_STEPS} steps per captured CUDA graph",
+                "pipelining": f"every step copies its inputs in (one stream) and its output "
+                              f"out (another); the compute waits on the input copies once "
+                              f"per {E2E_BATCH} steps, the next batch's inputs landing "
+                              f"while the current one computes; {GRAPH_STEPS} steps per "
+                              "captured CUDA graph",
                 "d2h_bytes_per_step": int(out.numel() * out.element_size()),
             },
             "gpu_launches": 2 * steps,
