@@ -34,7 +34,8 @@ METRIC = "us/call and weight-stream HBM GB/s (% of GB300 peak), MXFP8 GEMM m<=8"
 UNIT = "GB/s"
 WEIGHT_COPIES = 3
 GRAPH_STEPS = 30  # calls per captured graph (a multiple of WEIGHT_COPIES)
-E2E_BATCH = 5     # end-to-end steps per wait on the input copies (divides GRAPH_STEPS)
+E2E_GRAPH_STEPS = 120  # end-to-end steps per captured graph (a multiple of WEIGHT_COPIES)
+E2E_BATCH = 15         # end-to-end steps per wait on the input copies (divides E2E_GRAPH_STEPS)
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("mxfp8_gemm_mailbox_gb300/csrc/publish_gemm.cu",
                   "mxfp8_gemm_mailbox_gb300/csrc/ptx.cuh")
@@ -424,11 +425,11 @@ def run_ours(args):
     with torch.cuda.graph(e2e_graph, stream=stream):
         h2d_stream.wait_stream(stream)
         d2h_stream.wait_stream(stream)
-        e2e_steps(GRAPH_STEPS)
+        e2e_steps(E2E_GRAPH_STEPS)
         stream.wait_stream(h2d_stream)
         stream.wait_stream(d2h_stream)
-    e2e_replays = max(1, n_e2e // GRAPH_STEPS)
-    n_e2e = e2e_replays * GRAPH_STEPS
+    e2e_replays = max(1, n_e2e // E2E_GRAPH_STEPS)
+    n_e2e = e2e_replays * E2E_GRAPH_STEPS
     with torch.cuda.stream(stream):
         for _ in range(2):
             e2e_graph.replay()
@@ -441,7 +442,7 @@ def run_ours(args):
             e2e_graph.replay()
         f1.record(stream)
     stream.synchronize()
-    if not torch.equal(houts[(GRAPH_STEPS - 1) % nbuf], outs[(GRAPH_STEPS - 1) % nbuf].cpu()):
+    if not torch.equal(houts[(E2E_GRAPH_STEPS - 1) % nbuf], outs[(E2E_GRAPH_STEPS - 1) % nbuf].cpu()):
         raise RuntimeError("the end-to-end output read back differs from the device copy")
     e2e_s, e2e_bytes = aggregate(f0.elapsed_time(f1) / 1e3, float(n_e2e * wl.weight_bytes), group)
     status, words = mb.status(stream)
@@ -510,7 +511,7 @@ def run_ours(args):
                 "pipelining": f"every step copies its inputs in (one stream) and its output "
                               f"out (another); the compute waits on the input copies once "
                               f"per {E2E_BATCH} steps, the next batch's inputs landing "
-                              f"while the current one computes; {GRAPH_STEPS} steps per "
+                              f"while the current one computes; {E2E_GRAPH_STEPS} steps per "
                               "captured CUDA graph",
                 "d2h_bytes_per_step": int(out.numel() * out.element_size()),
             },
