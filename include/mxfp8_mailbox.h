@@ -76,7 +76,11 @@ typedef struct mxfp8_gemm_desc {
   int32_t n;          /* output columns N ("hidden"): a positive multiple of 128     */
   int32_t k;          /* reduction length K: a positive multiple of 32, <= 32768     */
   int32_t capacity_m; /* mailbox rows per generation: 1..8                           */
-  int32_t split_k;    /* cluster split-K S: 1, 2 or 4 (0 = choose)                   */
+  int32_t split_k;    /* cluster split-K S: 1, 2, 4 (the page's sizes) or 8 (a
+                         portable cluster, one token per CTA; measured slower than
+                         4 where both fit, so never chosen); 0 = choose among 1, 2,
+                         4: the largest with at most two CTAs per SM and >= 2 K
+                         tiles per split                                               */
   int32_t cta_k;      /* K elements per pipeline stage: 128 (0 = 128)                */
   int32_t stages;     /* shared-memory ring depth: 2..16 (0 = choose)                */
   int32_t acc_blocks; /* K blocks per promoted partial sum: 1 or 4 (0 = 4)           */

@@ -273,14 +273,14 @@ __device__ __forceinline__ void st_async_remote_v4(uint32_t remote_addr, uint4 v
       "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
       : "memory");
 }
-// Store one word into a peer CTA's shared memory; the byte count completes on
-// the peer's mbarrier.
-__device__ __forceinline__ void st_async_remote(uint32_t remote_addr, uint32_t value,
-                                                uint32_t remote_bar) {
+// Store 8 bytes (8-byte aligned) into a peer CTA's shared memory; the byte
+// count completes on the peer's mbarrier.
+__device__ __forceinline__ void st_async_remote_v2(uint32_t remote_addr, uint32_t a, uint32_t b,
+                                                   uint32_t remote_bar) {
   asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
           remote_addr),
-      "r"(value), "r"(remote_bar)
+      "r"(a), "r"(b), "r"(remote_bar)
       : "memory");
 }
 

@@ -494,9 +494,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     // own to their owners, then sums the S pairs of its own tokens in K-slice
     // order.  A split with no K tiles contributes zeros.  The receive buffer
     // is [sender][column][token][hi, lo]: one CTA's pairs for one column are
-    // 8 * kShard contiguous bytes, sent as 16-byte stores.
+    // 8 * kShard contiguous bytes, sent as 16-byte stores (8-byte ones at
+    // S = 8, where each CTA owns one token).
     constexpr int kShard = kRows / S;
-    static_assert(S == 1 || kShard % 2 == 0, "pairs travel two tokens per 16-byte store");
+    static_assert(kShard * S == kRows && (kShard == 1 || kShard % 2 == 0),
+                  "tokens split evenly, in pairs or one per CTA");
     float own_hi[kShard], own_lo[kShard];
     if constexpr (S > 1) {
       constexpr int kPairBytes = kShard * 8;
@@ -514,15 +516,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const uint32_t remote_bar = ptx::map_to_rank(bar_recv, peer);
         const uint32_t remote =
             ptx::map_to_rank(sbase + L.recv + (sender * kBlockN + col) * kPairBytes, peer);
+        if constexpr (kShard == 1) {
+          ptx::st_async_remote_v2(remote, __float_as_uint(hi[peer]), __float_as_uint(lo[peer]),
+                                  remote_bar);
+        } else {
 #pragma unroll
-        for (int jj = 0; jj < kShard; jj += 2)
-          ptx::st_async_remote_v4(
-              remote + jj * 8,
-              make_uint4(__float_as_uint(hi[peer * kShard + jj]),
-                         __float_as_uint(lo[peer * kShard + jj]),
-                         __float_as_uint(hi[peer * kShard + jj + 1]),
-                         __float_as_uint(lo[peer * kShard + jj + 1])),
-              remote_bar);
+          for (int jj = 0; jj < kShard; jj += 2)
+            ptx::st_async_remote_v4(
+                remote + jj * 8,
+                make_uint4(__float_as_uint(hi[peer * kShard + jj]),
+                           __float_as_uint(lo[peer * kShard + jj]),
+                           __float_as_uint(hi[peer * kShard + jj + 1]),
+                           __float_as_uint(lo[peer * kShard + jj + 1])),
+                remote_bar);
+        }
       }
       // This thread addresses no peer after its sends: its half of the final
       // cluster barrier, whose wait comes before the CTA exits.
@@ -751,6 +758,9 @@ cudaError_t set_gemm_smem_attribute(int split_k, int bytes) {
     case 4:
       if ((e = set(publish_gemm_kernel<4, false>)) != cudaSuccess) return e;
       return set(publish_gemm_kernel<4, true>);
+    case 8:
+      if ((e = set(publish_gemm_kernel<8, false>)) != cudaSuccess) return e;
+      return set(publish_gemm_kernel<8, true>);
     default:
       return cudaErrorInvalidValue;
   }
@@ -769,6 +779,9 @@ cudaError_t launch_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
     case 4:
       return wide ? launch_impl<4, true>(tmap_w, tmap_x, p, stream)
                   : launch_impl<4, false>(tmap_w, tmap_x, p, stream);
+    case 8:
+      return wide ? launch_impl<8, true>(tmap_w, tmap_x, p, stream)
+                  : launch_impl<8, false>(tmap_w, tmap_x, p, stream);
     default:
       return cudaErrorInvalidValue;
   }

@@ -77,6 +77,7 @@ def _create(lib, desc, w=0x1000, ws=0x2000, mb=0x3000, st=0x4000, work=0x5000, n
     ((256, 256, 0, 1, 0, 0), _lib.ERR_INVALID, "capacity_m"),
     ((256, 256, 9, 1, 0, 0), _lib.ERR_INVALID, "capacity_m"),
     ((256, 256, 8, 3, 0, 0), _lib.ERR_UNSUPPORTED, "split_k"),
+    ((256, 256, 8, 16, 0, 0), _lib.ERR_UNSUPPORTED, "split_k"),
     ((256, 256, 8, 1, 64, 0), _lib.ERR_UNSUPPORTED, "cta_k"),
     ((256, 256, 8, 1, 0, 1), _lib.ERR_UNSUPPORTED, "stages"),
     ((256, 65536, 8, 1, 0, 0), _lib.ERR_UNSUPPORTED, "32768"),

@@ -191,8 +191,35 @@ def test_l2_prefetch_leaves_results_unchanged(cuda, l2_prefetch, w_layout):
         g.close()
 
 
+@pytest.mark.parametrize("tmem_load", [1, 2])
+@pytest.mark.parametrize("n,k,m", [(256, 2048, 8), (1024, 8192, 5), (384, 1152, 1), (128, 4096, 8)])
+def test_split_eight_one_token_per_cta(cuda, n, k, m, tmem_load):
+    """Split-K over a cluster of 8: each CTA owns one token and receives the
+    other seven CTAs' (hi, lo) pairs for it in 8-byte stores; ragged K, every
+    m (CTAs whose token is past m publish nothing), bit-exact on integer
+    inputs and within 2 ULP on N(0, 1) ones, and the consumer's output."""
+    wi, wsi, xi, xsi = synthetic.integer_operands(n, k, m, seed=n + k + m)
+    c, between, sb, out, after, state, cfg = run_chain(wi, wsi, xi, xsi, 8)
+    assert cfg["split_k"] == 8 and cfg["grid_ctas"] == (n // 128) * 8
+    want = oracle.gemm_bf16(wi, wsi, xi, xsi)
+    assert (c == want).all() and (out == sanitized(want)).all()
+    check_published(between, sb, c, 8, n)
+    wl = synthetic.Workload("s8", n, k, m, 8, exp_lo=-5, exp_hi=3, seed=n * 3 + m)
+    w, ws = synthetic.make_weights(wl)
+    x, xs = synthetic.make_activations(wl)
+    mb = Mailbox(8, n)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=8, tmem_load=tmem_load)
+    cc = torch.full((m, n), 0x7FFF, dtype=torch.int16, device="cuda")
+    g.run(dev(x), dev(xs), cc)
+    o = mb.consume(m)
+    torch.cuda.synchronize()
+    assert_bf16_close(bits(cc), oracle.gemm_bf16(w, ws, x, xs))
+    assert (bits(o) == sanitized(bits(cc))).all() and mb.status()[0] == OK
+    g.close()
+
+
 @pytest.mark.parametrize("acc_blocks", [1, 4])
-@pytest.mark.parametrize("split_k", [1, 2, 4])
+@pytest.mark.parametrize("split_k", [1, 2, 4, 8])
 def test_tmem_load_shapes_give_identical_bits(cuda, split_k, acc_blocks):
     """The 16x256b accumulator read-out (the gemm page's default shape) and
     the 32x32b one (its column_lanes = 1 case) fold each element's partial
