@@ -34,8 +34,8 @@ METRIC = "us/call and weight-stream HBM GB/s (% of GB300 peak), MXFP8 GEMM m<=8"
 UNIT = "GB/s"
 WEIGHT_COPIES = 3
 GRAPH_STEPS = 30  # calls per captured graph (a multiple of WEIGHT_COPIES)
-E2E_GRAPH_STEPS = 120  # end-to-end steps per captured graph (a multiple of WEIGHT_COPIES)
-E2E_BATCH = 15         # end-to-end steps per wait on the input copies (divides E2E_GRAPH_STEPS)
+E2E_GRAPH_STEPS = 480  # end-to-end steps per captured graph (a multiple of WEIGHT_COPIES)
+E2E_BATCH = 30         # end-to-end steps per wait on the input copies (divides E2E_GRAPH_STEPS)
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("mxfp8_gemm_mailbox_gb300/csrc/publish_gemm.cu",
                   "mxfp8_gemm_mailbox_gb300/csrc/ptx.cuh")
