@@ -262,6 +262,45 @@ def test_pipes_that_do_not_divide_the_ring_are_refused(cuda):
         PublishGemm(dev(w), dev(ws), Mailbox(8, 256), split_k=1, stages=6, pipes=4)
 
 
+@pytest.mark.parametrize("split_k", [1, 2, 4])
+def test_longest_k(cuda, split_k):
+    """K = 32768, the largest K taken: 256 K tiles per CTA at S = 1 (the most a
+    split holds), every output bit-exact (integer inputs keep every partial sum
+    below 2^24)."""
+    n, k, m = 256, 32768, 8
+    w, ws, x, xs = synthetic.integer_operands(n, k, m, seed=77 + split_k)
+    c, between, sb, out, after, state, cfg = run_chain(w, ws, x, xs, split_k)
+    assert cfg["split_k"] == split_k
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    assert (c == want).all() and (out == sanitized(want)).all()
+    check_published(between, sb, c, 8, n)
+
+
+def test_grid_of_two_waves(cuda):
+    """N = 16384, K = 32768, S = 4: 512 CTAs, more than the GPU holds at once
+    (two per SM), so the clusters run in waves; for m = 8 and m = 1, 2,048
+    sampled outputs of C and of the consumer against the oracle, bit-exact on
+    integer inputs, and a clean mailbox after every call."""
+    n, k = 16384, 32768
+    w, ws, x, xs = synthetic.integer_operands(n, k, 8, seed=91)
+    mb = Mailbox(8, n)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=4)
+    assert g.config()["grid_ctas"] == 512
+    rng = np.random.default_rng(5)
+    for m in (8, 1):
+        rows = rng.integers(0, m, 2048)
+        cols = rng.integers(0, n, 2048)
+        want = oracle.gemm_sample(w, ws, x[:m], xs[:m], rows, cols)
+        c = torch.full((m, n), 0x7FFF, dtype=torch.int16, device="cuda")
+        g.run(dev(x[:m]), dev(xs[:m]), c)
+        out = mb.consume(m)
+        torch.cuda.synchronize()
+        assert (bits(c)[rows, cols] == want).all(), f"C, m={m}"
+        assert (bits(out)[rows, cols] == sanitized(want)).all(), f"consumer, m={m}"
+        assert mb.status()[0] == OK and (mailbox_words(mb) == oracle.SENTINEL).all()
+    g.close()
+
+
 def test_ring_too_deep_for_shared_memory_is_refused(cuda):
     w, ws, x, xs = synthetic.integer_operands(256, 4096, 8, seed=1)
     with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED"):
