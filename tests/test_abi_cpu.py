@@ -154,3 +154,51 @@ def test_tagged_calls_reject_bad_arguments(lib):
     assert lib.tagged_consume(pairs, 8, 128, 1, 1, ctypes.c_void_p(0x2008), 0, None,
                               None) == _lib.ERR_INVALID
     assert lib.tagged_mailbox_init(ctypes.c_void_p(0x1004), 8, 128, None) == _lib.ERR_INVALID
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "mxfp8_mailbox.h"
+
+int main(void) {
+  mxfp8_gemm_desc d;
+  memset(&d, 0, sizeof d);
+  d.n = 7168; d.k = 16384; d.capacity_m = 8; d.split_k = 4;
+  /* host-only calls: sizes and argument checks, no device needed */
+  if (mxfp8_mailbox_bytes(8, 7168) != 3u * 8u * 7168u * 2u) return 1;
+  if (mxfp8_publish_gemm_workspace_bytes(&d) == 0) return 2;
+  if (tagged_mailbox_bytes(8, 7168) == 0) return 3;
+  if (lamport_gather_mailbox_bytes(1u << 20) != 3u * (1u << 20)) return 4;
+  d.pipes = 3;
+  mxfp8_publish_gemm* g = NULL;
+  if (mxfp8_publish_gemm_create(&d, NULL, NULL, NULL, NULL, NULL, 0, NULL, &g) == MXFP8_OK) return 5;
+  if (g != NULL || strlen(mxfp8_last_error()) == 0) return 6;
+  printf("%s\n", mxfp8_last_error());
+  return 0;
+}
+"""
+
+
+def test_header_and_library_serve_a_c99_program(lib, tmp_path):
+    """The boundary is plain C: a C99 program that includes only the header
+    builds with warnings as errors, links against the library, and makes
+    the host-only calls (sizes and an argument check)."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = Path(_lib.LIBRARY).parent
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", f"-I{HEADER.parent}",
+           str(src), "-o", str(exe), f"-L{libdir}", f"-l:{Path(_lib.LIBRARY).name}",
+           f"-Wl,-rpath,{libdir}"]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert run.returncode == 0, (run.returncode, run.stdout, run.stderr)
+    assert "pipes" in run.stdout
