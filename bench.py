@@ -32,9 +32,13 @@ sys.path.insert(0, str(ROOT))
 
 METRIC = "us/call and weight-stream HBM GB/s (% of GB300 peak), MXFP8 GEMM m<=8"
 UNIT = "GB/s"
-WEIGHT_COPIES = 3
-GRAPH_STEPS = 30  # calls per captured graph (a multiple of WEIGHT_COPIES)
-E2E_GRAPH_STEPS = 480  # end-to-end steps per captured graph (a multiple of WEIGHT_COPIES)
+WEIGHT_COPIES = 3  # the headline's rotation; other workloads take more (weight_copies())
+L2_BYTES = 129 * 2**20
+WORKLOAD_CHOICES = {"headline": "HEADLINE", "graph": "GRAPH_8192", "chain": "CHAIN_4096",
+                    "tiny": "TINY"}
+_WORKLOAD = "headline"
+GRAPH_STEPS = 30  # calls per captured graph (a multiple of every weight-copy count)
+E2E_GRAPH_STEPS = 480  # end-to-end steps per captured graph (likewise)
 E2E_BATCH = 30         # end-to-end steps per wait on the input copies (divides E2E_GRAPH_STEPS)
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("mxfp8_gemm_mailbox_gb300/csrc/publish_gemm.cu",
@@ -53,6 +57,10 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="budget of the oracle CPU-baseline sample")
+    p.add_argument("--workload", choices=tuple(WORKLOAD_CHOICES), default="headline",
+                   help="the chain's workload: headline N=7168 K=16384 m=8 S=4 (default), "
+                        "graph N=7168 K=8192 m=8 S=2, chain N=4096 K=4096 m=4 S=1, "
+                        "tiny N=256 K=256 m=1 S=1")
     p.add_argument("--path", choices=("chain", "protocols", "sweep"), default="chain",
                    help="chain: the headline (default); protocols: the output hand-off "
                         "protocols on their own (sentinel mailbox, tagged pairs, all-gather); "
@@ -160,8 +168,8 @@ def kernel_source_hash() -> str:
 
 def recorded_traffic():
     """DRAM bytes per launch of the GEMM from the committed ncu summary, if it
-    was taken on the kernel as it is now."""
-    if not TRAFFIC_FILE.exists():
+    was taken on the kernel as it is now (the headline workload only)."""
+    if _WORKLOAD != "headline" or not TRAFFIC_FILE.exists():
         return None
     try:
         rec = json.loads(TRAFFIC_FILE.read_text())
@@ -175,7 +183,18 @@ def recorded_traffic():
 def workload():
     import synthetic
 
-    return synthetic.HEADLINE
+    return getattr(synthetic, WORKLOAD_CHOICES[_WORKLOAD])
+
+
+def weight_copies(weight_bytes: int) -> int:
+    """Weight copies the timed loops rotate through: enough that the copies
+    between two uses of one exceed twice the L2, and a divisor of both graph
+    lengths so every replay rotates the same way."""
+    need = max(WEIGHT_COPIES, -(-int(2.2 * L2_BYTES) // weight_bytes))
+    for c in (3, 5, 6, 10, 15, 30):
+        if c >= need:
+            return c
+    return 30
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -188,6 +207,7 @@ class OracleSample:
         import synthetic
 
         wl = workload()
+        columns = min(columns, wl.n)
         self.columns = columns
         self.k = k or wl.k
         sub = synthetic.Workload(wl.name, columns, self.k, wl.m, wl.split_k, wl.capacity,
@@ -276,7 +296,8 @@ def run_ours(args):
     WS = torch.from_numpy(ws).to(device)
     X = torch.from_numpy(x).to(device)
     XS = torch.from_numpy(xs).to(device)
-    weights = [W0] + [W0.clone() for _ in range(WEIGHT_COPIES - 1)]
+    copies = weight_copies(wl.weight_bytes)
+    weights = [W0] + [W0.clone() for _ in range(copies - 1)]
     mb = mx.Mailbox(wl.capacity, wl.n, device=device)
     gemms = [mx.PublishGemm(Wc, WS, mb, split_k=wl.split_k) for Wc in weights]
     cfg = gemms[0].config()
@@ -288,13 +309,13 @@ def run_ours(args):
     # Graphs of GRAPH_STEPS chained calls rotating through the weight copies.
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
-        for i in range(WEIGHT_COPIES):  # eager warm-up before capture
+        for i in range(copies):  # eager warm-up before capture
             gemms[i].run(X, XS)
             mb.consume(wl.m, out)
         stream.synchronize()
         with torch.cuda.graph(graph, stream=stream):
             for i in range(GRAPH_STEPS):
-                gemms[i % WEIGHT_COPIES].run(X, XS)
+                gemms[i % copies].run(X, XS)
                 mb.consume(wl.m, out)
     replays = max(1, -(-args.steps // GRAPH_STEPS))
     steps = replays * GRAPH_STEPS
@@ -331,7 +352,7 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         with torch.cuda.graph(gemm_graph, stream=stream):
             for i in range(GRAPH_STEPS):
-                gemms[i % WEIGHT_COPIES].run_unfused(X, XS, cbuf)
+                gemms[i % copies].run_unfused(X, XS, cbuf)
         for _ in range(warm):
             gemm_graph.replay()
         g0 = torch.cuda.Event(enable_timing=True)
@@ -350,7 +371,7 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         for i in range(n_iso):
             starts[i].record(stream)
-            gemms[i % WEIGHT_COPIES].run(X, XS)
+            gemms[i % copies].run(X, XS)
             ends[i].record(stream)
             mb.consume(wl.m, out)
     stream.synchronize()
@@ -404,7 +425,7 @@ def run_ours(args):
             for i in range(j * k, min(count, (j + 1) * k)):
                 b = i % nbuf
                 with torch.cuda.stream(stream):
-                    gemms[i % WEIGHT_COPIES].run(dXs[b], dXSs[b])
+                    gemms[i % copies].run(dXs[b], dXSs[b])
                     mb.consume(wl.m, outs[b])
                     step_done[i].record(stream)
                 with torch.cuda.stream(d2h_stream):
@@ -477,19 +498,23 @@ def run_ours(args):
             "dtype": "e4m3",
             "data": "synthetic (seeded N(0,1) E4M3, E8M0 block-32 scales, 1% zero x)",
             "config": {
-                "workload": "decode projection N=7168 K=16384 m=8 S=4 + mailbox publish/consume",
+                "workload": f"decode projection N={wl.n} K={wl.k} m={wl.m} S={wl.split_k} "
+                            "+ mailbox publish/consume",
                 "n": wl.n, "k": wl.k, "m": wl.m, "split_k": cfg["split_k"],
                 "stages": cfg["stages"], "grid_ctas": cfg["grid_ctas"],
                 "smem_bytes": cfg["smem_bytes"],
                 "weight_bytes_per_call": wl.weight_bytes,
-                "l2": f"{WEIGHT_COPIES} rotating weight copies ({WEIGHT_COPIES * wl.weight_bytes >> 20}"
-                      " MiB > 2 x 129 MB L2): every call streams its weight from HBM",
+                "l2": (f"{copies} rotating weight copies ({copies * wl.weight_bytes >> 20} MiB "
+                       "> 2 x 129 MB L2): every call streams its weight from HBM"
+                       if copies * wl.weight_bytes > 2 * L2_BYTES else
+                       f"{copies} rotating weight copies ({copies * wl.weight_bytes >> 10} KiB): "
+                       "the weights stay in L2; a latency figure, not a bandwidth one"),
                 "timing": f"CUDA graphs of {GRAPH_STEPS} chained calls (GEMM -> PDL consumer)",
                 "parallelism": "replicas" if world > 1 else "single GPU",
             },
             "roofline": {
                 "bound": "hbm",
-                "kernel": "publish_gemm_kernel<4, 0>",
+                "kernel": f"publish_gemm_kernel<{wl.split_k}, 0>",
                 "achieved": round(achieved, 1),
                 "peak": peak,
                 "peak_kind": peak_kind,
@@ -568,7 +593,8 @@ def run_reference(args):
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1) E4M3, E8M0 block-32 scales, 1% zero x)",
         "config": {
-            "workload": "decode projection N=7168 K=16384 m=8 S=4 + mailbox publish/consume",
+            "workload": f"decode projection N={wl.n} K={wl.k} m={wl.m} S={wl.split_k} "
+                        "+ mailbox publish/consume",
             "n": wl.n, "k": wl.k, "m": wl.m, "split_k": wl.split_k,
             "sample_columns": columns, "sample_k": k,
             "weight_bytes_per_step": sample.weight_bytes,
@@ -669,7 +695,6 @@ def run_protocols(args):
 
 
 # ---------------------------------------------------------- sweep table
-L2_BYTES = 129 * 2**20
 
 
 def run_sweep(args):
@@ -774,7 +799,9 @@ def run_sweep(args):
 
 
 def main(argv=None):
+    global _WORKLOAD
     args = parse_args(argv)
+    _WORKLOAD = args.workload
     if args.impl == "reference":
         run_reference(args)
     elif args.path == "protocols":
