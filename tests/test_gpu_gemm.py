@@ -301,6 +301,22 @@ def test_grid_of_two_waves(cuda):
     g.close()
 
 
+@pytest.mark.parametrize("shift", [100, -100, 60])
+@pytest.mark.parametrize("split_k", [1, 4])
+def test_scale_exponents_near_the_e8m0_limits(cuda, shift, split_k):
+    """W's scales moved up by `shift` powers of two and x's down by as many
+    (E8M0 codes from 27 to 228): every product, hence every output, is
+    unchanged, and exact; the scale plumbing must carry the extreme codes."""
+    n, k, m = 384, 4096, 8
+    w, ws, x, xs = synthetic.integer_operands(n, k, m, seed=500 + shift)
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    ws_s = (ws.astype(np.int32) + shift).astype(np.uint8)
+    xs_s = (xs.astype(np.int32) - shift).astype(np.uint8)
+    assert (oracle.gemm_bf16(w, ws_s, x, xs_s) == want).all()
+    c, between, sb, out, after, state, cfg = run_chain(w, ws_s, x, xs_s, split_k)
+    assert (c == want).all() and (out == sanitized(want)).all()
+
+
 def test_ring_too_deep_for_shared_memory_is_refused(cuda):
     w, ws, x, xs = synthetic.integer_operands(256, 4096, 8, seed=1)
     with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED"):
