@@ -87,9 +87,9 @@ typedef struct mxfp8_gemm_desc {
   int32_t w_layout;   /* MXFP8_W_IN_PLACE or MXFP8_W_TILED (0 = choose)              */
   int32_t l2_prefetch;/* W stages past the ring each CTA warms in L2 before its grid
                          wait, so HBM keeps streaming while the previous kernel and
-                         the grid wait hold the ring: 1..64, -1 = none, 0 = choose (6,
-                         the measured best on GB300: -2.6 % time per call on the
-                         N=7168, K=16384 chain)                                        */
+                         the grid wait hold the ring: 1..64, -1 = none, 0 = choose (6
+                         with two CTAs per SM, 10 with one: the measured best on
+                         GB300, -2.6 % time per call on the N=7168, K=16384 chain)     */
   int32_t pipes;      /* producer lanes and MMA-issuing warps sharing the ring: 1, 2
                          or 4, dividing `stages` (stage i and its ring slots belong to
                          pipe i % pipes).  0 = choose: 4 when the grid has at most one

@@ -54,8 +54,11 @@ bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % 
 constexpr uint64_t kDefaultPollTimeoutNs = 1000000000ull;
 constexpr uint64_t kGemmWaitLimitNs = 2000000000ull;
 // W stages past the ring each CTA warms in L2 by default (measured on GB300:
-// 6 beats 0, 4, 8, 12 and 16 on the N=7168, K=16384, S=4 chain).
+// with two CTAs per SM 6 beats 0, 4, 8, 12 and 16 on the N=7168, K=16384,
+// S=4 chain; with one, 10 is best on N=7168, K=8192, S=2 and no worse on
+// the smaller grids).
 constexpr int kDefaultL2Prefetch = 6;
+constexpr int kDefaultL2PrefetchOnePerSm = 10;
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -170,7 +173,6 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
   }
   d->cta_k = kTileK;
   if (d->acc_blocks == 0) d->acc_blocks = 4;
-  if (d->l2_prefetch == 0) d->l2_prefetch = kDefaultL2Prefetch;
   if (d->tmem_load == 0) d->tmem_load = MXFP8_TMEM_LOAD_32X32B;
   d->w_layout = resolved_w_layout(d->w_layout);
   const int tps = (k_tiles + d->split_k - 1) / d->split_k;
@@ -179,6 +181,8 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
   const int ctas = tiles * d->split_k;
   const int per_sm = ctas > lim.sms ? 2 : 1;
   const int budget = per_sm == 2 ? lim.smem_per_sm / 2 - 1024 : lim.smem_optin;
+  if (d->l2_prefetch == 0)
+    d->l2_prefetch = per_sm == 2 ? kDefaultL2Prefetch : kDefaultL2PrefetchOnePerSm;
   if (d->stages == 0) {
     int best = 0;
     for (int s = 2; s <= kMaxStages; ++s) {

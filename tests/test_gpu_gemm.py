@@ -181,7 +181,9 @@ def test_l2_prefetch_leaves_results_unchanged(cuda, l2_prefetch, w_layout):
         mb = Mailbox(8, n)
         g = PublishGemm(dev(w), dev(ws), mb, split_k=split, w_layout=w_layout,
                         l2_prefetch=l2_prefetch)
-        assert g.config()["l2_prefetch"] == (6 if l2_prefetch == 0 else l2_prefetch)
+        grid_ctas = n // 128 * split
+        default = 6 if grid_ctas > torch.cuda.get_device_properties(0).multi_processor_count else 10
+        assert g.config()["l2_prefetch"] == (default if l2_prefetch == 0 else l2_prefetch)
         c = torch.full((8, n), 0x7FFF, dtype=torch.int16, device="cuda")
         g.run(dev(x), dev(xs), c)
         out = mb.consume(8)
