@@ -102,6 +102,18 @@ typedef struct mxfp8_gemm_desc {
                          column_lanes = 1 being the 32x32b case: a thread holds 4
                          columns x 2 tokens and one warp-local transpose follows the
                          main loop).  The two give identical bits.                     */
+  int32_t fold;       /* K pieces stacked in the MMA's 128 rows: 1, 2 or 4.  A CTA then
+                         owns 128/fold output columns, its A operand holding fold
+                         consecutive 128-wide K pieces of those weight rows and its B
+                         operand the matching fold groups of 8 activation columns
+                         (N = 8 fold); only the diagonal blocks of the product are
+                         kept.  Each stage stays 16 KB of W and 4 MMAs; the grid has
+                         fold times more CTAs, for shapes whose N/128 x split_k CTAs
+                         leave SMs idle.  fold > 1 takes split_k 1, 2 or 4, acc_blocks
+                         4 and the 32x32b read-out.  0 = choose: the largest fold
+                         that keeps the grid within one CTA per SM and >= 1 full K
+                         piece per CTA (1 when those fields ask for what it cannot
+                         take).                                                         */
 } mxfp8_gemm_desc;
 
 /* Where the GEMM streams W from.  IN_PLACE: the caller's [N][K] buffer,

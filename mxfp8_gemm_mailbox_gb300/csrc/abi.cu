@@ -25,7 +25,7 @@ struct mxfp8_publish_gemm {
   uint16_t* mailbox;
   int32_t* state;
   int device;
-  int k_tiles;
+  int k_tiles;  // stages of K: ceil(K / (128 fold))
   int tiles_per_split;
   TmemPlan tmem;
   GemmSmemLayout layout;
@@ -59,6 +59,10 @@ constexpr uint64_t kGemmWaitLimitNs = 2000000000ull;
 // the smaller grids).
 constexpr int kDefaultL2Prefetch = 6;
 constexpr int kDefaultL2PrefetchOnePerSm = 10;
+// Tensor-memory columns a CTA may allocate: half of an SM's 512, so that two
+// CTAs sharing an SM never wait on each other's allocation (two CTAs of one
+// cluster on one SM would otherwise wait for ever).
+constexpr uint32_t kMaxTmemCols = 256;
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -125,18 +129,33 @@ mxfp8_status check_desc(const mxfp8_gemm_desc* d) {
       d->tmem_load != MXFP8_TMEM_LOAD_16X256B)
     return fail(MXFP8_ERR_UNSUPPORTED,
                 "tmem_load must be MXFP8_TMEM_LOAD_32X32B or MXFP8_TMEM_LOAD_16X256B");
+  if (d->fold != 0 && d->fold != 1 && d->fold != 2 && d->fold != 4)
+    return fail(MXFP8_ERR_UNSUPPORTED, "fold must be 1, 2 or 4 (or 0 to choose)");
+  if (d->fold > 1) {
+    if (d->split_k == 8)
+      return fail(MXFP8_ERR_UNSUPPORTED, "fold > 1 takes split_k 1, 2 or 4");
+    if (d->acc_blocks == 1)
+      return fail(MXFP8_ERR_UNSUPPORTED,
+                  "fold > 1 takes acc_blocks 4 (one slot per MMA does not fit in tensor memory)");
+    if (d->tmem_load == MXFP8_TMEM_LOAD_16X256B)
+      return fail(MXFP8_ERR_UNSUPPORTED, "fold > 1 reads accumulators with 32x32b");
+  }
   return MXFP8_OK;
 }
 
-int k_tiles_of(int k) { return (k + kTileK - 1) / kTileK; }
+// The fold a descriptor's buffers are sized for: 0 (choose) picks only folds
+// that pad K no further than 1 does, so it sizes like 1.
+int sizing_fold(int fold) { return fold == 0 ? 1 : fold; }
 
 int resolved_w_layout(int w_layout) { return w_layout == 0 ? MXFP8_W_TILED : w_layout; }
 
-size_t scale_chunk_bytes(int n, int k) {
-  return static_cast<size_t>(n / kBlockN) * k_tiles_of(k) * kSfChunkBytes;
+size_t scale_chunk_bytes(int n, int k, int fold) {
+  return static_cast<size_t>(n / (kBlockN / fold)) * k_tiles_for_fold(k, fold) * kSfChunkBytes;
 }
 
-size_t tiled_w_offset(int n, int k) { return (scale_chunk_bytes(n, k) + 255) & ~size_t{255}; }
+size_t tiled_w_offset(int n, int k, int fold) {
+  return (scale_chunk_bytes(n, k, fold) + 255) & ~size_t{255};
+}
 
 struct DeviceLimits {
   int sms = 0;
@@ -157,28 +176,42 @@ mxfp8_status device_limits(int device, DeviceLimits* out) {
   return MXFP8_OK;
 }
 
-// Fill split_k, cta_k, stages and pipes: split_k so the grid has about one or
-// two CTAs per SM; the deepest ring that still lets the intended number of
-// CTAs share an SM, rounded so the pipes divide it: with at most one CTA per
-// SM each CTA must stream fast, so 4 pipes (ring a multiple of 4); with two,
-// HBM is the limit and 2 pipes suffice (more in flight measured slower).
+// Fill split_k, cta_k, stages, pipes and fold: split_k so the grid has about
+// one or two CTAs per SM; then the largest fold that keeps at most one CTA
+// per SM (one SM streams only so fast: few-CTA grids leave HBM idle); the
+// deepest ring that still lets the intended number of CTAs share an SM,
+// rounded so the pipes divide it: with at most one CTA per SM each CTA must
+// stream fast, so 4 pipes (ring a multiple of 4); with two, HBM is the limit
+// and 2 pipes suffice (more in flight measured slower).
 mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
   const int tiles = d->n / kBlockN;
-  const int k_tiles = k_tiles_of(d->k);
+  const int k_tiles1 = k_tiles_for_fold(d->k, 1);
   if (d->split_k == 0) {
     int s = 1;
     for (int cand : {2, 4})  // 8 measured slower than 4 on every shape where both fit
-      if (tiles * cand <= 2 * lim.sms && k_tiles >= 2 * cand) s = cand;
+      if (tiles * cand <= 2 * lim.sms && k_tiles1 >= 2 * cand) s = cand;
     d->split_k = s;
   }
   d->cta_k = kTileK;
   if (d->acc_blocks == 0) d->acc_blocks = 4;
   if (d->tmem_load == 0) d->tmem_load = MXFP8_TMEM_LOAD_32X32B;
   d->w_layout = resolved_w_layout(d->w_layout);
+  if (d->fold == 0) {
+    int f = 1;
+    const bool foldable = d->split_k <= 4 && d->acc_blocks == 4 &&
+                          d->tmem_load == MXFP8_TMEM_LOAD_32X32B;
+    for (int cand : {2, 4})
+      if (foldable && tiles * d->split_k * cand <= lim.sms &&
+          k_tiles_for_fold(d->k, cand) * cand == k_tiles1 &&  // no more K padding
+          k_tiles_for_fold(d->k, cand) >= d->split_k)          // a full stage per split
+        f = cand;
+    d->fold = f;
+  }
+  const int k_tiles = k_tiles_for_fold(d->k, d->fold);
   const int tps = (k_tiles + d->split_k - 1) / d->split_k;
-  if (tps > kMaxTilesPerSplit)
+  if (tps * d->fold > kMaxTilesPerSplit)
     return fail(MXFP8_ERR_UNSUPPORTED, "too many K tiles per split: raise split_k");
-  const int ctas = tiles * d->split_k;
+  const int ctas = tiles * d->fold * d->split_k;
   const int per_sm = ctas > lim.sms ? 2 : 1;
   const int budget = per_sm == 2 ? lim.smem_per_sm / 2 - 1024 : lim.smem_optin;
   if (d->l2_prefetch == 0)
@@ -186,8 +219,8 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
   if (d->stages == 0) {
     int best = 0;
     for (int s = 2; s <= kMaxStages; ++s) {
-      if (static_cast<int>(gemm_smem_layout(s, d->split_k, tps).total) > budget) break;
-      if (gemm_tmem_plan(s, d->acc_blocks).cols > static_cast<uint32_t>(512 / per_sm)) break;
+      if (static_cast<int>(gemm_smem_layout(s, d->split_k, tps, d->fold).total) > budget) break;
+      if (gemm_tmem_plan(s, d->acc_blocks, d->fold).cols > kMaxTmemCols) break;
       best = s;
       if (s >= tps) break;  // more stages than K tiles buy nothing
     }
@@ -196,9 +229,10 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
     best -= best % unit;
     d->stages = best;
   }
-  if (static_cast<int>(gemm_smem_layout(d->stages, d->split_k, tps).total) > lim.smem_optin)
+  if (static_cast<int>(gemm_smem_layout(d->stages, d->split_k, tps, d->fold).total) >
+      lim.smem_optin)
     return fail(MXFP8_ERR_UNSUPPORTED, "the requested stages do not fit in shared memory");
-  if (gemm_tmem_plan(d->stages, d->acc_blocks).cols > 512)
+  if (gemm_tmem_plan(d->stages, d->acc_blocks, d->fold).cols > kMaxTmemCols)
     return fail(MXFP8_ERR_UNSUPPORTED, "the requested stages do not fit in tensor memory");
   if (d->pipes == 0) {
     d->pipes = (per_sm == 1 && d->stages % 4 == 0) ? 4 : (d->stages % 2 == 0 ? 2 : 1);
@@ -249,6 +283,7 @@ mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale,
   p.l2_prefetch = std::max(0, static_cast<int>(g->desc.l2_prefetch));
   p.pipes = g->desc.pipes;
   p.tmem_load = g->desc.tmem_load;
+  p.fold = g->desc.fold;
   p.tmem = g->tmem;
   p.x_scale = static_cast<const uint8_t*>(x_scale);
   p.w_sf = g->w_sf;
@@ -298,9 +333,13 @@ mxfp8_status mxfp8_mailbox_init(void* mailbox, int32_t* stage_state, int32_t cap
 
 size_t mxfp8_publish_gemm_workspace_bytes(const mxfp8_gemm_desc* desc) {
   if (!desc || desc->n <= 0 || desc->n % kBlockN || desc->k <= 0 || desc->k % 32) return 0;
-  if (resolved_w_layout(desc->w_layout) != MXFP8_W_TILED) return scale_chunk_bytes(desc->n, desc->k);
-  return tiled_w_offset(desc->n, desc->k) +
-         static_cast<size_t>(desc->n / kBlockN) * k_tiles_of(desc->k) * kWTileBytes;
+  if (desc->fold != 0 && desc->fold != 1 && desc->fold != 2 && desc->fold != 4) return 0;
+  const int fold = sizing_fold(desc->fold);
+  if (resolved_w_layout(desc->w_layout) != MXFP8_W_TILED)
+    return scale_chunk_bytes(desc->n, desc->k, fold);
+  return tiled_w_offset(desc->n, desc->k, fold) +
+         static_cast<size_t>(desc->n / (kBlockN / fold)) * k_tiles_for_fold(desc->k, fold) *
+             kWTileBytes;
 }
 
 mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* w,
@@ -339,37 +378,38 @@ mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* 
   }
   g->w = static_cast<const uint8_t*>(w);
   g->w_sf = static_cast<uint8_t*>(workspace);
+  const int fold = g->desc.fold;
   g->w_tiled = g->desc.w_layout == MXFP8_W_TILED
-                   ? static_cast<uint8_t*>(workspace) + tiled_w_offset(desc->n, desc->k)
+                   ? static_cast<uint8_t*>(workspace) + tiled_w_offset(desc->n, desc->k, fold)
                    : nullptr;
   g->mailbox = static_cast<uint16_t*>(mailbox);
   g->state = stage_state;
   g->device = device;
-  g->k_tiles = k_tiles_of(desc->k);
+  g->k_tiles = k_tiles_for_fold(desc->k, fold);
   g->tiles_per_split = (g->k_tiles + g->desc.split_k - 1) / g->desc.split_k;
-  g->tmem = gemm_tmem_plan(g->desc.stages, g->desc.acc_blocks);
-  g->layout = gemm_smem_layout(g->desc.stages, g->desc.split_k, g->tiles_per_split);
+  g->tmem = gemm_tmem_plan(g->desc.stages, g->desc.acc_blocks, fold);
+  g->layout = gemm_smem_layout(g->desc.stages, g->desc.split_k, g->tiles_per_split, fold);
   g->x_cached = nullptr;
   g->m_cached = 0;
   st = encode_rows(&g->tmap_w, w, static_cast<uint64_t>(desc->k), static_cast<uint64_t>(desc->n),
-                   kBlockN);
+                   kBlockN / fold);
   if (st != MXFP8_OK) {
     delete g;
     return st;
   }
-  e = set_gemm_smem_attribute(g->desc.split_k, static_cast<int>(g->layout.total));
+  e = set_gemm_smem_attribute(g->desc.split_k, fold, static_cast<int>(g->layout.total));
   if (e != cudaSuccess) {
     delete g;
     return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
   }
   e = launch_relayout_w_scales(static_cast<const uint8_t*>(w_scale), g->w_sf, desc->n, desc->k,
-                               static_cast<cudaStream_t>(stream));
+                               fold, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     delete g;
     return cuda_fail(e, "launching the W scale re-layout");
   }
   if (g->w_tiled != nullptr) {
-    e = launch_tile_weights(static_cast<const uint8_t*>(w), g->w_tiled, desc->n, desc->k,
+    e = launch_tile_weights(static_cast<const uint8_t*>(w), g->w_tiled, desc->n, desc->k, fold,
                             static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
       delete g;
@@ -387,7 +427,8 @@ mxfp8_status mxfp8_publish_gemm_config(const mxfp8_publish_gemm* gemm, mxfp8_gem
   if (desc) *desc = gemm->desc;
   if (smem_bytes) *smem_bytes = static_cast<int32_t>(gemm->layout.total);
   if (tmem_columns) *tmem_columns = static_cast<int32_t>(gemm->tmem.cols);
-  if (grid_ctas) *grid_ctas = (gemm->desc.n / kBlockN) * gemm->desc.split_k;
+  if (grid_ctas)
+    *grid_ctas = (gemm->desc.n / (kBlockN / gemm->desc.fold)) * gemm->desc.split_k;
   return MXFP8_OK;
 }
 
@@ -396,7 +437,8 @@ mxfp8_status mxfp8_publish_gemm_precompile(mxfp8_publish_gemm* gemm, int32_t m) 
   mxfp8_status st = check_rows(gemm, m);
   if (st != MXFP8_OK) return st;
   if (!encode_tiled()) return fail(MXFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-  cudaError_t e = set_gemm_smem_attribute(gemm->desc.split_k, static_cast<int>(gemm->layout.total));
+  cudaError_t e = set_gemm_smem_attribute(gemm->desc.split_k, gemm->desc.fold,
+                                          static_cast<int>(gemm->layout.total));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
   return MXFP8_OK;
 }
@@ -602,7 +644,7 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
   if (!x || !aligned(x, 16)) return fail(MXFP8_ERR_INVALID, "x must be a 16-byte aligned device pointer");
   if (!x_scale) return fail(MXFP8_ERR_INVALID, "x_scale is NULL");
   if (c && !aligned(c, 16)) return fail(MXFP8_ERR_INVALID, "c must be 16-byte aligned");
-  const size_t need = scale_chunk_bytes(desc->n, desc->k);
+  const size_t need = scale_chunk_bytes(desc->n, desc->k, sizing_fold(desc->fold));
   if (need > MXFP8_NOALLOC_SCRATCH_BYTES)
     return fail(MXFP8_ERR_UNSUPPORTED,
                 "N=" + std::to_string(desc->n) + ", K=" + std::to_string(desc->k) + " needs " +
@@ -623,10 +665,11 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
   st = noalloc_scratch(device, &scratch);
   if (st != MXFP8_OK) return st;
 
-  const int k_tiles = k_tiles_of(d.k);
+  const int k_tiles = k_tiles_for_fold(d.k, d.fold);
   const int tiles_per_split = (k_tiles + d.split_k - 1) / d.split_k;
   CUtensorMap tmap_w, tmap_x;
-  st = encode_rows(&tmap_w, w, static_cast<uint64_t>(d.k), static_cast<uint64_t>(d.n), kBlockN);
+  st = encode_rows(&tmap_w, w, static_cast<uint64_t>(d.k), static_cast<uint64_t>(d.n),
+                   kBlockN / d.fold);
   if (st != MXFP8_OK) return st;
   st = encode_rows(&tmap_x, x, static_cast<uint64_t>(d.k), static_cast<uint64_t>(m), kRows);
   if (st != MXFP8_OK) return st;
@@ -643,7 +686,8 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
   p.l2_prefetch = std::max(0, static_cast<int>(d.l2_prefetch));
   p.pipes = d.pipes;
   p.tmem_load = d.tmem_load;
-  p.tmem = gemm_tmem_plan(d.stages, d.acc_blocks);
+  p.fold = d.fold;
+  p.tmem = gemm_tmem_plan(d.stages, d.acc_blocks, d.fold);
   p.x_scale = static_cast<const uint8_t*>(x_scale);
   p.w_sf = scratch;
   p.w_tiled = nullptr;
@@ -651,11 +695,11 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
   p.mailbox = static_cast<uint16_t*>(mailbox);
   p.state = stage_state;
   p.wait_limit_ns = kGemmWaitLimitNs;
-  p.smem = gemm_smem_layout(d.stages, d.split_k, tiles_per_split);
-  e = set_gemm_smem_attribute(d.split_k, static_cast<int>(p.smem.total));
+  p.smem = gemm_smem_layout(d.stages, d.split_k, tiles_per_split, d.fold);
+  e = set_gemm_smem_attribute(d.split_k, d.fold, static_cast<int>(p.smem.total));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  e = launch_relayout_w_scales(static_cast<const uint8_t*>(w_scale), scratch, d.n, d.k, s);
+  e = launch_relayout_w_scales(static_cast<const uint8_t*>(w_scale), scratch, d.n, d.k, d.fold, s);
   if (e != cudaSuccess) return cuda_fail(e, "launching the W scale re-layout");
   e = launch_publish_gemm(tmap_w, tmap_x, p, d.split_k, s);
   if (e != cudaSuccess) return cuda_fail(e, "launching the publishing GEMM");

@@ -9,9 +9,9 @@
 
 namespace mxfp8 {
 
-constexpr int kBlockN = 128;      // output columns per CTA: the MMA's M
-constexpr int kRows = 8;          // activation rows per tile: the MMA's N
-constexpr int kTileK = 128;       // K elements per stage: one 128-byte swizzle row
+constexpr int kBlockN = 128;      // the MMA's M: output columns per CTA (128 / fold folded)
+constexpr int kRows = 8;          // activation rows per x tile: the MMA's N (8 fold folded)
+constexpr int kTileK = 128;       // K elements per stage piece: one 128-byte swizzle row
 constexpr int kSfPerTile = 4;     // scale blocks of 32 per stage
 // Warp 0 loads (one lane per pipe), warp 1 and warps 6.. issue MMAs (one
 // warp per pipe), warps 2-5 run the epilogue.
@@ -54,7 +54,7 @@ struct TmemPlan {
 
 struct GemmParams {
   int32_t n, k, m;
-  int32_t k_tiles;          // ceil(k / 128)
+  int32_t k_tiles;          // stages of K: ceil(k / (128 fold))
   int32_t tiles_per_split;  // ceil(k_tiles / split_k)
   int32_t stages;
   int32_t capacity;
@@ -63,10 +63,12 @@ struct GemmParams {
   int32_t l2_prefetch;      // stages past the ring warmed in L2 before the grid wait
   int32_t pipes;            // producer lanes = MMA-issuing warps (1, 2, 4; divides stages)
   int32_t tmem_load;        // MXFP8_TMEM_LOAD_32X32B or MXFP8_TMEM_LOAD_16X256B
+  int32_t fold;             // K pieces stacked in the MMA's 128 rows: 1, 2, 4 (128/fold
+                            // output columns per CTA)
   TmemPlan tmem;
   const uint8_t* x_scale;   // [m][k/32]
-  const uint8_t* w_sf;      // [n/128][k_tiles][512] tiled W scales
-  const uint8_t* w_tiled;   // [n/128][k_tiles][16384] shared-memory images of W, or nullptr
+  const uint8_t* w_sf;      // [n/R][k_tiles][512] tiled W scales (R = 128 / fold)
+  const uint8_t* w_tiled;   // [n/R][k_tiles][16384] shared-memory images of W, or nullptr
   uint16_t* c;              // [m][n] BF16 or nullptr
   const float* alpha;       // global scale of C (device scalar) or nullptr for 1
   uint16_t* mailbox;        // [3][capacity][n] BF16
@@ -75,16 +77,20 @@ struct GemmParams {
   GemmSmemLayout smem;
 };
 
-GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split);
-TmemPlan gemm_tmem_plan(int stages, int acc_blocks);
+GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, int fold);
+TmemPlan gemm_tmem_plan(int stages, int acc_blocks, int fold);
+int k_tiles_for_fold(int k, int fold);  // ceil(k / (128 fold))
 
 // Kernel launchers (return the CUDA error of the launch).
 cudaError_t launch_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
                                 const GemmParams& p, int split_k, cudaStream_t stream);
-cudaError_t set_gemm_smem_attribute(int split_k, int bytes);
+cudaError_t set_gemm_smem_attribute(int split_k, int fold, int bytes);
+cudaError_t launch_folded_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
+                                       const GemmParams& p, int split_k, cudaStream_t stream);
+cudaError_t set_folded_gemm_smem_attribute(int split_k, int fold, int bytes);
 cudaError_t launch_relayout_w_scales(const uint8_t* w_scale, uint8_t* w_sf, int n, int k,
-                                     cudaStream_t stream);
-cudaError_t launch_tile_weights(const uint8_t* w, uint8_t* w_tiled, int n, int k,
+                                     int fold, cudaStream_t stream);
+cudaError_t launch_tile_weights(const uint8_t* w, uint8_t* w_tiled, int n, int k, int fold,
                                 cudaStream_t stream);
 cudaError_t launch_mailbox_init(uint16_t* mailbox, int32_t* state, int capacity, int n,
                                 cudaStream_t stream);

@@ -1,648 +1,23 @@
-// MXFP8 low-batch GEMM with a publishing epilogue, for sm_103a.
-//
-// C[t][n] = sum_k W[n][k] x[t][k] (page "vllm.models.deepseek_v41.nvidia.
-// specialized_decode.boundary.publishing_gemm", module description "GEMM
-// structure"): the weight is the MMA's A operand (128 output columns per CTA,
-// N/128 tiles), the at most 8 activation rows its B operand (N = 8).  Each
-// CTA of a split-K cluster of S multiplies one K slice; the partials are
-// exchanged through distributed shared memory and each CTA reduces 1/S of
-// the tokens.  The epilogue rounds to BF16, writes C, and publishes every
-// value with negative zero cleared into generation stage_state[0] of the
-// mailbox as aligned 16-byte packs of eight consecutive columns, then one
-// thread sets stage_state[1] (same page, publish_value and epilog_warp).
-//
-// Accumulation.  The tensor core's own FP32 accumulation over a long K loses
-// too much on outputs that nearly cancel, so partial sums leave tensor memory
-// early: each MMA (or each group of acc_blocks MMAs) writes a fresh
-// accumulator slot of a ring, and the epilogue warps fold every slot into a
-// compensated FP32 pair (hi + lo, Knuth's TwoSum) as soon as it completes.
-// The pair is rounded once to BF16 (hi + lo taken exactly, from its FP32
-// bits).
-//
-// Warp roles (pipes = 1, 2 or 4 per launch):
-//   warp 0      TMA producer: one lane per pipe, lane l taking stages
-//               l, l + pipes, ...; per stage the W tile + W scale chunk
-//               (started before the programmatic grid wait) and the x tile.
-//   warp 1, 6.. MMA issuers, one warp per pipe (warp 1 also allocates tensor
-//               memory): one thread each issues, per stage, tcgen05.cp of the
-//               W and x scale chunks and one block-scaled tcgen05.mma per
-//               32-wide K block.  Blocks have 160 + 32 * pipes threads.
-//   warps 2-5   epilogue: x scales staged for the copies, partial sums read
-//               back (tcgen05.ld 32x32b: thread = output column, registers =
-//               tokens) and folded into the compensated sums, split-K
-//               exchange, BF16 rounding, C store, publish.
-//
-// Tensor-memory columns: [acc, +acc_ring * acc_slot) the accumulator ring (FP32,
-// lane = output column, column = block * 8 + token); then the W and x scale
-// rings, one 4-column slot per stage each, filled by tcgen05.cp (32x128b,
-// multicast to the four lane quarters) from 16-byte-row scale chunks in
-// shared memory.  Every scale address is 4-column aligned.
-#include <cuda_bf16.h>
-
+// Host side of the publishing GEMM: shared-memory and tensor-memory plans,
+// the create-time re-layouts of W and its scales, and the launches of the
+// unfolded kernels (the folded ones come from publish_gemm_fold.cu).
 #include <algorithm>
 
-#include "internal.h"
-#include "ptx.cuh"
+#include "publish_gemm_kernel.cuh"
 
 namespace mxfp8 {
 namespace {
 
-constexpr uint32_t kStageTxBytes = kWTileBytes + kXTileBytes + kSfChunkBytes;
-// The 16x256b load's transpose buffer inside W stage 0: 4 warps x 32 columns
-// x 8 tokens x 8 bytes, after the BF16 tile (at most 8 x 128 x 2 bytes).
-constexpr uint32_t kTransposeOffset = 4096;
-static_assert(kTransposeOffset >= kRows * kBlockN * 2 &&
-                  kTransposeOffset + 4 * 32 * kRows * 8 <= kWTileBytes,
-              "the transpose buffer lies in W stage 0, past the BF16 tile");
-static_assert(kMaxAccRing % kMaxPipes == 0 && 4 % kMaxPipes == 0,
-              "every accumulator slot belongs to one pipe");
-static_assert(threads_for_pipes(kMaxPipes) == kMaxThreads && threads_for_pipes(1) == 192,
-              "warps 0-5 always, one more MMA-issuing warp per pipe past the first");
-
-// Instruction descriptor of kind::mxf8f6f4 with block scaling: A and B E4M3
-// (format 0), both K-major, N = 8 (bits 17-22: N >> 3), E8M0 scales (bit 23),
-// M = 128 (bits 24-28: M >> 4).  The scale-factor byte ids of A (bits 29-30)
-// and B (bits 4-5) select the K block inside a 32-bit scale column.
-constexpr uint32_t kIdescBase = (static_cast<uint32_t>(kRows >> 3) << 17) | (1u << 23) |
-                                (static_cast<uint32_t>(kBlockN >> 4) << 24);
-
-__device__ __forceinline__ uint32_t idesc_for_block(uint32_t kb) {
-  return kIdescBase | (kb << 4) | (kb << 29);
-}
-
-// Each BF16 half equal to 0x8000 becomes 0x0000, so no word is the sentinel.
-__device__ __forceinline__ uint32_t clear_negative_zero(uint32_t w) {
-  uint32_t lo = w & 0xFFFFu, hi = w >> 16;
-  lo = (lo == 0x8000u) ? 0u : lo;
-  hi = (hi == 0x8000u) ? 0u : hi;
-  return lo | (hi << 16);
-}
-
-__device__ __forceinline__ void raise_flag(int32_t* state, uint32_t bit) {
-  atomicOr(reinterpret_cast<unsigned int*>(state + 3), bit);
-}
-
-__device__ __forceinline__ void epilogue_barrier() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-
-// Compensated summation: (hi, lo) += v with the rounding error of the add
-// kept in lo (TwoSum: exact error of a floating-point addition, valid for
-// operands of either magnitude order).
-__device__ __forceinline__ void two_sum_add(float& hi, float& lo, float v) {
-  const float s = __fadd_rn(hi, v);
-  const float bp = __fsub_rn(s, hi);
-  const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(v, bp));
-  hi = s;
-  lo = __fadd_rn(lo, err);
-}
-
-// BF16 bits of the exact value hi + lo, rounded once to nearest with ties to
-// even.  TwoSum gives s = fl(hi + lo) and the exact remainder e with
-// |e| <= ulp(s) / 2.  A BF16 midpoint has low 16 bits 0x8000 in FP32, and
-// every other FP32 value lies at least one FP32 ulp from the nearest midpoint,
-// so s + e rounds as s does unless s is itself a midpoint; there the sign of
-// e decides (towards it: away from the midpoint in that direction), and e = 0
-// is a true tie.  BF16 being the upper half of FP32, this covers subnormals
-// and overflow to infinity alike.
-__device__ __forceinline__ uint16_t bf16_bits_from_pair(float hi, float lo) {
-  const float s = __fadd_rn(hi, lo);
-  const float bp = __fsub_rn(s, hi);
-  const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(lo, bp));
-  const uint32_t b = __float_as_uint(s);
-  if ((b & 0x7F800000u) == 0x7F800000u)  // infinity, or NaN (kept quiet)
-    return static_cast<uint16_t>((b >> 16) | ((b & 0x007FFFFFu) != 0u ? 0x0040u : 0u));
-  const uint32_t low = b & 0xFFFFu;
-  const uint32_t keep = b >> 16;  // sign, exponent and the 7 kept mantissa bits
-  bool up;
-  if (low != 0x8000u)
-    up = low > 0x8000u;
-  else if (e == 0.0f)
-    up = (keep & 1u) != 0u;
-  else
-    up = (__float_as_uint(e) >> 31) == (b >> 31);  // e points away from zero
-  return static_cast<uint16_t>(keep + (up ? 1u : 0u));  // magnitude + 1 ulp
-}
-
-// Position in a ring of mbarrier-guarded slots: the slot and the parity of
-// its current use, advanced without divisions in the hot loops.
-struct RingCursor {
-  int slot;
-  uint32_t phase;
-  __device__ __forceinline__ void next(int size) {
-    if (++slot == size) {
-      slot = 0;
-      phase ^= 1u;
-    }
-  }
-};
-
-// kWideLoad: accumulators read with tcgen05.ld 16x256b (else 32x32b); a
-// template parameter so each read-out compiles to its own kernel.
-template <int S, bool kWideLoad>
-__global__ void __launch_bounds__(kMaxThreads, 1)
-    publish_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                        const __grid_constant__ CUtensorMap tmap_x,
-                        const __grid_constant__ GemmParams p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const uint32_t raw_addr = ptx::smem_addr(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  const uint32_t sbase = ptx::smem_addr(smem);
-  const GemmSmemLayout& L = p.smem;
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const uint32_t split = (S > 1) ? ptx::cluster_ctarank() : 0u;
-  const int tile = blockIdx.x / S;
-  const int kt_begin = static_cast<int>(split) * p.tiles_per_split;
-  const int kt_end = min(p.k_tiles, kt_begin + p.tiles_per_split);
-  const int nkt = max(0, kt_end - kt_begin);
-  const int stages = p.stages;
-  const bool per_block = p.acc_blocks == 1;
-  // `pipes` producer lanes and MMA issuers share the ring, and pipes divides
-  // the ring size: then stage i, its slot i % stages, its scale slots and its
-  // accumulator slot (the accumulator ring is a multiple of 4) all belong to
-  // lane / issuer i % pipes, so every mbarrier is waited on by one thread in
-  // use order.  Were a slot to pass between issuers, one could wait on use
-  // u + 1 of it before use u completed, while the phase parity it tests still
-  // shows the phase before (the parity aliases) and the wait returns at once.
-  const int pipes = p.pipes;
-
-  const uint32_t bar_full = sbase + L.bars;                     // [stages]
-  const uint32_t bar_empty = bar_full + 8u * stages;            // [stages]
-  const int acc_ring = static_cast<int>(p.tmem.acc_ring);
-  const uint32_t bar_acc_full = bar_empty + 8u * stages;          // [acc_ring]
-  const uint32_t bar_acc_empty = bar_acc_full + 8u * kMaxAccRing;  // [acc_ring]
-  const uint32_t bar_sfb = bar_acc_empty + 8u * kMaxAccRing;
-  const uint32_t bar_recv = bar_sfb + 8u;
-  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L.misc);  // [0] tmem base, [1] generation
-
-  if (tid == 0) {
-    ptx::prefetch_tensormap(&tmap_w);
-    ptx::prefetch_tensormap(&tmap_x);
-    for (int s = 0; s < stages; ++s) {
-      ptx::mbar_init(bar_full + 8u * s, 1);
-      ptx::mbar_init(bar_empty + 8u * s, 1);
-    }
-    for (int r = 0; r < acc_ring; ++r) {
-      ptx::mbar_init(bar_acc_full + 8u * r, 1);
-      ptx::mbar_init(bar_acc_empty + 8u * r, 128);
-    }
-    ptx::mbar_init(bar_sfb, 128);
-    ptx::mbar_init(bar_recv, 1);
-    ptx::fence_mbarrier_init();
-    ptx::fence_proxy_async_smem();
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc(sbase + L.misc, p.tmem.cols);
-    ptx::tmem_relinquish();
-  }
-  ptx::tc_fence_before();
-  if (S > 1) {
-    ptx::cluster_sync();  // peers' barriers exist before any remote store
-  } else {
-    __syncthreads();
-  }
-  ptx::tc_fence_after();
-  const uint32_t tmem = misc[0];
-
-  if (warp == 0) {
-    // -------------------------------------------------------------- producer
-    // The bulk copies one thread issues are served one after another (about
-    // 43 GB/s from HBM per issuing thread, whatever the ring depth), so lane
-    // l < pipes issues the W tile, W scale chunk and x tile of stages l,
-    // l + pipes, l + 2 * pipes, ...
-    const int producers = pipes;
-    if (lane == 0) ptx::launch_dependents();
-    if (lane < producers) {
-      const uint64_t pol_stream = ptx::policy_evict_first();
-      const uint64_t pol_keep = ptx::policy_evict_last();
-      const int npre = min(stages, nkt);
-      // One 128 x 128-byte W tile: a contiguous 16 KB image from the tiled
-      // copy, or a 2-D TMA box (with the same 128-byte swizzle) of W in place.
-      auto load_w_tile = [&](uint32_t dst, int kt, uint32_t bar) {
-        if (p.w_tiled != nullptr)
-          ptx::bulk_load(dst, p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt) * kWTileBytes,
-                         kWTileBytes, bar, pol_stream);
-        else
-          ptx::tma_load_2d(dst, &tmap_w, kt * kTileK, tile * kBlockN, bar, pol_stream);
-      };
-      // W and its scales do not depend on the previous kernel: start them now.
-      for (int i = lane; i < npre; i += producers) {
-        const uint32_t full = bar_full + 8u * i;
-        const int kt = kt_begin + i;
-        ptx::mbar_arrive_expect_tx(full, kStageTxBytes);
-        load_w_tile(sbase + L.w + i * kWTileBytes, kt, full);
-        ptx::bulk_load(sbase + L.sfa + i * kSfChunkBytes,
-                       p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt) * kSfChunkBytes,
-                       kSfChunkBytes, full, pol_stream);
-      }
-      // Warm L2 with the stages that come after the ring, so HBM keeps
-      // streaming while the previous kernel finishes and the grid wait holds.
-      const int nwarm = min(nkt, npre + p.l2_prefetch);
-      if (lane == 0 && nwarm > npre) {
-        if (p.w_tiled != nullptr) {
-          ptx::prefetch_l2(p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt_begin + npre) *
-                                           kWTileBytes,
-                           static_cast<uint32_t>(nwarm - npre) * kWTileBytes);
-        } else {
-          for (int i = npre; i < nwarm; ++i)
-            ptx::prefetch_l2_tile(&tmap_w, (kt_begin + i) * kTileK, tile * kBlockN);
-        }
-        ptx::prefetch_l2(p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt_begin + npre) *
-                                      kSfChunkBytes,
-                         static_cast<uint32_t>(nwarm - npre) * kSfChunkBytes);
-      }
-      // The activations follow the programmatic grid wait.
-      ptx::grid_dependency_wait();
-      for (int i = lane; i < npre; i += producers)
-        ptx::tma_load_2d(sbase + L.x + i * kXTileBytes, &tmap_x, (kt_begin + i) * kTileK, 0,
-                         bar_full + 8u * i, pol_keep);
-      // From here every slot is on its second or later use: wait until the
-      // MMAs of its previous use released it.  This lane's stages advance the
-      // ring by `producers` slots at a time.
-      int issued = -1;  // the last stage this lane issued
-      for (int i = lane; i < npre; i += producers) issued = i;
-      const int first = npre + ((lane - npre % producers) % producers + producers) % producers;
-      RingCursor ring{first - npre, 1u};  // npre == stages whenever this loop runs
-      for (int i = first; i < nkt; i += producers) {
-        const int s = ring.slot;
-        if (!ptx::mbar_wait(bar_empty + 8u * s, ring.phase ^ 1u, p.wait_limit_ns)) {
-          raise_flag(p.state, 0x2u);
-          break;
-        }
-        const uint32_t full = bar_full + 8u * s;
-        const int kt = kt_begin + i;
-        ptx::mbar_arrive_expect_tx(full, kStageTxBytes);
-        load_w_tile(sbase + L.w + s * kWTileBytes, kt, full);
-        ptx::bulk_load(sbase + L.sfa + s * kSfChunkBytes,
-                       p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt) * kSfChunkBytes,
-                       kSfChunkBytes, full, pol_stream);
-        ptx::tma_load_2d(sbase + L.x + s * kXTileBytes, &tmap_x, kt * kTileK, 0, full, pol_keep);
-        issued = i;
-        ring.slot += producers;
-        if (ring.slot >= stages) {
-          ring.slot -= stages;
-          ring.phase ^= 1u;
-        }
-      }
-      // This lane's copies still in flight land before the CTA leaves
-      // (immediate when the MMAs consumed them, which is the normal case):
-      // its stages among the last `stages` of the split, the latest use of
-      // their slots (no stage past nkt - 1 reuses them, so each wait is on
-      // the phase of this lane's own copy).
-      for (int i = issued; i >= max(0, nkt - stages); i -= producers)
-        ptx::mbar_wait(bar_full + 8u * (i % stages), static_cast<uint32_t>(i / stages) & 1u,
-                       p.wait_limit_ns);
-    }
-  } else if (warp == 1 || warp >= 6) {
-    const int issuer = warp == 1 ? 0 : warp - 5;
-    if (lane == 0 && issuer < pipes) {
-      // --------------------------------------------------------- MMA issuers
-      // tcgen05 instructions cost their issuing thread a fixed time each
-      // (about 65 ns per stage of 2 copies, 4 MMAs and 2 commits), which caps
-      // one thread near 65 GB/s of weight, so issuer j < pipes takes stages
-      // j, j + pipes, ...
-      ptx::grid_dependency_wait();
-      bool ok = true;
-      if (nkt > 0) {
-        ok = ptx::mbar_wait(bar_sfb, 0, p.wait_limit_ns);
-        if (!ok) raise_flag(p.state, 0x2u);
-        ptx::tc_fence_after();
-      }
-      RingCursor stage{0, 0u}, acc{0, 0u};
-      for (int q = 0; q < issuer; ++q) {
-        stage.next(stages);
-        acc.next(acc_ring);
-      }
-      for (int i = issuer; i < nkt && ok; i += pipes) {
-        const int s = stage.slot;
-        const int r = acc.slot;
-        if (!ptx::mbar_wait(bar_full + 8u * s, stage.phase, p.wait_limit_ns) ||
-            (i >= acc_ring &&
-             !ptx::mbar_wait(bar_acc_empty + 8u * r, acc.phase ^ 1u, p.wait_limit_ns))) {
-          raise_flag(p.state, 0x2u);
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        const uint32_t sfa_t = tmem + p.tmem.sfa + 4u * s;
-        const uint32_t sfb_t = tmem + p.tmem.sfb + 4u * s;
-        ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::desc_rows16(sbase + L.sfa + s * kSfChunkBytes));
-        ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::desc_rows16(sbase + L.sx + i * 128));
-        const uint32_t a0 = sbase + L.w + s * kWTileBytes;
-        const uint32_t b0 = sbase + L.x + s * kXTileBytes;
-        const uint32_t d0 = tmem + p.tmem.acc + p.tmem.acc_slot * static_cast<uint32_t>(r);
-#pragma unroll
-        for (uint32_t kb = 0; kb < kSfPerTile; ++kb) {
-          // One 8-column accumulator per block, or one per stage.
-          const uint32_t d = per_block ? d0 + 8u * kb : d0;
-          const uint32_t accumulate = per_block ? 0u : (kb > 0 ? 1u : 0u);
-          ptx::mma_mxf8(d, ptx::desc_kmajor_sw128(a0 + 32u * kb),
-                        ptx::desc_kmajor_sw128(b0 + 32u * kb), idesc_for_block(kb), accumulate,
-                        sfa_t, sfb_t);
-        }
-        ptx::mma_commit(bar_empty + 8u * s);
-        ptx::mma_commit(bar_acc_full + 8u * r);
-        for (int q = 0; q < pipes; ++q) {
-          stage.next(stages);
-          acc.next(acc_ring);
-        }
-      }
-    }
-  }
-  if (warp < 2 || warp >= 6) {
-    __syncwarp();
-    if (S > 1) {
-      ptx::cluster_sync();    // matches the epilogue's barrier before the exchange
-      ptx::cluster_arrive();  // these warps address no peer: the final barrier's arrival
-    }
-  } else {
-    // ------------------------------------------------------------- epilogue
-    const int etid = tid - 64;               // 0..127
-    const int quarter = warp & 3;            // the 32 TMEM lanes this warp reaches
-    const int col = quarter * 32 + lane;     // output column within the tile
-    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    ptx::grid_dependency_wait();
-    if (etid == 0) misc[1] = ptx::ld_volatile_u32(p.state + 0);
-
-    // x scales of this CTA's K range as one 128-byte chunk per K tile: row r
-    // (< 8) of tile j at byte j * 128 + r * 16, its four E8M0 codes first and
-    // 12 zero bytes after.  Rows >= m and blocks past K take 127 (a scale of
-    // 1; those x elements are zero).  The copy of a chunk reads 32 rows; rows
-    // 8..31 (the next chunks, or the tail) feed no output column.  (Loading
-    // every word into registers before any store measured 2-6 % slower per
-    // call than this loop.)
-    uint8_t* sx = smem + L.sx;
-    const int kblocks = p.k / 32;
-    const int words = kRows * nkt;
-    constexpr int kMaxWords = kRows * kMaxTilesPerSplit / 128;  // per thread
-#pragma unroll
-    for (int it = 0; it < kMaxWords; ++it) {
-      const int w = etid + it * 128;
-      if (w >= words) break;
-      const int r = w / nkt;
-      const int j = w - r * nkt;
-      uint32_t v = 0x7F7F7F7Fu;
-      if (r < p.m) {
-        const int kb0 = (kt_begin + j) * kSfPerTile;
-        const uint8_t* row = p.x_scale + static_cast<size_t>(r) * kblocks;
-        uint32_t b[kSfPerTile];
-#pragma unroll
-        for (int q = 0; q < kSfPerTile; ++q) b[q] = kb0 + q < kblocks ? row[kb0 + q] : 127u;
-        v = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-      }
-      *reinterpret_cast<uint4*>(sx + j * 128 + r * 16) = make_uint4(v, 0u, 0u, 0u);
-    }
-    ptx::fence_proxy_async_smem();  // the tensor-memory copy reads them
-    ptx::mbar_arrive(bar_sfb);
-
-    // Fold every completed accumulator slot into the compensated sums.  With
-    // the 32x32b load thread = output column and hi[t] / lo[t] hold token t;
-    // with the 16x256b load (two per slot, lane halves 0-15 and 16-31 of the
-    // warp's quarter) element a = 4 h + r of a thread holds column
-    // 16 h + 8 (r / 2) + lane / 4 of the quarter and token 2 (lane % 4) +
-    // r % 2, and one warp-local transpose after the loop brings back the
-    // column-per-thread layout.  Each element sees the same values in the same
-    // order either way, so the two loads give identical bits.
-    constexpr bool wide_load = kWideLoad;
-    float hi[kRows], lo[kRows];
-#pragma unroll
-    for (int t = 0; t < kRows; ++t) hi[t] = lo[t] = 0.0f;
-    RingCursor acc{0, 0u};
-    for (int i = 0; i < nkt; ++i, acc.next(acc_ring)) {
-      const int r = acc.slot;
-      if (!ptx::mbar_wait(bar_acc_full + 8u * r, acc.phase, p.wait_limit_ns)) {
-        raise_flag(p.state, 0x2u);
-        break;
-      }
-      ptx::tc_fence_after();
-      const uint32_t slot =
-          tmem + lane_base + p.tmem.acc + p.tmem.acc_slot * static_cast<uint32_t>(r);
-      if constexpr (wide_load) {
-        constexpr uint32_t kHalf = 16u << 16;  // lane offset of the second half
-        if (per_block) {
-          uint32_t v0[16], v1[16];
-          ptx::tmem_ld_16x256b_x4(slot, v0);
-          ptx::tmem_ld_16x256b_x4(slot + kHalf, v1);
-          ptx::tmem_wait_ld();
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(bar_acc_empty + 8u * r);
-#pragma unroll
-          for (int kb = 0; kb < kSfPerTile; ++kb)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              two_sum_add(hi[e], lo[e], __uint_as_float(v0[kb * 4 + e]));
-              two_sum_add(hi[4 + e], lo[4 + e], __uint_as_float(v1[kb * 4 + e]));
-            }
-        } else {
-          uint32_t v0[4], v1[4];
-          ptx::tmem_ld_16x256b_x1(slot, v0);
-          ptx::tmem_ld_16x256b_x1(slot + kHalf, v1);
-          ptx::tmem_wait_ld();
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(bar_acc_empty + 8u * r);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            two_sum_add(hi[e], lo[e], __uint_as_float(v0[e]));
-            two_sum_add(hi[4 + e], lo[4 + e], __uint_as_float(v1[e]));
-          }
-        }
-      } else if (per_block) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(slot, v);
-        ptx::tmem_wait_ld();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_acc_empty + 8u * r);
-#pragma unroll
-        for (int kb = 0; kb < kSfPerTile; ++kb)
-#pragma unroll
-          for (int t = 0; t < kRows; ++t)
-            two_sum_add(hi[t], lo[t], __uint_as_float(v[kb * 8 + t]));
-      } else {
-        uint32_t v[8];
-        ptx::tmem_ld_32x32b_x8(slot, v);
-        ptx::tmem_wait_ld();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_acc_empty + 8u * r);
-#pragma unroll
-        for (int t = 0; t < kRows; ++t) two_sum_add(hi[t], lo[t], __uint_as_float(v[t]));
-      }
-    }
-
-    if constexpr (wide_load) {
-      // Transpose through this warp's 2 KB of the dead W stage 0 (past the
-      // BF16 tile): [column of the quarter][token] pairs.
-      float2* pairs = reinterpret_cast<float2*>(smem + L.w + kTransposeOffset) + quarter * 32 * kRows;
-#pragma unroll
-      for (int a = 0; a < kRows; ++a) {
-        const int c = (a / 4) * 16 + ((a % 4) / 2) * 8 + lane / 4;
-        const int t = 2 * (lane % 4) + (a % 2);
-        pairs[c * kRows + t] = make_float2(hi[a], lo[a]);
-      }
-      __syncwarp();
-#pragma unroll
-      for (int t = 0; t < kRows; ++t) {
-        const float2 v = pairs[lane * kRows + t];
-        hi[t] = v.x;
-        lo[t] = v.y;
-      }
-    }
-
-    // Split-K: every CTA sends the (hi, lo) pairs of the tokens it does not
-    // own to their owners, then sums the S pairs of its own tokens in K-slice
-    // order.  A split with no K tiles contributes zeros.  The receive buffer
-    // is [sender][column][token][hi, lo]: one CTA's pairs for one column are
-    // 8 * kShard contiguous bytes, sent as 16-byte stores (8-byte ones at
-    // S = 8, where each CTA owns one token).
-    constexpr int kShard = kRows / S;
-    static_assert(kShard * S == kRows && (kShard == 1 || kShard % 2 == 0),
-                  "tokens split evenly, in pairs or one per CTA");
-    float own_hi[kShard], own_lo[kShard];
-    if constexpr (S > 1) {
-      constexpr int kPairBytes = kShard * 8;
-      // The receive buffer lives in the W ring, which is dead only once every
-      // CTA of the cluster has finished its main loop.
-      ptx::cluster_sync();
-      if (etid == 0)
-        ptx::mbar_arrive_expect_tx(bar_recv,
-                                   static_cast<uint32_t>((S - 1) * kBlockN * kPairBytes));
-#pragma unroll
-      for (int peer = 0; peer < S; ++peer) {
-        if (peer == static_cast<int>(split)) continue;
-        const int sender = static_cast<int>(split) < peer ? static_cast<int>(split)
-                                                          : static_cast<int>(split) - 1;
-        const uint32_t remote_bar = ptx::map_to_rank(bar_recv, peer);
-        const uint32_t remote =
-            ptx::map_to_rank(sbase + L.recv + (sender * kBlockN + col) * kPairBytes, peer);
-        if constexpr (kShard == 1) {
-          ptx::st_async_remote_v2(remote, __float_as_uint(hi[peer]), __float_as_uint(lo[peer]),
-                                  remote_bar);
-        } else {
-#pragma unroll
-          for (int jj = 0; jj < kShard; jj += 2)
-            ptx::st_async_remote_v4(
-                remote + jj * 8,
-                make_uint4(__float_as_uint(hi[peer * kShard + jj]),
-                           __float_as_uint(lo[peer * kShard + jj]),
-                           __float_as_uint(hi[peer * kShard + jj + 1]),
-                           __float_as_uint(lo[peer * kShard + jj + 1])),
-                remote_bar);
-        }
-      }
-      // This thread addresses no peer after its sends: its half of the final
-      // cluster barrier, whose wait comes before the CTA exits.
-      ptx::cluster_arrive();
-      if (!ptx::mbar_wait_cluster(bar_recv, 0, p.wait_limit_ns)) raise_flag(p.state, 0x2u);
-      const uint8_t* recv = smem + L.recv;
-#pragma unroll
-      for (int jj = 0; jj < kShard; ++jj) {
-        float sh = 0.0f, sl = 0.0f;
-#pragma unroll
-        for (int src = 0; src < S; ++src) {
-          float vh, vl;
-          if (src == static_cast<int>(split)) {
-            vh = 0.0f;
-            vl = 0.0f;
-#pragma unroll
-            for (int q = 0; q < kRows; ++q)
-              if (q == static_cast<int>(split) * kShard + jj) {
-                vh = hi[q];
-                vl = lo[q];
-              }
-          } else {
-            const int sidx = src < static_cast<int>(split) ? src : src - 1;
-            const float2 pair = *reinterpret_cast<const float2*>(
-                recv + (sidx * kBlockN + col) * kPairBytes + jj * 8);
-            vh = pair.x;
-            vl = pair.y;
-          }
-          two_sum_add(sh, sl, vh);
-          sl = __fadd_rn(sl, vl);
-        }
-        own_hi[jj] = sh;
-        own_lo[jj] = sl;
-      }
-    } else {
-#pragma unroll
-      for (int jj = 0; jj < kShard; ++jj) {
-        own_hi[jj] = hi[jj];
-        own_lo[jj] = lo[jj];
-      }
-    }
-
-    // The global scale (gemm page, epilog_warp with use_scale: the
-    // accumulator times mScale[0]) multiplies the compensated sum before its
-    // one rounding: alpha * hi exactly as a product and its FMA error, plus
-    // alpha * lo.  It is read after the grid wait like x.
-    if (p.alpha != nullptr) {
-      const float a = *p.alpha;
-#pragma unroll
-      for (int jj = 0; jj < kShard; ++jj) {
-        const float ph = __fmul_rn(a, own_hi[jj]);
-        const float pe = __fmaf_rn(a, own_hi[jj], -ph);
-        own_lo[jj] = __fmaf_rn(a, own_lo[jj], pe);
-        own_hi[jj] = ph;
-      }
-    }
-
-    uint16_t* ctile = reinterpret_cast<uint16_t*>(smem + L.ctile);  // [kShard][128]
-#pragma unroll
-    for (int jj = 0; jj < kShard; ++jj)
-      ctile[jj * kBlockN + col] = bf16_bits_from_pair(own_hi[jj], own_lo[jj]);
-    epilogue_barrier();
-
-    const uint32_t g = misc[1];
-    const bool generation_ok = g < static_cast<uint32_t>(kGenerations);
-    const size_t n0 = static_cast<size_t>(tile) * kBlockN;
-    for (int pk = etid; pk < kShard * (kBlockN / 8); pk += 128) {
-      const int jj = pk / (kBlockN / 8);
-      const int chunk = pk % (kBlockN / 8);
-      const int t = static_cast<int>(split) * kShard + jj;
-      if (t >= p.m) continue;
-      const uint4 v = *reinterpret_cast<const uint4*>(ctile + jj * kBlockN + chunk * 8);
-      const size_t column = n0 + chunk * 8;
-      if (p.c != nullptr) ptx::st_v4(p.c + static_cast<size_t>(t) * p.n + column, v);
-      if (p.publish && generation_ok) {
-        const uint4 clean = make_uint4(clear_negative_zero(v.x), clear_negative_zero(v.y),
-                                       clear_negative_zero(v.z), clear_negative_zero(v.w));
-        ptx::st_v4(p.mailbox + (static_cast<size_t>(g) * p.capacity + t) * p.n + column, clean);
-      }
-    }
-    // Hand the generation to the consumer, once per grid.
-    if (p.publish && blockIdx.x == 0 && etid == 0) {
-      if (generation_ok)
-        p.state[1] = static_cast<int32_t>(g);
-      else
-        raise_flag(p.state, 0x4u);
-    }
-  }
-
-  // --------------------------------------------------------------- teardown
-  ptx::tc_fence_before();
-  __syncthreads();
-  if (S > 1) {
-    // No CTA leaves while a peer may still address it: every thread arrived
-    // after its last remote store, and this CTA's own receive barrier
-    // completed, so the wait is normally immediate.
-    __syncwarp();
-    ptx::cluster_wait();
-  }
-  if (warp == 1) {
-    ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, p.tmem.cols);
-  }
-}
-
-// W scales [n][k/32] -> [n/128][k_tiles][512]: inside a chunk, row r of the
-// tile and K block b of the stage sit at byte (r % 32) * 16 + (r / 32) * 4 + b,
-// the order the 32x128b tensor-memory copy and the MMA's scale lookup expect.
-// Blocks past K take 127.
+// W scales [n][k/32] -> [n/R][k_tiles][512] (R = 128 / fold rows per CTA,
+// k_tiles = ceil(k / (128 fold))): inside a chunk, MMA row a and K block b of
+// a 128-wide piece sit at byte (a % 32) * 16 + (a / 32) * 4 + b, the order the
+// 32x128b tensor-memory copy and the MMA's scale lookup expect; MMA row a is
+// weight row a % R of the tile in K piece a / R.  Blocks past K take 127.
 __global__ void relayout_w_scales_kernel(const uint8_t* __restrict__ w_scale,
                                          uint8_t* __restrict__ w_sf, int n, int kblocks,
-                                         int k_tiles) {
-  const size_t total = static_cast<size_t>(n / kBlockN) * k_tiles * kSfChunkBytes;
+                                         int k_tiles, int fold) {
+  const int rows = kBlockN / fold;
+  const size_t total = static_cast<size_t>(n / rows) * k_tiles * kSfChunkBytes;
   for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < total;
        idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const size_t chunk = idx / kSfChunkBytes;
@@ -652,89 +27,70 @@ __global__ void relayout_w_scales_kernel(const uint8_t* __restrict__ w_scale,
     const int r0 = within / 16;
     const int r1 = (within % 16) / 4;
     const int b = within % 4;
-    const int row = tile * kBlockN + r1 * 32 + r0;
-    const int blk = kt * kSfPerTile + b;
+    const int arow = r1 * 32 + r0;
+    const int row = tile * rows + arow % rows;
+    const int blk = (kt * fold + arow / rows) * kSfPerTile + b;
     w_sf[idx] = blk < kblocks ? w_scale[static_cast<size_t>(row) * kblocks + blk] : 127;
   }
 }
 
-// W [n][k] -> [n/128][k_tiles][16384]: each 16 KB block is the shared-memory
-// image of one 128-row x 128-byte tile in the 128-byte swizzle (row r at byte
-// r * 128, its 16-byte chunk c at position c ^ (r % 8)), so one bulk copy
-// lands it exactly as a swizzled TMA box would.  Bytes past K are zero.
+// W [n][k] -> [n/R][k_tiles][16384]: each 16 KB block is the shared-memory
+// image of one stage, 128 MMA rows x 128 bytes in the 128-byte swizzle (row a
+// at byte a * 128, its 16-byte chunk c at position c ^ (a % 8)), MMA row a
+// being weight row a % R of the tile in K piece a / R; one bulk copy lands it
+// exactly as the fold's swizzled TMA boxes would.  Bytes past K are zero.
 __global__ void tile_weights_kernel(const uint8_t* __restrict__ w, uint8_t* __restrict__ w_tiled,
-                                    int n, int k, int k_tiles) {
-  const size_t chunks = static_cast<size_t>(n / kBlockN) * k_tiles * (kWTileBytes / 16);
+                                    int n, int k, int k_tiles, int fold) {
+  const int rows = kBlockN / fold;
+  const size_t chunks = static_cast<size_t>(n / rows) * k_tiles * (kWTileBytes / 16);
   for (size_t q = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; q < chunks;
        q += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const size_t block = q / (kWTileBytes / 16);
     const int within = static_cast<int>(q % (kWTileBytes / 16));
     const int tile = static_cast<int>(block / k_tiles);
     const int kt = static_cast<int>(block % k_tiles);
-    const int r = within / 8;
+    const int a = within / 8;
     const int position = within % 8;
-    const int c = position ^ (r & 7);
-    const int k0 = kt * kTileK + c * 16;
+    const int c = position ^ (a & 7);
+    const int k0 = (kt * fold + a / rows) * kTileK + c * 16;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (k0 < k)
-      v = *reinterpret_cast<const uint4*>(w + static_cast<size_t>(tile * kBlockN + r) * k + k0);
+      v = *reinterpret_cast<const uint4*>(w + static_cast<size_t>(tile * rows + a % rows) * k + k0);
     reinterpret_cast<uint4*>(w_tiled)[q] = v;
   }
 }
 
-template <int S, bool kWideLoad>
-cudaError_t launch_impl(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, const GemmParams& p,
-                        cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((p.n / kBlockN) * S), 1, 1);
-  cfg.blockDim = dim3(static_cast<unsigned>(threads_for_pipes(p.pipes)), 1, 1);
-  cfg.dynamicSmemBytes = p.smem.total;
-  cfg.stream = stream;
-  cudaLaunchAttribute attrs[2];
-  int count = 0;
-  attrs[count].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attrs[count].val.programmaticStreamSerializationAllowed = 1;
-  ++count;
-  if (S > 1) {
-    attrs[count].id = cudaLaunchAttributeClusterDimension;
-    attrs[count].val.clusterDim.x = S;
-    attrs[count].val.clusterDim.y = 1;
-    attrs[count].val.clusterDim.z = 1;
-    ++count;
-  }
-  cfg.attrs = attrs;
-  cfg.numAttrs = count;
-  return cudaLaunchKernelEx(&cfg, publish_gemm_kernel<S, kWideLoad>, tmap_w, tmap_x, p);
-}
-
 }  // namespace
 
-GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split) {
+GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, int fold) {
   (void)split_k;
   GemmSmemLayout L{};
   L.w = 0;
   L.x = L.w + stages * kWTileBytes;
-  L.sfa = L.x + stages * kXTileBytes;
+  L.sfa = L.x + stages * kXTileBytes * fold;
   // Written only after the main loop: the epilogue's BF16 tile in W stage 0,
   // the split-K partials from peers ((S-1) x 8/S x 128 x 8 bytes <= 6 KB) in
   // W stage 1 (every ring has at least two stages).
   L.ctile = L.w;
   L.recv = L.w + kWTileBytes;
-  // One 128-byte x scale chunk per K tile, plus the 384 bytes the copy of the
-  // last chunk reads past it (rows that feed no output column).
+  // One 128 fold-byte x scale chunk per stage, plus the 384 bytes the copy of
+  // the last chunk reads past it (rows that feed no kept column).
   L.sx = L.sfa + stages * kSfChunkBytes;
-  const uint32_t sx_bytes = static_cast<uint32_t>(tiles_per_split * 128 + 384);
+  const uint32_t sx_bytes = static_cast<uint32_t>(tiles_per_split * 128 * fold + 384);
   L.bars = (L.sx + sx_bytes + 7u) & ~7u;
   L.misc = L.bars + static_cast<uint32_t>(2 * stages + 2 * kMaxAccRing + 2) * 8u;
   L.total = L.misc + 16u + 1024u;
   return L;
 }
 
-TmemPlan gemm_tmem_plan(int stages, int acc_blocks) {
+TmemPlan gemm_tmem_plan(int stages, int acc_blocks, int fold) {
   TmemPlan t{};
   t.acc = 0;
-  t.acc_slot = acc_blocks == 1 ? static_cast<uint32_t>(kSfPerTile * kRows) : kRows;
-  t.acc_ring = acc_blocks == 1 ? 4u : static_cast<uint32_t>(kMaxAccRing);
+  const uint32_t block_cols = static_cast<uint32_t>(kRows * fold);  // one MMA's N
+  t.acc_slot = acc_blocks == 1 ? kSfPerTile * block_cols : block_cols;
+  // 32-column slots (fold 4) come 4 to a ring, so the plan stays within 256
+  // columns.
+  t.acc_ring = (acc_blocks == 1 || fold == 4) ? 4u : static_cast<uint32_t>(kMaxAccRing);
   t.sfa = t.acc + t.acc_slot * t.acc_ring;
   t.sfb = t.sfa + 4u * static_cast<uint32_t>(stages);
   const uint32_t used = t.sfb + 4u * static_cast<uint32_t>(stages);
@@ -743,24 +99,22 @@ TmemPlan gemm_tmem_plan(int stages, int acc_blocks) {
   return t;
 }
 
-cudaError_t set_gemm_smem_attribute(int split_k, int bytes) {
-  auto set = [bytes](auto kernel) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  };
+cudaError_t set_gemm_smem_attribute(int split_k, int fold, int bytes) {
+  if (fold != 1) return set_folded_gemm_smem_attribute(split_k, fold, bytes);
   cudaError_t e = cudaSuccess;
   switch (split_k) {
     case 1:
-      if ((e = set(publish_gemm_kernel<1, false>)) != cudaSuccess) return e;
-      return set(publish_gemm_kernel<1, true>);
+      if ((e = set_smem_impl<1, false, 1>(bytes)) != cudaSuccess) return e;
+      return set_smem_impl<1, true, 1>(bytes);
     case 2:
-      if ((e = set(publish_gemm_kernel<2, false>)) != cudaSuccess) return e;
-      return set(publish_gemm_kernel<2, true>);
+      if ((e = set_smem_impl<2, false, 1>(bytes)) != cudaSuccess) return e;
+      return set_smem_impl<2, true, 1>(bytes);
     case 4:
-      if ((e = set(publish_gemm_kernel<4, false>)) != cudaSuccess) return e;
-      return set(publish_gemm_kernel<4, true>);
+      if ((e = set_smem_impl<4, false, 1>(bytes)) != cudaSuccess) return e;
+      return set_smem_impl<4, true, 1>(bytes);
     case 8:
-      if ((e = set(publish_gemm_kernel<8, false>)) != cudaSuccess) return e;
-      return set(publish_gemm_kernel<8, true>);
+      if ((e = set_smem_impl<8, false, 1>(bytes)) != cudaSuccess) return e;
+      return set_smem_impl<8, true, 1>(bytes);
     default:
       return cudaErrorInvalidValue;
   }
@@ -768,42 +122,50 @@ cudaError_t set_gemm_smem_attribute(int split_k, int bytes) {
 
 cudaError_t launch_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
                                 const GemmParams& p, int split_k, cudaStream_t stream) {
+  if (p.fold != 1) return launch_folded_publish_gemm(tmap_w, tmap_x, p, split_k, stream);
   const bool wide = p.tmem_load == MXFP8_TMEM_LOAD_16X256B;
   switch (split_k) {
     case 1:
-      return wide ? launch_impl<1, true>(tmap_w, tmap_x, p, stream)
-                  : launch_impl<1, false>(tmap_w, tmap_x, p, stream);
+      return wide ? launch_impl<1, true, 1>(tmap_w, tmap_x, p, stream)
+                  : launch_impl<1, false, 1>(tmap_w, tmap_x, p, stream);
     case 2:
-      return wide ? launch_impl<2, true>(tmap_w, tmap_x, p, stream)
-                  : launch_impl<2, false>(tmap_w, tmap_x, p, stream);
+      return wide ? launch_impl<2, true, 1>(tmap_w, tmap_x, p, stream)
+                  : launch_impl<2, false, 1>(tmap_w, tmap_x, p, stream);
     case 4:
-      return wide ? launch_impl<4, true>(tmap_w, tmap_x, p, stream)
-                  : launch_impl<4, false>(tmap_w, tmap_x, p, stream);
+      return wide ? launch_impl<4, true, 1>(tmap_w, tmap_x, p, stream)
+                  : launch_impl<4, false, 1>(tmap_w, tmap_x, p, stream);
     case 8:
-      return wide ? launch_impl<8, true>(tmap_w, tmap_x, p, stream)
-                  : launch_impl<8, false>(tmap_w, tmap_x, p, stream);
+      return wide ? launch_impl<8, true, 1>(tmap_w, tmap_x, p, stream)
+                  : launch_impl<8, false, 1>(tmap_w, tmap_x, p, stream);
     default:
       return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_tile_weights(const uint8_t* w, uint8_t* w_tiled, int n, int k,
+int k_tiles_for_fold(int k, int fold) {
+  const int stage_k = kTileK * fold;
+  return (k + stage_k - 1) / stage_k;
+}
+
+cudaError_t launch_tile_weights(const uint8_t* w, uint8_t* w_tiled, int n, int k, int fold,
                                 cudaStream_t stream) {
-  const int k_tiles = (k + kTileK - 1) / kTileK;
-  const size_t chunks = static_cast<size_t>(n / kBlockN) * k_tiles * (kWTileBytes / 16);
+  const int k_tiles = k_tiles_for_fold(k, fold);
+  const size_t chunks =
+      static_cast<size_t>(n / (kBlockN / fold)) * k_tiles * (kWTileBytes / 16);
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<size_t>((chunks + threads - 1) / threads, 8192));
-  tile_weights_kernel<<<blocks, threads, 0, stream>>>(w, w_tiled, n, k, k_tiles);
+  tile_weights_kernel<<<blocks, threads, 0, stream>>>(w, w_tiled, n, k, k_tiles, fold);
   return cudaGetLastError();
 }
 
 cudaError_t launch_relayout_w_scales(const uint8_t* w_scale, uint8_t* w_sf, int n, int k,
-                                     cudaStream_t stream) {
-  const int k_tiles = (k + kTileK - 1) / kTileK;
-  const size_t total = static_cast<size_t>(n / kBlockN) * k_tiles * kSfChunkBytes;
+                                     int fold, cudaStream_t stream) {
+  const int k_tiles = k_tiles_for_fold(k, fold);
+  const size_t total = static_cast<size_t>(n / (kBlockN / fold)) * k_tiles * kSfChunkBytes;
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<size_t>((total + threads - 1) / threads, 4096));
-  relayout_w_scales_kernel<<<blocks, threads, 0, stream>>>(w_scale, w_sf, n, k / 32, k_tiles);
+  relayout_w_scales_kernel<<<blocks, threads, 0, stream>>>(w_scale, w_sf, n, k / 32, k_tiles,
+                                                           fold);
   return cudaGetLastError();
 }
 

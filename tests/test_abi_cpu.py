@@ -62,6 +62,23 @@ def test_workspace_bytes(lib):
     assert lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(d)) == 0
 
 
+def test_workspace_bytes_folded(lib):
+    # fold f: N / (128 / f) tiles x ceil(K / (128 f)) stages, 512 scale bytes and
+    # 16 KB of W each; K pads to a multiple of 128 f.
+    in_place, tiled = _lib.W_IN_PLACE, _lib.W_TILED
+    d = _lib.GemmDesc(4096, 4096, 8, 1, 0, 0, 0, in_place, 0, 0, 0, 4)
+    assert lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(d)) == 128 * 8 * 512
+    d = _lib.GemmDesc(4096, 4096, 8, 1, 0, 0, 0, tiled, 0, 0, 0, 4)
+    assert lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(d)) == 128 * 8 * 512 + 4096 * 4096
+    d = _lib.GemmDesc(256, 96, 8, 1, 0, 0, 0, tiled, 0, 0, 0, 2)  # K pads to 256
+    assert lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(d)) == 4 * 512 + 4 * 16384
+    d = _lib.GemmDesc(256, 640, 8, 1, 0, 0, 0, in_place, 0, 0, 0, 4)  # K pads to 1024
+    assert lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(d)) == 8 * 2 * 512
+    for fold in (3, 8, -1):
+        d = _lib.GemmDesc(256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 0, fold)
+        assert lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(d)) == 0
+
+
 def _create(lib, desc, w=0x1000, ws=0x2000, mb=0x3000, st=0x4000, work=0x5000, nbytes=1 << 30):
     out = ctypes.c_void_p()
     status = lib.mxfp8_publish_gemm_create(ctypes.byref(desc), ctypes.c_void_p(w),
@@ -87,6 +104,11 @@ def _create(lib, desc, w=0x1000, ws=0x2000, mb=0x3000, st=0x4000, work=0x5000, n
     ((256, 256, 8, 1, 0, 0, 0, 0, -2), _lib.ERR_UNSUPPORTED, "l2_prefetch"),
     ((256, 256, 8, 1, 0, 0, 0, 0, 0, 3), _lib.ERR_UNSUPPORTED, "pipes"),
     ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 3), _lib.ERR_UNSUPPORTED, "tmem_load"),
+    ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 0, 3), _lib.ERR_UNSUPPORTED, "fold"),
+    ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 0, 8), _lib.ERR_UNSUPPORTED, "fold"),
+    ((256, 2048, 8, 8, 0, 0, 0, 0, 0, 0, 0, 2), _lib.ERR_UNSUPPORTED, "split_k 1, 2 or 4"),
+    ((256, 256, 8, 1, 0, 0, 1, 0, 0, 0, 0, 2), _lib.ERR_UNSUPPORTED, "acc_blocks 4"),
+    ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 2, 4), _lib.ERR_UNSUPPORTED, "32x32b"),
 ])
 def test_create_rejects_bad_descriptors(lib, desc, expect, needle):
     status, out, msg = _create(lib, _lib.GemmDesc(*desc))

@@ -1,11 +1,12 @@
 """Seeded random combinations of shape and tactic -- N, ragged K, m, split-K
 S, ring depth, pipes, accumulation granularity, weight layout, TMEM read-out,
-L2 prefetch, mailbox capacity -- each run through GEMM and consumer on
+L2 prefetch, fold, mailbox capacity -- each run through GEMM and consumer on
 integer-valued inputs and checked bit-exactly against the oracle: C, the
 published mailbox words between the two kernels, the consumer's output, the
 state words and the reset mailbox.  Combinations the library refuses (a ring
-that does not fit, pipes that do not divide it) must be refused on the host
-with MXFP8_ERR_UNSUPPORTED."""
+that does not fit, pipes that do not divide it, a fold with S = 8, one slot
+per MMA or the 16x256b read-out) must be refused on the host with
+MXFP8_ERR_UNSUPPORTED."""
 import numpy as np
 import pytest
 import torch
@@ -32,13 +33,14 @@ def draw(rng):
         tmem_load=int(rng.choice([0, 1, 2])),
         l2_prefetch=int(rng.choice([-1, 0, 3])),
         capacity=int(rng.integers(m, 9)),
+        fold=int(rng.choice([0, 0, 1, 2, 4])),
     )
 
 
 def test_random_shapes_and_tactics(cuda):
     rng = np.random.default_rng(20261202)
     ran = refused = 0
-    for case in range(48):
+    for case in range(64):
         p = draw(rng)
         n, k, m, cap = p["n"], p["k"], p["m"], p["capacity"]
         w, ws, x, xs = synthetic.integer_operands(n, k, m, seed=case)
@@ -47,7 +49,7 @@ def test_random_shapes_and_tactics(cuda):
             g = PublishGemm(dev(w), dev(ws), mb, split_k=p["split_k"], stages=p["stages"],
                             acc_blocks=p["acc_blocks"], w_layout=p["w_layout"],
                             l2_prefetch=p["l2_prefetch"], pipes=p["pipes"],
-                            tmem_load=p["tmem_load"])
+                            tmem_load=p["tmem_load"], fold=p["fold"])
         except Mxfp8Error as e:
             assert "ERR_UNSUPPORTED" in str(e), (p, str(e))
             refused += 1
@@ -72,4 +74,4 @@ def test_random_shapes_and_tactics(cuda):
         assert mb.status()[0] == OK
         g.close()
         ran += 1
-    assert ran >= 30 and ran + refused == 48, (ran, refused)
+    assert ran >= 30 and ran + refused == 64, (ran, refused)

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 
 
 def run_chain(w, ws, x, xs, split_k, capacity=8, stages=0, mailbox=None, acc_blocks=0,
-              w_layout=0):
+              w_layout=0, fold=0):
     """GEMM (C requested) -> snapshot of mailbox + state -> consume.  Returns
     (C bits, mailbox words between the two kernels, state then, out bits,
     mailbox words after, state after, handle config)."""
@@ -27,7 +27,7 @@ def run_chain(w, ws, x, xs, split_k, capacity=8, stages=0, mailbox=None, acc_blo
     m = x.shape[0]
     mb = mailbox or Mailbox(capacity, n)
     g = PublishGemm(dev(w), dev(ws), mb, split_k=split_k, stages=stages, acc_blocks=acc_blocks,
-                    w_layout=w_layout)
+                    w_layout=w_layout, fold=fold)
     c = torch.full((m, n), 0x7FFF, dtype=torch.int16, device="cuda")
     g.run(dev(x), dev(xs), c)
     torch.cuda.synchronize()
@@ -54,15 +54,21 @@ def check_published(between, state_between, c_bits, capacity, n, generation=0):
     del lo, hi
 
 
+@pytest.mark.parametrize("fold", [1, 2, 4])
 @pytest.mark.parametrize("w_layout", [W_IN_PLACE, W_TILED])
 @pytest.mark.parametrize("split_k", [1, 2, 4])
 @pytest.mark.parametrize("n,k,m", [(128, 128, 1), (384, 1024, 8), (256, 2048, 5), (512, 4096, 3),
                                    (128, 96, 2), (256, 160, 7), (128, 32, 8), (256, 1152, 4)])
-def test_integer_inputs_bit_exact(cuda, n, k, m, split_k, w_layout):
+def test_integer_inputs_bit_exact(cuda, n, k, m, split_k, w_layout, fold):
+    """Every shape, split and W layout unfolded and folded (a CTA holding
+    128/fold columns in fold K pieces; K padded to whole pieces, splits with
+    no K tile contributing zeros)."""
     w, ws, x, xs = synthetic.integer_operands(n, k, m, seed=n + k + m)
     want = oracle.gemm_bf16(w, ws, x, xs)
-    c, between, sb, out, after, state, cfg = run_chain(w, ws, x, xs, split_k, w_layout=w_layout)
-    assert cfg["split_k"] == split_k
+    c, between, sb, out, after, state, cfg = run_chain(w, ws, x, xs, split_k, w_layout=w_layout,
+                                                      fold=fold)
+    assert cfg["split_k"] == split_k and cfg["fold"] == fold
+    assert cfg["grid_ctas"] == n // (128 // fold) * split_k
     assert cfg["w_layout"] == {W_IN_PLACE: "in_place", W_TILED: "tiled"}[w_layout]
     assert (c == want).all(), f"{int((c != want).sum())} of {c.size} differ"
     check_published(between, sb, c, 8, n)
@@ -71,57 +77,69 @@ def test_integer_inputs_bit_exact(cuda, n, k, m, split_k, w_layout):
     assert state == [1, 0, 0, 0]
 
 
+@pytest.mark.parametrize("fold", [1, 2, 4])
 @pytest.mark.parametrize("w_layout", [W_IN_PLACE, W_TILED])
 @pytest.mark.parametrize("split_k", [1, 2, 4])
 @pytest.mark.parametrize("n,k,m,lo,hi", [(256, 256, 1, -3, 3), (1024, 4096, 8, -4, 2),
                                          (640, 2048, 6, -6, 3), (384, 8192, 4, -4, 2),
                                          (256, 1056, 3, -4, 2)])
-def test_normal_inputs_within_two_ulps(cuda, n, k, m, lo, hi, split_k, w_layout):
+def test_normal_inputs_within_two_ulps(cuda, n, k, m, lo, hi, split_k, w_layout, fold):
     wl = synthetic.Workload("p", n, k, m, split_k, exp_lo=lo, exp_hi=hi, x_zero_fraction=0.01,
                             seed=7 * n + k + m)
     w, ws = synthetic.make_weights(wl)
     x, xs = synthetic.make_activations(wl)
     want = oracle.gemm_bf16(w, ws, x, xs)
-    c, between, sb, out, after, state, _ = run_chain(w, ws, x, xs, split_k, w_layout=w_layout)
-    assert_bf16_close(c, want, f"N={n} K={k} m={m} S={split_k}")
+    c, between, sb, out, after, state, cfg = run_chain(w, ws, x, xs, split_k, w_layout=w_layout,
+                                                      fold=fold)
+    assert cfg["fold"] == fold
+    assert_bf16_close(c, want, f"N={n} K={k} m={m} S={split_k} fold={fold}")
     check_published(between, sb, c, 8, n)
     assert (out == sanitized(c)).all()
     assert (after == oracle.SENTINEL).all()
 
 
 def test_split_k_results_agree(cuda):
+    """Every split and fold: within tolerance of the oracle on N(0, 1)
+    inputs, identical bits on integer inputs."""
     wl = synthetic.Workload("s", 512, 4096, 8, exp_lo=-4, exp_hi=2, seed=3)
     w, ws = synthetic.make_weights(wl)
     x, xs = synthetic.make_activations(wl)
     want = oracle.gemm_bf16(w, ws, x, xs)
-    results = [run_chain(w, ws, x, xs, s)[0] for s in (1, 2, 4)]
+    tactics = [(s, f) for s in (1, 2, 4) for f in (1, 2, 4)]
+    results = [run_chain(w, ws, x, xs, s, fold=f)[0] for s, f in tactics]
     for r in results:
         assert_bf16_close(r, want)
     wi, wsi, xi, xsi = synthetic.integer_operands(512, 4096, 8, seed=4)
-    ints = [run_chain(wi, wsi, xi, xsi, s)[0] for s in (1, 2, 4)]
-    assert (ints[0] == ints[1]).all() and (ints[0] == ints[2]).all()
+    ints = [run_chain(wi, wsi, xi, xsi, s, fold=f)[0] for s, f in tactics]
+    assert all((i == ints[0]).all() for i in ints)
 
 
+@pytest.mark.parametrize("fold", [1, 4])
 @pytest.mark.parametrize("stages", [2, 3, 7, 12])
-def test_every_ring_depth(cuda, stages):
+def test_every_ring_depth(cuda, stages, fold):
     w, ws, x, xs = synthetic.integer_operands(256, 4096, 8, seed=stages)
     want = oracle.gemm_bf16(w, ws, x, xs)
-    c, *_, cfg = run_chain(w, ws, x, xs, 1, stages=stages)
-    assert cfg["stages"] == stages
+    if stages * (16 + fold + 0.5) * 1024 > 227 * 1024:  # W, x and scale rings alone
+        with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED"):
+            run_chain(w, ws, x, xs, 1, stages=stages, fold=fold)
+        return
+    c, *_, cfg = run_chain(w, ws, x, xs, 1, stages=stages, fold=fold)
+    assert cfg["stages"] == stages and cfg["fold"] == fold
     assert (c == want).all()
 
 
+@pytest.mark.parametrize("fold", [1, 4])
 @pytest.mark.parametrize("stages", [2, 4, 5, 7, 10])
-def test_short_rings_over_a_long_k_loop(cuda, stages):
-    """128 K tiles per CTA through a short ring, ten chained calls, with the
-    default pipes for the ring (4, 2 or 1: each slot owned by one producer
-    lane and one MMA issuer); every call bit-exact."""
+def test_short_rings_over_a_long_k_loop(cuda, stages, fold):
+    """128 K tiles per CTA (32 folded stages) through a short ring, ten
+    chained calls, with the default pipes for the ring (4, 2 or 1: each slot
+    owned by one producer lane and one MMA issuer); every call bit-exact."""
     n, k = 1024, 16384
     w, ws, x, xs = synthetic.integer_operands(n, k, 8, seed=100 + stages)
     want = oracle.gemm_bf16(w, ws, x, xs)
     mb = Mailbox(8, n)
-    g = PublishGemm(dev(w), dev(ws), mb, split_k=1, stages=stages)
-    assert g.config()["stages"] == stages
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=1, stages=stages, fold=fold)
+    assert (g.config()["stages"], g.config()["fold"]) == (stages, fold)
     X, XS = dev(x), dev(xs)
     for call in range(10):
         c = torch.full((8, n), 0x7FFF, dtype=torch.int16, device="cuda")
@@ -147,16 +165,41 @@ def test_default_pipes_divide_the_ring(cuda):
         g.close()
 
 
+def test_default_fold(cuda):
+    """The largest fold that keeps the grid within one CTA per SM, pads K no
+    further and leaves every split a stage; 1 where the tactic asks for what
+    folding does not take (one slot per MMA, the 16x256b read-out, S = 8)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert sms >= 128
+    for n, k, split, extra, fold in [(4096, 4096, 1, {}, 4), (2048, 16384, 1, {}, 4),
+                                     (2048, 2048, 4, {}, 2), (7168, 8192, 2, {}, 1),
+                                     (7168, 16384, 4, {}, 1), (4096, 4096, 1, {"acc_blocks": 1}, 1),
+                                     (4096, 4096, 1, {"tmem_load": TMEM_LOAD_16X256B}, 1),
+                                     (256, 2048, 8, {}, 1), (256, 96, 1, {}, 1), (256, 384, 1, {}, 1),
+                                     (256, 512, 1, {}, 4), (256, 512, 2, {}, 2), (256, 256, 2, {}, 1),
+                                     (256, 256, 4, {}, 1)]:
+        w = torch.zeros((n, k), dtype=torch.uint8, device="cuda")
+        ws = torch.full((n, k // 32), 127, dtype=torch.uint8, device="cuda")
+        g = PublishGemm(w, ws, Mailbox(8, n), split_k=split, **extra)
+        cfg = g.config()
+        assert cfg["fold"] == fold, (n, k, split, extra, cfg)
+        assert cfg["grid_ctas"] == n // (128 // fold) * split, cfg
+        assert cfg["tmem_columns"] <= 256, cfg
+        g.close()
+
+
+@pytest.mark.parametrize("fold", [1, 2, 4])
 @pytest.mark.parametrize("stages,pipes", [(8, 4), (4, 4), (8, 2), (6, 2), (5, 1), (8, 1)])
-def test_every_pipe_count_over_a_long_k_loop(cuda, stages, pipes):
+def test_every_pipe_count_over_a_long_k_loop(cuda, stages, pipes, fold):
     """Each pipe count (producer lanes = MMA-issuing warps) on a ring it
-    divides, 128 K tiles per CTA, five chained calls, bit-exact."""
+    divides, 128 K tiles per CTA (128 / fold stages), five chained calls,
+    bit-exact."""
     n, k = 1024, 16384
     w, ws, x, xs = synthetic.integer_operands(n, k, 8, seed=200 + stages * 8 + pipes)
     want = oracle.gemm_bf16(w, ws, x, xs)
     mb = Mailbox(8, n)
-    g = PublishGemm(dev(w), dev(ws), mb, split_k=1, stages=stages, pipes=pipes)
-    assert (g.config()["stages"], g.config()["pipes"]) == (stages, pipes)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=1, stages=stages, pipes=pipes, fold=fold)
+    assert (g.config()["stages"], g.config()["pipes"], g.config()["fold"]) == (stages, pipes, fold)
     X, XS = dev(x), dev(xs)
     for call in range(5):
         c = torch.full((8, n), 0x7FFF, dtype=torch.int16, device="cuda")
@@ -169,9 +212,10 @@ def test_every_pipe_count_over_a_long_k_loop(cuda, stages, pipes):
     g.close()
 
 
+@pytest.mark.parametrize("fold", [1, 4])
 @pytest.mark.parametrize("w_layout", [W_IN_PLACE, W_TILED])
 @pytest.mark.parametrize("l2_prefetch", [-1, 0, 3, 40])
-def test_l2_prefetch_leaves_results_unchanged(cuda, l2_prefetch, w_layout):
+def test_l2_prefetch_leaves_results_unchanged(cuda, l2_prefetch, w_layout, fold):
     """Warming later W stages in L2 before the grid wait (the default, 6
     stages; none; a few; more than the CTA has) is bit-exact."""
     n, k = 512, 8192
@@ -180,8 +224,9 @@ def test_l2_prefetch_leaves_results_unchanged(cuda, l2_prefetch, w_layout):
     for split in (1, 4):
         mb = Mailbox(8, n)
         g = PublishGemm(dev(w), dev(ws), mb, split_k=split, w_layout=w_layout,
-                        l2_prefetch=l2_prefetch)
-        grid_ctas = n // 128 * split
+                        l2_prefetch=l2_prefetch, fold=fold)
+        grid_ctas = n // (128 // fold) * split
+        assert g.config()["grid_ctas"] == grid_ctas
         default = 6 if grid_ctas > torch.cuda.get_device_properties(0).multi_processor_count else 10
         assert g.config()["l2_prefetch"] == (default if l2_prefetch == 0 else l2_prefetch)
         c = torch.full((8, n), 0x7FFF, dtype=torch.int16, device="cuda")
@@ -237,7 +282,7 @@ def test_tmem_load_shapes_give_identical_bits(cuda, split_k, acc_blocks):
         for load in (TMEM_LOAD_32X32B, TMEM_LOAD_16X256B):
             mb = Mailbox(8, 768)
             g = PublishGemm(dev(ww), dev(wws), mb, split_k=split_k, acc_blocks=acc_blocks,
-                            tmem_load=load)
+                            tmem_load=load, fold=1)
             assert g.config()["tmem_load"] == {1: "32x32b", 2: "16x256b"}[load]
             m = xx.shape[0]
             c = torch.full((m, 768), 0x7FFF, dtype=torch.int16, device="cuda")
@@ -264,15 +309,16 @@ def test_pipes_that_do_not_divide_the_ring_are_refused(cuda):
         PublishGemm(dev(w), dev(ws), Mailbox(8, 256), split_k=1, stages=6, pipes=4)
 
 
+@pytest.mark.parametrize("fold", [1, 4])
 @pytest.mark.parametrize("split_k", [1, 2, 4])
-def test_longest_k(cuda, split_k):
+def test_longest_k(cuda, split_k, fold):
     """K = 32768, the largest K taken: 256 K tiles per CTA at S = 1 (the most a
-    split holds), every output bit-exact (integer inputs keep every partial sum
-    below 2^24)."""
+    split holds; 64 stages of 4 pieces folded), every output bit-exact
+    (integer inputs keep every partial sum below 2^24)."""
     n, k, m = 256, 32768, 8
     w, ws, x, xs = synthetic.integer_operands(n, k, m, seed=77 + split_k)
-    c, between, sb, out, after, state, cfg = run_chain(w, ws, x, xs, split_k)
-    assert cfg["split_k"] == split_k
+    c, between, sb, out, after, state, cfg = run_chain(w, ws, x, xs, split_k, fold=fold)
+    assert cfg["split_k"] == split_k and cfg["fold"] == fold
     want = oracle.gemm_bf16(w, ws, x, xs)
     assert (c == want).all() and (out == sanitized(want)).all()
     check_published(between, sb, c, 8, n)
@@ -303,9 +349,10 @@ def test_grid_of_two_waves(cuda):
     g.close()
 
 
+@pytest.mark.parametrize("fold", [1, 2, 4])
 @pytest.mark.parametrize("shift", [100, -100, 60])
 @pytest.mark.parametrize("split_k", [1, 4])
-def test_scale_exponents_near_the_e8m0_limits(cuda, shift, split_k):
+def test_scale_exponents_near_the_e8m0_limits(cuda, shift, split_k, fold):
     """W's scales moved up by `shift` powers of two and x's down by as many
     (E8M0 codes from 27 to 228): every product, hence every output, is
     unchanged, and exact; the scale plumbing must carry the extreme codes."""
@@ -315,7 +362,8 @@ def test_scale_exponents_near_the_e8m0_limits(cuda, shift, split_k):
     ws_s = (ws.astype(np.int32) + shift).astype(np.uint8)
     xs_s = (xs.astype(np.int32) - shift).astype(np.uint8)
     assert (oracle.gemm_bf16(w, ws_s, x, xs_s) == want).all()
-    c, between, sb, out, after, state, cfg = run_chain(w, ws_s, x, xs_s, split_k)
+    c, between, sb, out, after, state, cfg = run_chain(w, ws_s, x, xs_s, split_k, fold=fold)
+    assert cfg["fold"] == fold
     assert (c == want).all() and (out == sanitized(want)).all()
 
 
