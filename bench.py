@@ -41,7 +41,8 @@ GRAPH_STEPS = 30  # calls per captured graph (a multiple of every weight-copy co
 E2E_GRAPH_STEPS = 480  # end-to-end steps per captured graph (likewise)
 E2E_BATCH = 30         # end-to-end steps per wait on the input copies (divides E2E_GRAPH_STEPS)
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ("mxfp8_gemm_mailbox_gb300/csrc/publish_gemm.cu",
+KERNEL_SOURCES = ("mxfp8_gemm_mailbox_gb300/csrc/publish_gemm_kernel.cuh",
+                  "mxfp8_gemm_mailbox_gb300/csrc/publish_gemm.cu",
                   "mxfp8_gemm_mailbox_gb300/csrc/ptx.cuh")
 TRAFFIC_FILE = ROOT / "profiles" / "publish_gemm_headline_traffic.json"
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -514,7 +515,7 @@ def run_ours(args):
             },
             "roofline": {
                 "bound": "hbm",
-                "kernel": f"publish_gemm_kernel<{wl.split_k}, 0>",
+                "kernel": f"publish_gemm_kernel<{wl.split_k}, 0, {cfg['fold']}>",
                 "achieved": round(achieved, 1),
                 "peak": peak,
                 "peak_kind": peak_kind,
@@ -541,7 +542,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": int(out.numel() * out.element_size()),
             },
             "gpu_launches": 2 * steps,
-            "tactic": {k: cfg[k] for k in ("split_k", "stages", "acc_blocks", "w_layout",
+            "tactic": {k: cfg[k] for k in ("split_k", "fold", "stages", "acc_blocks", "w_layout",
                                             "l2_prefetch", "pipes", "tmem_columns")},
             "clocks": clocks.summary(),
         }
@@ -769,8 +770,8 @@ def run_sweep(args):
                     gbs = weight_bytes / (us * 1e-6) / 1e9
                     rows.append({"m": m, "n": n, "k": k, "split_k": s, "us_per_call": round(us, 3),
                                  "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
-                                 "stages": cfg["stages"], "grid_ctas": cfg["grid_ctas"],
-                                 "copies": copies})
+                                 "stages": cfg["stages"], "fold": cfg["fold"],
+                                 "grid_ctas": cfg["grid_ctas"], "copies": copies})
                     del graph
                 for g in gemms:
                     g.close()

@@ -406,8 +406,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const int etid = tid - 64;               // 0..127
     const int quarter = warp & 3;            // the 32 TMEM lanes this warp reaches
     const int arow = quarter * 32 + lane;    // MMA row = TMEM lane
-    const int piece = arow / kTileRows;      // the K piece this lane holds
-    const int col = arow % kTileRows;        // output column within the tile
+    const int piece = F == 1 ? 0 : arow / kTileRows;     // the K piece this lane holds
+    const int col = F == 1 ? arow : arow % kTileRows;    // output column within the tile
     // The lane's diagonal block: columns [8 piece, 8 piece + 8) of a slot.
     const uint32_t lane_base =
         (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(kRows * piece);
@@ -432,10 +432,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       if (w >= words) break;
       const int r = w / nkt;
       const int j = w - r * nkt;
-      const int t = r % kRows;
+      const int t = F == 1 ? r : r % kRows;
       uint32_t v = 0x7F7F7F7Fu;
       if (t < p.m) {
-        const int kb0 = ((kt_begin + j) * F + r / kRows) * kSfPerTile;
+        const int kb0 = ((kt_begin + j) * F + (F == 1 ? 0 : r / kRows)) * kSfPerTile;
         const uint8_t* row = p.x_scale + static_cast<size_t>(t) * kblocks;
         uint32_t b[kSfPerTile];
 #pragma unroll
