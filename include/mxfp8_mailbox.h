@@ -118,9 +118,10 @@ typedef struct mxfp8_gemm_desc {
 
 /* Where the GEMM streams W from.  IN_PLACE: the caller's [N][K] buffer,
  * through 2-D TMA tiles (the handle borrows w).  TILED: a copy made once at
- * create inside the workspace, laid out tile by tile (128 rows x 128 K bytes,
- * already in the order shared memory holds it) so every pipeline stage is one
- * contiguous 16 KB read; the caller's w is not read after create. */
+ * create inside the workspace, laid out stage by stage (128 rows x 128 K
+ * bytes; 128/fold rows x fold K pieces when folded), already in the order
+ * shared memory holds it, so every pipeline stage is one contiguous 16 KB
+ * read; the caller's w is not read after create. */
 #define MXFP8_W_IN_PLACE 1
 #define MXFP8_W_TILED 2
 
@@ -152,8 +153,11 @@ mxfp8_status mxfp8_mailbox_init(void* mailbox, int32_t* stage_state, int32_t cap
 /* Device bytes the handle needs: W's scale factors re-laid once at create
  * into the tiled order the tensor-core copy reads (N/128 x ceil(K/128) chunks
  * of 512 bytes), plus, for MXFP8_W_TILED (and for w_layout 0, which chooses
- * it), the tiled copy of W (N x ceil(K/128) x 128 bytes).  0 for an invalid
- * descriptor. */
+ * it), the tiled copy of W (N x ceil(K/128) x 128 bytes).  With an explicit
+ * fold f, K rounds up to a multiple of 128 f instead (N/(128/f) x
+ * ceil(K/(128 f)) chunks; N x ceil(K/(128 f)) x 128 f bytes of W); fold 0
+ * sizes like 1, as it only chooses folds that pad K no further.  0 for an
+ * invalid descriptor. */
 size_t mxfp8_publish_gemm_workspace_bytes(const mxfp8_gemm_desc* desc);
 
 /* Build a publishing GEMM for one weight and one mailbox (publishing_gemm
