@@ -379,7 +379,7 @@ def test_accumulation_granularity(cuda, acc_blocks, split_k):
     w, ws, x, xs = synthetic.integer_operands(512, 4096, 8, seed=17)
     want = oracle.gemm_bf16(w, ws, x, xs)
     c, between, sb, out, after, state, cfg = run_chain(w, ws, x, xs, split_k,
-                                                      acc_blocks=acc_blocks)
+                                                      acc_blocks=acc_blocks, fold=1)
     assert cfg["acc_blocks"] == acc_blocks
     assert (c == want).all()
     check_published(between, sb, c, 8, 512)
@@ -405,10 +405,11 @@ def test_negative_zero_is_cleared_in_the_mailbox_only(cuda):
     assert not (out == 0x8000).any()
 
 
-def test_capacity_and_row_limits(cuda):
+@pytest.mark.parametrize("fold", [1, 2])
+def test_capacity_and_row_limits(cuda, fold):
     w, ws, x, xs = synthetic.integer_operands(128, 256, 3, seed=1)
     mb = Mailbox(3, 128)
-    g = PublishGemm(dev(w), dev(ws), mb, split_k=1)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=1, fold=fold)
     g.precompile(3)
     with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED"):
         g.precompile(4)
@@ -424,16 +425,19 @@ def test_capacity_and_row_limits(cuda):
     assert mb.status()[0] == OK
 
 
-def test_fused_equals_unfused_bit_for_bit(cuda):
+@pytest.mark.parametrize("fold", [1, 0])
+def test_fused_equals_unfused_bit_for_bit(cuda, fold):
     # The unfused path: the GEMM writes only C, the standalone publish kernel
-    # reads it back; mailbox and consumer output must match the fused epilogue.
+    # reads it back; mailbox and consumer output must match the fused epilogue
+    # (unfolded, and with the default fold, 4 here).
     wl = synthetic.Workload("u", 1024, 2048, 7, 2, exp_lo=-6, exp_hi=3, signed_pairs=True, seed=11)
     w, ws = synthetic.make_weights(wl)
     x, xs = synthetic.make_activations(wl)
     W, WS, X, XS = dev(w), dev(ws), dev(x), dev(xs)
     fused_mb, unfused_mb = Mailbox(8, 1024), Mailbox(8, 1024)
-    gf = PublishGemm(W, WS, fused_mb, split_k=2)
-    gu = PublishGemm(W, WS, unfused_mb, split_k=2)
+    gf = PublishGemm(W, WS, fused_mb, split_k=2, fold=fold)
+    gu = PublishGemm(W, WS, unfused_mb, split_k=2, fold=fold)
+    assert gf.config()["fold"] == gu.config()["fold"] == (fold or 4)
     for call in range(4):  # walk the generations
         cf = torch.empty((7, 1024), dtype=torch.int16, device="cuda")
         cu = torch.empty((7, 1024), dtype=torch.int16, device="cuda")
@@ -452,20 +456,22 @@ def test_fused_equals_unfused_bit_for_bit(cuda):
     assert_bf16_close(bits(cf), oracle.gemm_bf16(w, ws, x, xs))
 
 
-def test_publish_without_c(cuda):
+@pytest.mark.parametrize("fold", [1, 2])
+def test_publish_without_c(cuda, fold):
     w, ws, x, xs = synthetic.integer_operands(256, 512, 8, seed=2)
     mb = Mailbox(8, 256)
-    g = PublishGemm(dev(w), dev(ws), mb, split_k=2)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=2, fold=fold)
     g.run(dev(x), dev(xs), None)
     out = mb.consume(8)
     torch.cuda.synchronize()
     assert (bits(out) == sanitized(oracle.gemm_bf16(w, ws, x, xs))).all()
 
 
-def test_bad_next_generation_is_flagged(cuda):
+@pytest.mark.parametrize("fold", [1, 2])
+def test_bad_next_generation_is_flagged(cuda, fold):
     w, ws, x, xs = synthetic.integer_operands(128, 256, 2, seed=5)
     mb = Mailbox(8, 128)
-    g = PublishGemm(dev(w), dev(ws), mb, split_k=1)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=1, fold=fold)
     mb.state[0] = 4
     c = torch.empty((2, 128), dtype=torch.int16, device="cuda")
     g.run(dev(x), dev(xs), c)
@@ -475,14 +481,15 @@ def test_bad_next_generation_is_flagged(cuda):
     assert mb.status()[0] == ERR_STATE
 
 
+@pytest.mark.parametrize("fold", [1, 0])
 @pytest.mark.parametrize("alpha,split_k", [(0.25, 1), (-1.7, 2), (3.0e-3, 4), (1.0, 4)])
-def test_global_scale(cuda, alpha, split_k):
+def test_global_scale(cuda, alpha, split_k, fold):
     wl = synthetic.Workload("alpha", 768, 4096, 6, split_k, exp_lo=-4, exp_hi=2, seed=91)
     w, ws = synthetic.make_weights(wl)
     x, xs = synthetic.make_activations(wl)
     want = oracle.gemm_bf16_scaled(w, ws, x, xs, alpha)
     mb = Mailbox(8, 768)
-    g = PublishGemm(dev(w), dev(ws), mb, split_k=split_k)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=split_k, fold=fold)
     a = torch.tensor([alpha], dtype=torch.float32, device="cuda")
     c = torch.empty((6, 768), dtype=torch.bfloat16, device="cuda")
     g.run_scaled(dev(x), dev(xs), a, c)
@@ -492,7 +499,7 @@ def test_global_scale(cuda, alpha, split_k):
     assert (bits(out) == sanitized(bits(c))).all()
     # integer inputs with a power-of-two scale stay exact
     wi, wsi, xi, xsi = synthetic.integer_operands(768, 4096, 6, seed=3)
-    g2 = PublishGemm(dev(wi), dev(wsi), Mailbox(8, 768), split_k=split_k)
+    g2 = PublishGemm(dev(wi), dev(wsi), Mailbox(8, 768), split_k=split_k, fold=fold)
     a2 = torch.tensor([0.5], dtype=torch.float32, device="cuda")
     g2.run_scaled(dev(xi), dev(xsi), a2, c)
     g2.mailbox.consume(6)

@@ -31,15 +31,17 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(None)
 
 
-def test_noalloc_matches_the_handle_path_on_two_calls(cuda):
+@pytest.mark.parametrize("fold", [1, 0])
+def test_noalloc_matches_the_handle_path_on_two_calls(cuda, fold):
     lib = _lib.load()
     n, k, m, split = 1024, 4096, 5, 2
     wl = synthetic.Workload("noalloc", n, k, m, split, exp_lo=-4, exp_hi=2, seed=4242)
     w, ws = synthetic.make_weights(wl)
     W, WS = dev(w), dev(ws)
     handle_mb, noalloc_mb = Mailbox(8, n), Mailbox(8, n)
-    gemm = PublishGemm(W, WS, handle_mb, split_k=split, w_layout=_lib.W_IN_PLACE)
-    desc = _lib.GemmDesc(n, k, 8, split, 0, 0, 0, 0, 0)
+    gemm = PublishGemm(W, WS, handle_mb, split_k=split, w_layout=_lib.W_IN_PLACE, fold=fold)
+    assert gemm.config()["fold"] == (fold or 4)  # 8 tiles x 2 splits fold 4 ways by default
+    desc = _lib.GemmDesc(n, k, 8, split, 0, 0, 0, 0, 0, 0, 0, fold)
     for call in range(2):
         x, xs = synthetic.make_activations(wl, salt=call)
         X, XS = dev(x), dev(xs)
