@@ -59,9 +59,13 @@ constexpr uint64_t kGemmWaitLimitNs = 2000000000ull;
 // the smaller grids).
 constexpr int kDefaultL2Prefetch = 6;
 constexpr int kDefaultL2PrefetchOnePerSm = 10;
-// Tensor-memory columns a CTA may allocate: half of an SM's 512, so that two
-// CTAs sharing an SM never wait on each other's allocation (two CTAs of one
-// cluster on one SM would otherwise wait for ever).
+// Tensor-memory columns a CTA may allocate: half of an SM's 512, so two CTAs
+// on an SM never wait for each other's allocation.  A third may wait until one
+// of them exits: harmless unless they wait for it, which split-K clusters do
+// (at their cluster barriers), hence the shared-memory floor of
+// at_most_two_per_sm for clustered launches.  A CTA of a later programmatic
+// grid never holds columns an earlier one waits for: each CTA allocates before
+// it lets its dependents launch.
 constexpr uint32_t kMaxTmemCols = 256;
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -174,6 +178,16 @@ mxfp8_status device_limits(int device, DeviceLimits* out) {
                                   device)) != cudaSuccess)
     return cuda_fail(e, "cudaDeviceGetAttribute(shared memory per SM)");
   return MXFP8_OK;
+}
+
+// A clustered launch (split_k > 1) asks for at least a third of an SM's shared
+// memory, so at most two of its CTAs share an SM and none waits in tcgen05.alloc
+// for columns held by a cluster peer that waits for it.  (Unclustered short
+// rings stay small: the padding costs latency-bound shapes about 0.35 us.)
+GemmSmemLayout at_most_two_per_sm(GemmSmemLayout layout, int split_k, const DeviceLimits& lim) {
+  if (split_k > 1)
+    layout.total = std::max(layout.total, static_cast<uint32_t>(lim.smem_per_sm / 3));
+  return layout;
 }
 
 // Fill split_k, cta_k, stages, pipes and fold: split_k so the grid has about
@@ -388,7 +402,9 @@ mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* 
   g->k_tiles = k_tiles_for_fold(desc->k, fold);
   g->tiles_per_split = (g->k_tiles + g->desc.split_k - 1) / g->desc.split_k;
   g->tmem = gemm_tmem_plan(g->desc.stages, g->desc.acc_blocks, fold);
-  g->layout = gemm_smem_layout(g->desc.stages, g->desc.split_k, g->tiles_per_split, fold);
+  g->layout = at_most_two_per_sm(
+      gemm_smem_layout(g->desc.stages, g->desc.split_k, g->tiles_per_split, fold),
+      g->desc.split_k, lim);
   g->x_cached = nullptr;
   g->m_cached = 0;
   st = encode_rows(&g->tmap_w, w, static_cast<uint64_t>(desc->k), static_cast<uint64_t>(desc->n),
@@ -695,7 +711,8 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
   p.mailbox = static_cast<uint16_t*>(mailbox);
   p.state = stage_state;
   p.wait_limit_ns = kGemmWaitLimitNs;
-  p.smem = gemm_smem_layout(d.stages, d.split_k, tiles_per_split, d.fold);
+  p.smem = at_most_two_per_sm(gemm_smem_layout(d.stages, d.split_k, tiles_per_split, d.fold),
+                              d.split_k, lim);
   e = set_gemm_smem_attribute(d.split_k, d.fold, static_cast<int>(p.smem.total));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);

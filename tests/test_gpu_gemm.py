@@ -188,6 +188,25 @@ def test_default_fold(cuda):
         g.close()
 
 
+def test_at_most_two_ctas_per_sm(cuda):
+    """A clustered launch asks for more than a third of an SM's shared memory,
+    short rings included, so at most two of its CTAs (each holding at most 256
+    of the SM's 512 tensor-memory columns) share an SM and no allocation waits
+    on a cluster peer; every launch holds at most 256 columns."""
+    props = torch.cuda.get_device_properties(0)
+    per_sm = getattr(props, "shared_memory_per_multiprocessor", 233472)
+    for n, k, split, stages in [(128, 128, 4, 0), (256, 256, 1, 0), (128, 32, 8, 2),
+                                (256, 512, 2, 2), (1024, 4096, 4, 2), (7168, 16384, 4, 0)]:
+        w = torch.zeros((n, k), dtype=torch.uint8, device="cuda")
+        ws = torch.full((n, k // 32), 127, dtype=torch.uint8, device="cuda")
+        g = PublishGemm(w, ws, Mailbox(8, n), split_k=split, stages=stages)
+        cfg = g.config()
+        if split > 1:
+            assert 3 * (cfg["smem_bytes"] + 1024) > per_sm, cfg  # 1 KB reserved per CTA
+        assert cfg["tmem_columns"] <= 256, cfg
+        g.close()
+
+
 @pytest.mark.parametrize("fold", [1, 2, 4])
 @pytest.mark.parametrize("stages,pipes", [(8, 4), (4, 4), (8, 2), (6, 2), (5, 1), (8, 1)])
 def test_every_pipe_count_over_a_long_k_loop(cuda, stages, pipes, fold):
