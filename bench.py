@@ -160,10 +160,20 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_lines(text: str):
+    """The lines of a C++ source with // comments and blank lines dropped, so
+    that editing a comment does not mark the kernel as changed."""
+    for line in text.splitlines():
+        code = line.split("//", 1)[0].rstrip()
+        if code:
+            yield code
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        h.update((ROOT / rel).read_bytes())
+        for line in _code_lines((ROOT / rel).read_text()):
+            h.update(line.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

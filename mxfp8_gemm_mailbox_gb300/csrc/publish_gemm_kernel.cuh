@@ -3,7 +3,8 @@
 // C[t][n] = sum_k W[n][k] x[t][k] (page "vllm.models.deepseek_v41.nvidia.
 // specialized_decode.boundary.publishing_gemm", module description "GEMM
 // structure"): the weight is the MMA's A operand (128 output columns per CTA,
-// N/128 tiles), the at most 8 activation rows its B operand (N = 8).  Each
+// N/128 tiles; 128/F when folded, below), the at most 8 activation rows its
+// B operand (N = 8).  Each
 // CTA of a split-K cluster of S multiplies one K slice; the partials are
 // exchanged through distributed shared memory and each CTA reduces 1/S of
 // the tokens.  The epilogue rounds to BF16, writes C, and publishes every
@@ -32,21 +33,23 @@
 // Warp roles (pipes = 1, 2 or 4 per launch):
 //   warp 0      TMA producer: one lane per pipe, lane l taking stages
 //               l, l + pipes, ...; per stage the W tile + W scale chunk
-//               (started before the programmatic grid wait) and the x tile.
+//               (started before the programmatic grid wait) and the F x
+//               tiles.
 //   warp 1, 6.. MMA issuers, one warp per pipe (warp 1 also allocates tensor
 //               memory): one thread each issues, per stage, tcgen05.cp of the
 //               W and x scale chunks and one block-scaled tcgen05.mma per
 //               32-wide K block.  Blocks have 160 + 32 * pipes threads.
 //   warps 2-5   epilogue: x scales staged for the copies, partial sums read
-//               back (tcgen05.ld 32x32b: thread = output column, registers =
-//               tokens) and folded into the compensated sums, split-K
-//               exchange, BF16 rounding, C store, publish.
+//               back (tcgen05.ld 32x32b: thread = MMA row, registers =
+//               tokens of its diagonal block) and folded into the compensated
+//               sums, the F pieces of a column added, split-K exchange, BF16
+//               rounding, C store, publish.
 //
 // Tensor-memory columns: [acc, +acc_ring * acc_slot) the accumulator ring (FP32,
-// lane = output column, column = block * 8 + token); then the W and x scale
-// rings, one 4-column slot per stage each, filled by tcgen05.cp (32x128b,
-// multicast to the four lane quarters) from 16-byte-row scale chunks in
-// shared memory.  Every scale address is 4-column aligned.
+// lane = MMA row, column = block * 8 F + piece * 8 + token); then the W and x
+// scale rings, one 4-column slot per stage each, filled by tcgen05.cp
+// (32x128b, multicast to the four lane quarters) from 16-byte-row scale chunks
+// in shared memory.  Every scale address is 4-column aligned.
 //
 // The kernel template lives in this header so its instantiations can be
 // spread over translation units that compile in parallel: publish_gemm.cu
