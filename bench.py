@@ -32,8 +32,13 @@ sys.path.insert(0, str(ROOT))
 
 METRIC = "us/call and weight-stream HBM GB/s (% of GB300 peak), MXFP8 GEMM m<=8"
 UNIT = "GB/s"
-WEIGHT_COPIES = 3  # the headline's rotation; other workloads take more (weight_copies())
 L2_BYTES = 129 * 2**20
+# Weight bytes the timed loops rotate through, in L2 sizes.  Three copies of
+# the N=7168, K=16384 weight (2.8 x L2) let 8-10 % of each call's weight
+# bytes come from L2 (ncu over a whole graph replay: lines the GEMM warms in
+# L2 with normal priority outlive the evict-first stream until their copy
+# comes round again); six (5.6 x L2) still 5 %; fifteen (14 x L2) none.
+ROTATION_L2_MULTIPLE = 12
 WORKLOAD_CHOICES = {"headline": "HEADLINE", "graph": "GRAPH_8192", "chain": "CHAIN_4096",
                     "tiny": "TINY"}
 _WORKLOAD = "headline"
@@ -62,6 +67,9 @@ def parse_args(argv=None):
                    help="the chain's workload: headline N=7168 K=16384 m=8 S=4 (default), "
                         "graph N=7168 K=8192 m=8 S=2, chain N=4096 K=4096 m=4 S=1, "
                         "tiny N=256 K=256 m=1 S=1")
+    p.add_argument("--profile-graph", action="store_true",
+                   help="after the timed region, replay the chain's graph once more between "
+                        "cudaProfilerStart and cudaProfilerStop (for ncu's graph profiling)")
     p.add_argument("--path", choices=("chain", "protocols", "sweep"), default="chain",
                    help="chain: the headline (default); protocols: the output hand-off "
                         "protocols on their own (sentinel mailbox, tagged pairs, all-gather); "
@@ -198,14 +206,29 @@ def workload():
 
 
 def weight_copies(weight_bytes: int) -> int:
-    """Weight copies the timed loops rotate through: enough that the copies
-    between two uses of one exceed twice the L2, and a divisor of both graph
-    lengths so every replay rotates the same way."""
-    need = max(WEIGHT_COPIES, -(-int(2.2 * L2_BYTES) // weight_bytes))
+    """Weight copies the timed loops rotate through: enough that their bytes
+    exceed ROTATION_L2_MULTIPLE x the L2, so no call finds another call's
+    weight in L2 (at most 30), and a divisor of both graph lengths so every
+    replay rotates the same way."""
+    need = max(3, -(-ROTATION_L2_MULTIPLE * L2_BYTES // weight_bytes))
     for c in (3, 5, 6, 10, 15, 30):
         if c >= need:
             return c
     return 30
+
+
+def rotation_note(copies: int, weight_bytes: int) -> str:
+    """What the rotation does to L2, for the JSON line."""
+    total = copies * weight_bytes
+    head = (f"{copies} rotating weight copies ({total >> 20} MiB, "
+            f"{total / L2_BYTES:.1f} x the 129 MB L2)")
+    if total >= ROTATION_L2_MULTIPLE * L2_BYTES:
+        return head + ": no call finds another call's weight in L2; every call reads its " \
+                      "weight from HBM"
+    if total >= 2 * L2_BYTES:
+        return head + ": weights stream from HBM, though lines warmed in L2 can outlive a " \
+                      "rotation"
+    return head + ": the weights stay in L2; a latency figure, not a bandwidth one"
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -350,6 +373,15 @@ def run_ours(args):
     barrier(group)
     torch.cuda.synchronize(device)
     local_s = e0.elapsed_time(e1) / 1e3
+    if args.profile_graph:
+        # One more replay of the timed graph between the CUDA profiler's start
+        # and stop, for `ncu --profile-from-start off --graph-profiling graph`:
+        # the DRAM bytes of GRAPH_STEPS whole chained calls.
+        torch.cuda.profiler.start()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        stream.synchronize()
+        torch.cuda.profiler.stop()
     seconds, bytes_all = aggregate(local_s, float(steps * wl.weight_bytes), group)
     us_per_call = seconds / steps * 1e6
     value = bytes_all / seconds / 1e9
@@ -515,11 +547,7 @@ def run_ours(args):
                 "stages": cfg["stages"], "grid_ctas": cfg["grid_ctas"],
                 "smem_bytes": cfg["smem_bytes"],
                 "weight_bytes_per_call": wl.weight_bytes,
-                "l2": (f"{copies} rotating weight copies ({copies * wl.weight_bytes >> 20} MiB "
-                       "> 2 x 129 MB L2): every call streams its weight from HBM"
-                       if copies * wl.weight_bytes > 2 * L2_BYTES else
-                       f"{copies} rotating weight copies ({copies * wl.weight_bytes >> 10} KiB): "
-                       "the weights stay in L2; a latency figure, not a bandwidth one"),
+                "l2": rotation_note(copies, wl.weight_bytes),
                 "timing": f"CUDA graphs of {GRAPH_STEPS} chained calls (GEMM -> PDL consumer)",
                 "parallelism": "replicas" if world > 1 else "single GPU",
             },
@@ -553,7 +581,8 @@ def run_ours(args):
             },
             "gpu_launches": 2 * steps,
             "tactic": {k: cfg[k] for k in ("split_k", "fold", "stages", "acc_blocks", "w_layout",
-                                            "l2_prefetch", "pipes", "tmem_columns")},
+                                            "l2_prefetch", "l2_prefetch_early", "pipes",
+                                            "tmem_columns")},
             "clocks": clocks.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -737,7 +766,7 @@ def run_sweep(args):
             W = torch.from_numpy(w).to(device)
             WS = torch.from_numpy(ws).to(device)
             weight_bytes = n * k + n * k // 32
-            copies = max(3, math.ceil(2.2 * L2_BYTES / weight_bytes))
+            copies = min(64, max(3, -(-ROTATION_L2_MULTIPLE * L2_BYTES // weight_bytes)))
             for s in synthetic.SWEEP_S:
                 mb = mx.Mailbox(8, n, device=device)
                 gemms = [mx.PublishGemm(W, WS, mb, split_k=s, stream=stream)
@@ -800,8 +829,9 @@ def run_sweep(args):
                 "scale exponents in [-6, 3])",
         "config": {"workload": "sweep m 1..8 x N {2048, 4096, 7168} x K {2048, 4096, 8192, "
                                "16384} x S {1, 2, 4}",
-                   "timing": "one CUDA graph of >= 30 chained calls per case, rotating weight "
-                             "copies > 2 x L2"},
+                   "timing": "one CUDA graph of >= 30 chained calls per case, rotating "
+                             f"min(64, {ROTATION_L2_MULTIPLE} x L2 / weight bytes) weight "
+                             "copies (rows give the count)"},
         "peak": peak, "peak_kind": peak_kind,
         "rows": rows,
     }

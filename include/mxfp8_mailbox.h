@@ -85,11 +85,10 @@ typedef struct mxfp8_gemm_desc {
   int32_t stages;     /* shared-memory ring depth: 2..16 (0 = choose)                */
   int32_t acc_blocks; /* K blocks per promoted partial sum: 1 or 4 (0 = 4)           */
   int32_t w_layout;   /* MXFP8_W_IN_PLACE or MXFP8_W_TILED (0 = choose)              */
-  int32_t l2_prefetch;/* W stages past the ring each CTA warms in L2 before its grid
-                         wait, so HBM keeps streaming while the previous kernel and
-                         the grid wait hold the ring: 1..64, -1 = none, 0 = choose (6
-                         with two CTAs per SM, 10 with one: the measured best on
-                         GB300, -2.6 % time per call on the N=7168, K=16384 chain)     */
+  int32_t l2_prefetch;/* W stages past the ring each of the grid's later CTAs warms in
+                         L2 before its grid wait, so HBM keeps streaming while the
+                         previous kernel finishes and the grid wait holds the ring:
+                         1..64, -1 = none, 0 = choose (16)                              */
   int32_t pipes;      /* producer lanes and MMA-issuing warps sharing the ring: 1, 2
                          or 4, dividing `stages` (stage i and its ring slots belong to
                          pipe i % pipes).  0 = choose: 4 when the grid has at most one
@@ -114,6 +113,14 @@ typedef struct mxfp8_gemm_desc {
                          that keeps the grid within one CTA per SM and >= 1 full K
                          piece per CTA (1 when those fields ask for what it cannot
                          take).                                                         */
+  int32_t l2_prefetch_early;/* W stages past the ring that each of the first 70 % of
+                         the grid's CTAs warms in L2 (l2_prefetch covers the rest).
+                         Those launch while the previous kernel still streams, and
+                         a deep prefetch would take HBM from it: 1..64, -1 = none,
+                         0 = choose (an explicit l2_prefetch's value, else 4 with
+                         two CTAs per SM and none with one; measured on GB300: the
+                         N=7168, K=16384, S=4 chain 21.44 -> 20.25 us per call
+                         against 6 stages for every CTA)                              */
 } mxfp8_gemm_desc;
 
 /* Where the GEMM streams W from.  IN_PLACE: the caller's [N][K] buffer,

@@ -84,13 +84,13 @@ class PublishGemm:
     def __init__(self, w: torch.Tensor, w_scale: torch.Tensor, mailbox: Mailbox,
                  split_k: int = 0, stages: int = 0, acc_blocks: int = 0, w_layout: int = 0,
                  l2_prefetch: int = 0, pipes: int = 0, tmem_load: int = 0, fold: int = 0,
-                 stream=None):
+                 l2_prefetch_early: int = 0, stream=None):
         lib = _lib.load()
         _bytes_tensor(w, "w")
         _bytes_tensor(w_scale, "w_scale")
         n, k = w.shape
         self.desc = GemmDesc(n, k, mailbox.capacity, split_k, 0, stages, acc_blocks, w_layout,
-                             l2_prefetch, pipes, tmem_load, fold)
+                             l2_prefetch, pipes, tmem_load, fold, l2_prefetch_early)
         ws_bytes = lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(self.desc))
         if ws_bytes == 0:
             raise ValueError(f"invalid GEMM shape N={n}, K={k}")
@@ -114,7 +114,8 @@ class PublishGemm:
         return {"n": d.n, "k": d.k, "capacity_m": d.capacity_m, "split_k": d.split_k,
                 "cta_k": d.cta_k, "stages": d.stages, "acc_blocks": d.acc_blocks,
                 "w_layout": {1: "in_place", 2: "tiled"}.get(d.w_layout, d.w_layout),
-                "l2_prefetch": d.l2_prefetch, "pipes": d.pipes,
+                "l2_prefetch": d.l2_prefetch, "l2_prefetch_early": d.l2_prefetch_early,
+                "pipes": d.pipes,
                 "tmem_load": {1: "32x32b", 2: "16x256b"}.get(d.tmem_load, d.tmem_load),
                 "fold": d.fold, "smem_bytes": smem.value,
                 "tmem_columns": tmem.value, "grid_ctas": grid.value}

@@ -53,12 +53,18 @@ bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % 
 
 constexpr uint64_t kDefaultPollTimeoutNs = 1000000000ull;
 constexpr uint64_t kGemmWaitLimitNs = 2000000000ull;
-// W stages past the ring each CTA warms in L2 by default (measured on GB300:
-// with two CTAs per SM 6 beats 0, 4, 8, 12 and 16 on the N=7168, K=16384,
-// S=4 chain; with one, 10 is best on N=7168, K=8192, S=2 and no worse on
-// the smaller grids).
-constexpr int kDefaultL2Prefetch = 6;
-constexpr int kDefaultL2PrefetchOnePerSm = 10;
+// W stages past the ring each CTA warms in L2 by default.  The first 70 % of
+// a grid's CTAs launch while the previous kernel streams and warm few; the
+// rest warm many.  Measured on GB300, chains of GEMM + consumer rotating
+// weights through 14 x the L2: N=7168, K=16384, S=4 (two CTAs per SM) 21.44 us
+// per call with 6 stages for every CTA, 20.25 with 4 early and 16 late, best
+// among early 0-6, late 8-24 and splits at 36-70 % of the grid; N=7168,
+// K=8192, S=2 (one per SM) 13.67 us with 10 for every CTA, 12.98 with none
+// early and 16 late.
+constexpr int kDefaultL2Prefetch = 16;
+constexpr int kDefaultL2PrefetchEarly = 4;          // two CTAs per SM
+constexpr int kDefaultL2PrefetchEarlyOnePerSm = -1;  // none
+constexpr int kEarlyCtaPercent = 70;
 // Tensor-memory columns a CTA may allocate: half of an SM's 512, so two CTAs
 // on an SM never wait for each other's allocation.  A third may wait until one
 // of them exits: harmless unless they wait for it, which split-K clusters do
@@ -127,6 +133,9 @@ mxfp8_status check_desc(const mxfp8_gemm_desc* d) {
     return fail(MXFP8_ERR_UNSUPPORTED, "w_layout must be MXFP8_W_IN_PLACE or MXFP8_W_TILED");
   if (d->l2_prefetch < -1 || d->l2_prefetch > 64)
     return fail(MXFP8_ERR_UNSUPPORTED, "l2_prefetch must be in 1..64, -1 (none) or 0 (choose)");
+  if (d->l2_prefetch_early < -1 || d->l2_prefetch_early > 64)
+    return fail(MXFP8_ERR_UNSUPPORTED,
+                "l2_prefetch_early must be in 1..64, -1 (none) or 0 (choose)");
   if (d->pipes != 0 && d->pipes != 1 && d->pipes != 2 && d->pipes != 4)
     return fail(MXFP8_ERR_UNSUPPORTED, "pipes must be 1, 2 or 4 (or 0 to choose)");
   if (d->tmem_load != 0 && d->tmem_load != MXFP8_TMEM_LOAD_32X32B &&
@@ -228,8 +237,11 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
   const int ctas = tiles * d->fold * d->split_k;
   const int per_sm = ctas > lim.sms ? 2 : 1;
   const int budget = per_sm == 2 ? lim.smem_per_sm / 2 - 1024 : lim.smem_optin;
-  if (d->l2_prefetch == 0)
-    d->l2_prefetch = per_sm == 2 ? kDefaultL2Prefetch : kDefaultL2PrefetchOnePerSm;
+  if (d->l2_prefetch_early == 0)
+    d->l2_prefetch_early = d->l2_prefetch != 0 ? d->l2_prefetch
+                           : per_sm == 2       ? kDefaultL2PrefetchEarly
+                                               : kDefaultL2PrefetchEarlyOnePerSm;
+  if (d->l2_prefetch == 0) d->l2_prefetch = kDefaultL2Prefetch;
   if (d->stages == 0) {
     int best = 0;
     for (int s = 2; s <= kMaxStages; ++s) {
@@ -255,6 +267,12 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
                                        "belong to pipe i % pipes)");
   }
   return MXFP8_OK;
+}
+
+// The grid's first CTAs, which launch while the previous kernel still runs.
+int32_t early_ctas_of(const mxfp8_gemm_desc& d) {
+  const int ctas = d.n / (kBlockN / d.fold) * d.split_k;
+  return static_cast<int32_t>(ctas * kEarlyCtaPercent / 100);
 }
 
 mxfp8_status check_rows(const mxfp8_publish_gemm* g, int32_t m) {
@@ -295,6 +313,8 @@ mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale,
   p.publish = publish ? 1 : 0;
   p.acc_blocks = g->desc.acc_blocks;
   p.l2_prefetch = std::max(0, static_cast<int>(g->desc.l2_prefetch));
+  p.l2_prefetch_early = std::max(0, static_cast<int>(g->desc.l2_prefetch_early));
+  p.early_ctas = early_ctas_of(g->desc);
   p.pipes = g->desc.pipes;
   p.tmem_load = g->desc.tmem_load;
   p.fold = g->desc.fold;
@@ -700,6 +720,8 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
   p.publish = 1;
   p.acc_blocks = d.acc_blocks;
   p.l2_prefetch = std::max(0, static_cast<int>(d.l2_prefetch));
+  p.l2_prefetch_early = std::max(0, static_cast<int>(d.l2_prefetch_early));
+  p.early_ctas = early_ctas_of(d);
   p.pipes = d.pipes;
   p.tmem_load = d.tmem_load;
   p.fold = d.fold;

@@ -61,6 +61,8 @@ struct GemmParams {
   int32_t publish;          // 1: fused publish into the mailbox; 0: C only
   int32_t acc_blocks;       // 32-wide K blocks summed in TMEM per promoted partial: 1 or 4
   int32_t l2_prefetch;      // stages past the ring warmed in L2 before the grid wait
+  int32_t l2_prefetch_early;  // the same for CTAs with blockIdx.x < early_ctas
+  int32_t early_ctas;       // the first CTAs, which launch beside the previous kernel
   int32_t pipes;            // producer lanes = MMA-issuing warps (1, 2, 4; divides stages)
   int32_t tmem_load;        // MXFP8_TMEM_LOAD_32X32B or MXFP8_TMEM_LOAD_16X256B
   int32_t fold;             // K pieces stacked in the MMA's 128 rows: 1, 2, 4 (128/fold

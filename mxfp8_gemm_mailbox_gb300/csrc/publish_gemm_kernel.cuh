@@ -284,7 +284,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       }
       // Warm L2 with the stages that come after the ring, so HBM keeps
       // streaming while the previous kernel finishes and the grid wait holds.
-      const int nwarm = min(nkt, npre + p.l2_prefetch);
+      // The first CTAs of the grid launch while the previous kernel still
+      // streams (its dependents launch as soon as it starts), so they warm
+      // fewer stages and leave it the bandwidth; the later ones, which start
+      // as its CTAs exit, warm more and bridge the hand-over.
+      const int depth = static_cast<int>(blockIdx.x) < p.early_ctas ? p.l2_prefetch_early
+                                                                     : p.l2_prefetch;
+      const int nwarm = min(nkt, npre + depth);
       if (lane == 0 && nwarm > npre) {
         if (p.w_tiled != nullptr) {
           ptx::prefetch_l2(p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt_begin + npre) *

@@ -105,6 +105,8 @@ def _create(lib, desc, w=0x1000, ws=0x2000, mb=0x3000, st=0x4000, work=0x5000, n
     ((256, 256, 8, 1, 0, 0, 0, 0, 0, 3), _lib.ERR_UNSUPPORTED, "pipes"),
     ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 3), _lib.ERR_UNSUPPORTED, "tmem_load"),
     ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 0, 3), _lib.ERR_UNSUPPORTED, "fold"),
+    ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 0, 0, 65), _lib.ERR_UNSUPPORTED, "l2_prefetch_early"),
+    ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 0, 0, -2), _lib.ERR_UNSUPPORTED, "l2_prefetch_early"),
     ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 0, 8), _lib.ERR_UNSUPPORTED, "fold"),
     ((256, 2048, 8, 8, 0, 0, 0, 0, 0, 0, 0, 2), _lib.ERR_UNSUPPORTED, "split_k 1, 2 or 4"),
     ((256, 256, 8, 1, 0, 0, 1, 0, 0, 0, 0, 2), _lib.ERR_UNSUPPORTED, "acc_blocks 4"),

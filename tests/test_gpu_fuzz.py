@@ -1,7 +1,8 @@
 """Seeded random combinations of shape and tactic -- N, ragged K, m, split-K
 S, ring depth, pipes, accumulation granularity, weight layout, TMEM read-out,
-L2 prefetch, fold, mailbox capacity -- each run through GEMM and consumer on
-integer-valued inputs and checked bit-exactly against the oracle: C, the
+L2 prefetch (both groups of CTAs), fold, mailbox capacity -- each run
+through GEMM and consumer on integer-valued inputs and checked bit-exactly
+against the oracle: C, the
 published mailbox words between the two kernels, the consumer's output, the
 state words and the reset mailbox.  Combinations the library refuses (a ring
 that does not fit, pipes that do not divide it, a fold with S = 8, one slot
@@ -34,6 +35,7 @@ def draw(rng):
         l2_prefetch=int(rng.choice([-1, 0, 3])),
         capacity=int(rng.integers(m, 9)),
         fold=int(rng.choice([0, 0, 1, 2, 4])),
+        l2_prefetch_early=int(rng.choice([-1, 0, 0, 2, 12])),
     )
 
 
@@ -49,7 +51,8 @@ def test_random_shapes_and_tactics(cuda):
             g = PublishGemm(dev(w), dev(ws), mb, split_k=p["split_k"], stages=p["stages"],
                             acc_blocks=p["acc_blocks"], w_layout=p["w_layout"],
                             l2_prefetch=p["l2_prefetch"], pipes=p["pipes"],
-                            tmem_load=p["tmem_load"], fold=p["fold"])
+                            tmem_load=p["tmem_load"], fold=p["fold"],
+                            l2_prefetch_early=p["l2_prefetch_early"])
         except Mxfp8Error as e:
             assert "ERR_UNSUPPORTED" in str(e), (p, str(e))
             refused += 1

@@ -233,21 +233,27 @@ def test_every_pipe_count_over_a_long_k_loop(cuda, stages, pipes, fold):
 
 @pytest.mark.parametrize("fold", [1, 4])
 @pytest.mark.parametrize("w_layout", [W_IN_PLACE, W_TILED])
-@pytest.mark.parametrize("l2_prefetch", [-1, 0, 3, 40])
-def test_l2_prefetch_leaves_results_unchanged(cuda, l2_prefetch, w_layout, fold):
-    """Warming later W stages in L2 before the grid wait (the default, 6
-    stages; none; a few; more than the CTA has) is bit-exact."""
+@pytest.mark.parametrize("l2_prefetch,l2_prefetch_early", [(-1, 0), (0, 0), (3, 0), (40, 0),
+                                                           (0, -1), (12, 2), (-1, 30)])
+def test_l2_prefetch_leaves_results_unchanged(cuda, l2_prefetch, l2_prefetch_early, w_layout,
+                                              fold):
+    """Warming later W stages in L2 before the grid wait (the defaults: 16 for
+    the later CTAs, 4 or none for the first 70 %; none; a few; more than the
+    CTA has; different depths for the two groups) is bit-exact."""
     n, k = 512, 8192
     w, ws, x, xs = synthetic.integer_operands(n, k, 8, seed=300 + l2_prefetch)
     want = oracle.gemm_bf16(w, ws, x, xs)
     for split in (1, 4):
         mb = Mailbox(8, n)
         g = PublishGemm(dev(w), dev(ws), mb, split_k=split, w_layout=w_layout,
-                        l2_prefetch=l2_prefetch, fold=fold)
+                        l2_prefetch=l2_prefetch, l2_prefetch_early=l2_prefetch_early, fold=fold)
         grid_ctas = n // (128 // fold) * split
         assert g.config()["grid_ctas"] == grid_ctas
-        default = 6 if grid_ctas > torch.cuda.get_device_properties(0).multi_processor_count else 10
-        assert g.config()["l2_prefetch"] == (default if l2_prefetch == 0 else l2_prefetch)
+        two_per_sm = grid_ctas > torch.cuda.get_device_properties(0).multi_processor_count
+        assert g.config()["l2_prefetch"] == (16 if l2_prefetch == 0 else l2_prefetch)
+        early = (l2_prefetch_early if l2_prefetch_early != 0 else
+                 l2_prefetch if l2_prefetch != 0 else 4 if two_per_sm else -1)
+        assert g.config()["l2_prefetch_early"] == early
         c = torch.full((8, n), 0x7FFF, dtype=torch.int16, device="cuda")
         g.run(dev(x), dev(xs), c)
         out = mb.consume(8)
