@@ -71,10 +71,10 @@ constexpr uint32_t kTransposeOffset = 4096;
 static_assert(kTransposeOffset >= kRows * kBlockN * 2 &&
                   kTransposeOffset + 4 * 32 * kRows * 8 <= kWTileBytes,
               "the transpose buffer lies in W stage 0, past the BF16 tile");
-// Folded tiles park the pairs of pieces 1..F-1 there too: (F - 1) x 128 / F
-// columns x 8 tokens x 8 bytes <= 6 KB.
+// Folded tiles park pieces' pairs there too: at most F x 128 / F columns x 8
+// tokens x 8 bytes = 8 KB.
 constexpr uint32_t kParkOffset = kTransposeOffset;
-static_assert(kParkOffset + 3 * 32 * kRows * 8 <= kWTileBytes,
+static_assert(kParkOffset + kBlockN * kRows * 8 <= kWTileBytes,
               "the folded pieces' pairs lie in W stage 0, past the BF16 tile");
 static_assert(kMaxAccRing % kMaxPipes == 0 && 4 % kMaxPipes == 0,
               "every accumulator slot belongs to one pipe");
@@ -548,134 +548,185 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       }
     }
 
-    // Folded tiles: the lanes of pieces 1..F-1 leave their pairs in W stage 0
-    // (dead: every MMA of this CTA has completed), [piece - 1][column][token],
-    // past the BF16 tile; the lane of piece 0 adds them in piece order and
-    // carries the column from here on.
-    const bool owner = piece == 0;
-    if constexpr (F > 1) {
-      float2* park = reinterpret_cast<float2*>(smem + L.w + kParkOffset);
-      if (!owner) {
-#pragma unroll
-        for (int t = 0; t < kRows; ++t)
-          park[((piece - 1) * kTileRows + col) * kRows + t] = make_float2(hi[t], lo[t]);
-      }
-      epilogue_barrier();
-      if (owner) {
-#pragma unroll
-        for (int pc = 1; pc < F; ++pc)
-#pragma unroll
-          for (int t = 0; t < kRows; ++t) {
-            const float2 v = park[((pc - 1) * kTileRows + col) * kRows + t];
-            two_sum_add(hi[t], lo[t], v.x);
-            lo[t] = __fadd_rn(lo[t], v.y);
-          }
-      }
-    }
-
-    // Split-K: every CTA sends the (hi, lo) pairs of the tokens it does not
-    // own to their owners, then sums the S pairs of its own tokens in K-slice
-    // order.  A split with no K tiles contributes zeros.  The receive buffer
-    // is [sender][column][token][hi, lo]: one CTA's pairs for one column are
-    // 8 * kShard contiguous bytes, sent as 16-byte stores (8-byte ones at
-    // S = 8, where each CTA owns one token).  Only the lanes of piece 0 take
-    // part (all of them unfolded).
-    constexpr int kShard = kRows / S;
+    // Folded tiles: the F lanes that hold one output column (one K piece
+    // each) add its pieces in piece order, the pairs passing through W stage
+    // 0 (dead: every MMA of this CTA has completed), past the BF16 tile.
+    // Unsplit (S = 1) each of the F lanes finishes 8/F of the column's tokens
+    // (parking the pairs of the others, [piece][column][token]), so the adds
+    // and roundings spread over all 128 epilogue threads; with split-K the
+    // lane of piece 0 collects all 8 tokens ([piece - 1][column][token]) and
+    // carries the column into the exchange.  Both add in the same order, so
+    // both give the same bits.
+    constexpr bool kSpreadPieces = F > 1 && S == 1;
+    constexpr int kShard = kRows / S;  // tokens this CTA finishes
     static_assert(kShard * S == kRows && (kShard == 1 || kShard % 2 == 0),
                   "tokens split evenly, in pairs or one per CTA");
-    float own_hi[kShard], own_lo[kShard];
-    if constexpr (S > 1) {
-      constexpr int kPairBytes = kShard * 8;
-      // The receive buffer lives in the W ring, which is dead only once every
-      // CTA of the cluster has finished its main loop.
-      ptx::cluster_sync();
-      if (etid == 0)
-        ptx::mbar_arrive_expect_tx(bar_recv,
-                                   static_cast<uint32_t>((S - 1) * kTileRows * kPairBytes));
+    const bool owner = piece == 0;
+    uint16_t* ctile = reinterpret_cast<uint16_t*>(smem + L.ctile);  // [tokens][kTileRows]
+    if constexpr (kSpreadPieces) {
+      constexpr int kPerLane = kRows / F;
+      float2* park = reinterpret_cast<float2*>(smem + L.w + kParkOffset);
 #pragma unroll
-      for (int peer = 0; peer < S; ++peer) {
-        if (peer == static_cast<int>(split) || !owner) continue;
-        const int sender = static_cast<int>(split) < peer ? static_cast<int>(split)
-                                                          : static_cast<int>(split) - 1;
-        const uint32_t remote_bar = ptx::map_to_rank(bar_recv, peer);
-        const uint32_t remote =
-            ptx::map_to_rank(sbase + L.recv + (sender * kTileRows + col) * kPairBytes, peer);
-        if constexpr (kShard == 1) {
-          ptx::st_async_remote_v2(remote, __float_as_uint(hi[peer]), __float_as_uint(lo[peer]),
-                                  remote_bar);
-        } else {
+      for (int t = 0; t < kRows; ++t)
+        if (t / kPerLane != piece) park[(piece * kTileRows + col) * kRows + t] = make_float2(hi[t], lo[t]);
+      epilogue_barrier();
+      const float a = p.alpha != nullptr ? *p.alpha : 1.0f;
 #pragma unroll
-          for (int jj = 0; jj < kShard; jj += 2)
-            ptx::st_async_remote_v4(
-                remote + jj * 8,
-                make_uint4(__float_as_uint(hi[peer * kShard + jj]),
-                           __float_as_uint(lo[peer * kShard + jj]),
-                           __float_as_uint(hi[peer * kShard + jj + 1]),
-                           __float_as_uint(lo[peer * kShard + jj + 1])),
-                remote_bar);
-        }
-      }
-      // This thread addresses no peer after its sends: its half of the final
-      // cluster barrier, whose wait comes before the CTA exits.
-      ptx::cluster_arrive();
-      if (!ptx::mbar_wait_cluster(bar_recv, 0, p.wait_limit_ns)) raise_flag(p.state, 0x2u);
-      const uint8_t* recv = smem + L.recv;
+      for (int j = 0; j < kPerLane; ++j) {
+        float oh = 0.0f, ol = 0.0f;  // this lane's own pair of token piece * kPerLane + j
 #pragma unroll
-      for (int jj = 0; jj < kShard; ++jj) {
+        for (int t = j; t < kRows; t += kPerLane)
+          if (t / kPerLane == piece) {
+            oh = hi[t];
+            ol = lo[t];
+          }
+        const int t = piece * kPerLane + j;
         float sh = 0.0f, sl = 0.0f;
 #pragma unroll
-        for (int src = 0; src < S; ++src) {
-          float vh, vl;
-          if (src == static_cast<int>(split)) {
-            vh = 0.0f;
-            vl = 0.0f;
-#pragma unroll
-            for (int q = 0; q < kRows; ++q)
-              if (q == static_cast<int>(split) * kShard + jj) {
-                vh = hi[q];
-                vl = lo[q];
-              }
-          } else {
-            const int sidx = src < static_cast<int>(split) ? src : src - 1;
-            const float2 pair = *reinterpret_cast<const float2*>(
-                recv + (sidx * kTileRows + col) * kPairBytes + jj * 8);
-            vh = pair.x;
-            vl = pair.y;
+        for (int q = 0; q < F; ++q) {
+          float vh = oh, vl = ol;
+          if (q != piece) {
+            const float2 v = park[(q * kTileRows + col) * kRows + t];
+            vh = v.x;
+            vl = v.y;
           }
-          two_sum_add(sh, sl, vh);
-          sl = __fadd_rn(sl, vl);
+          if (q == 0) {
+            sh = vh;
+            sl = vl;
+          } else {
+            two_sum_add(sh, sl, vh);
+            sl = __fadd_rn(sl, vl);
+          }
         }
-        own_hi[jj] = sh;
-        own_lo[jj] = sl;
+        if (p.alpha != nullptr) {  // the global scale, as below
+          const float ph = __fmul_rn(a, sh);
+          const float pe = __fmaf_rn(a, sh, -ph);
+          sl = __fmaf_rn(a, sl, pe);
+          sh = ph;
+        }
+        ctile[t * kTileRows + col] = bf16_bits_from_pair(sh, sl);
       }
     } else {
+      if constexpr (F > 1) {
+        float2* park = reinterpret_cast<float2*>(smem + L.w + kParkOffset);
+        if (!owner) {
 #pragma unroll
-      for (int jj = 0; jj < kShard; ++jj) {
-        own_hi[jj] = hi[jj];
-        own_lo[jj] = lo[jj];
+          for (int t = 0; t < kRows; ++t)
+            park[((piece - 1) * kTileRows + col) * kRows + t] = make_float2(hi[t], lo[t]);
+        }
+        epilogue_barrier();
+        if (owner) {
+#pragma unroll
+          for (int pc = 1; pc < F; ++pc)
+#pragma unroll
+            for (int t = 0; t < kRows; ++t) {
+              const float2 v = park[((pc - 1) * kTileRows + col) * kRows + t];
+              two_sum_add(hi[t], lo[t], v.x);
+              lo[t] = __fadd_rn(lo[t], v.y);
+            }
+        }
       }
-    }
 
-    // The global scale (gemm page, epilog_warp with use_scale: the
-    // accumulator times mScale[0]) multiplies the compensated sum before its
-    // one rounding: alpha * hi exactly as a product and its FMA error, plus
-    // alpha * lo.  It is read after the grid wait like x.
-    if (p.alpha != nullptr) {
-      const float a = *p.alpha;
+      // Split-K: every CTA sends the (hi, lo) pairs of the tokens it does not
+      // own to their owners, then sums the S pairs of its own tokens in K-slice
+      // order.  A split with no K tiles contributes zeros.  The receive buffer
+      // is [sender][column][token][hi, lo]: one CTA's pairs for one column are
+      // 8 * kShard contiguous bytes, sent as 16-byte stores (8-byte ones at
+      // S = 8, where each CTA owns one token).  Only the lanes of piece 0 take
+      // part (all of them unfolded).
+      float own_hi[kShard], own_lo[kShard];
+      if constexpr (S > 1) {
+        constexpr int kPairBytes = kShard * 8;
+        // The receive buffer lives in the W ring, which is dead only once every
+        // CTA of the cluster has finished its main loop.
+        ptx::cluster_sync();
+        if (etid == 0)
+          ptx::mbar_arrive_expect_tx(bar_recv,
+                                     static_cast<uint32_t>((S - 1) * kTileRows * kPairBytes));
 #pragma unroll
-      for (int jj = 0; jj < kShard; ++jj) {
-        const float ph = __fmul_rn(a, own_hi[jj]);
-        const float pe = __fmaf_rn(a, own_hi[jj], -ph);
-        own_lo[jj] = __fmaf_rn(a, own_lo[jj], pe);
-        own_hi[jj] = ph;
+        for (int peer = 0; peer < S; ++peer) {
+          if (peer == static_cast<int>(split) || !owner) continue;
+          const int sender = static_cast<int>(split) < peer ? static_cast<int>(split)
+                                                            : static_cast<int>(split) - 1;
+          const uint32_t remote_bar = ptx::map_to_rank(bar_recv, peer);
+          const uint32_t remote =
+              ptx::map_to_rank(sbase + L.recv + (sender * kTileRows + col) * kPairBytes, peer);
+          if constexpr (kShard == 1) {
+            ptx::st_async_remote_v2(remote, __float_as_uint(hi[peer]), __float_as_uint(lo[peer]),
+                                    remote_bar);
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < kShard; jj += 2)
+              ptx::st_async_remote_v4(
+                  remote + jj * 8,
+                  make_uint4(__float_as_uint(hi[peer * kShard + jj]),
+                             __float_as_uint(lo[peer * kShard + jj]),
+                             __float_as_uint(hi[peer * kShard + jj + 1]),
+                             __float_as_uint(lo[peer * kShard + jj + 1])),
+                  remote_bar);
+          }
+        }
+        // This thread addresses no peer after its sends: its half of the final
+        // cluster barrier, whose wait comes before the CTA exits.
+        ptx::cluster_arrive();
+        if (!ptx::mbar_wait_cluster(bar_recv, 0, p.wait_limit_ns)) raise_flag(p.state, 0x2u);
+        const uint8_t* recv = smem + L.recv;
+#pragma unroll
+        for (int jj = 0; jj < kShard; ++jj) {
+          float sh = 0.0f, sl = 0.0f;
+#pragma unroll
+          for (int src = 0; src < S; ++src) {
+            float vh, vl;
+            if (src == static_cast<int>(split)) {
+              vh = 0.0f;
+              vl = 0.0f;
+#pragma unroll
+              for (int q = 0; q < kRows; ++q)
+                if (q == static_cast<int>(split) * kShard + jj) {
+                  vh = hi[q];
+                  vl = lo[q];
+                }
+            } else {
+              const int sidx = src < static_cast<int>(split) ? src : src - 1;
+              const float2 pair = *reinterpret_cast<const float2*>(
+                  recv + (sidx * kTileRows + col) * kPairBytes + jj * 8);
+              vh = pair.x;
+              vl = pair.y;
+            }
+            two_sum_add(sh, sl, vh);
+            sl = __fadd_rn(sl, vl);
+          }
+          own_hi[jj] = sh;
+          own_lo[jj] = sl;
+        }
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < kShard; ++jj) {
+          own_hi[jj] = hi[jj];
+          own_lo[jj] = lo[jj];
+        }
       }
-    }
 
-    uint16_t* ctile = reinterpret_cast<uint16_t*>(smem + L.ctile);  // [kShard][kTileRows]
-    if (owner) {
+      // The global scale (gemm page, epilog_warp with use_scale: the
+      // accumulator times mScale[0]) multiplies the compensated sum before its
+      // one rounding: alpha * hi exactly as a product and its FMA error, plus
+      // alpha * lo.  It is read after the grid wait like x.
+      if (p.alpha != nullptr) {
+        const float a = *p.alpha;
 #pragma unroll
-      for (int jj = 0; jj < kShard; ++jj)
-        ctile[jj * kTileRows + col] = bf16_bits_from_pair(own_hi[jj], own_lo[jj]);
+        for (int jj = 0; jj < kShard; ++jj) {
+          const float ph = __fmul_rn(a, own_hi[jj]);
+          const float pe = __fmaf_rn(a, own_hi[jj], -ph);
+          own_lo[jj] = __fmaf_rn(a, own_lo[jj], pe);
+          own_hi[jj] = ph;
+        }
+      }
+
+      if (owner) {
+#pragma unroll
+        for (int jj = 0; jj < kShard; ++jj)
+          ctile[jj * kTileRows + col] = bf16_bits_from_pair(own_hi[jj], own_lo[jj]);
+      }
     }
     epilogue_barrier();
 
