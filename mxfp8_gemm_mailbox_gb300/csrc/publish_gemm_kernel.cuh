@@ -550,30 +550,27 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
     // Folded tiles: the F lanes that hold one output column (one K piece
     // each) add its pieces in piece order, the pairs passing through W stage
-    // 0 (dead: every MMA of this CTA has completed), past the BF16 tile.
-    // Unsplit (S = 1) each of the F lanes finishes 8/F of the column's tokens
-    // (parking the pairs of the others, [piece][column][token]), so the adds
-    // and roundings spread over all 128 epilogue threads; with split-K the
-    // lane of piece 0 collects all 8 tokens ([piece - 1][column][token]) and
-    // carries the column into the exchange.  Both add in the same order, so
-    // both give the same bits.
-    constexpr bool kSpreadPieces = F > 1 && S == 1;
+    // 0 (dead: every MMA of this CTA has completed), past the BF16 tile: lane
+    // p of a column takes its tokens [p 8/F, (p+1) 8/F), parks the pairs of the
+    // others ([piece][column][token]) and adds the F pieces of its own.  With
+    // split-K it then sends each of its tokens that another CTA owns to the
+    // same lane of that CTA, and finishes those its own CTA owns.  The sums
+    // keep piece order, then K-slice order, as an unfolded tile does.
     constexpr int kShard = kRows / S;  // tokens this CTA finishes
     static_assert(kShard * S == kRows && (kShard == 1 || kShard % 2 == 0),
                   "tokens split evenly, in pairs or one per CTA");
-    const bool owner = piece == 0;
-    uint16_t* ctile = reinterpret_cast<uint16_t*>(smem + L.ctile);  // [tokens][kTileRows]
-    if constexpr (kSpreadPieces) {
-      constexpr int kPerLane = kRows / F;
+    uint16_t* ctile = reinterpret_cast<uint16_t*>(smem + L.ctile);  // [kShard][kTileRows]
+    if constexpr (F > 1) {
+      constexpr int kPerLane = kRows / F;  // tokens a lane adds the pieces of
       float2* park = reinterpret_cast<float2*>(smem + L.w + kParkOffset);
 #pragma unroll
       for (int t = 0; t < kRows; ++t)
         if (t / kPerLane != piece) park[(piece * kTileRows + col) * kRows + t] = make_float2(hi[t], lo[t]);
       epilogue_barrier();
-      const float a = p.alpha != nullptr ? *p.alpha : 1.0f;
+      float red_hi[kPerLane], red_lo[kPerLane];  // tokens piece * kPerLane + j
 #pragma unroll
       for (int j = 0; j < kPerLane; ++j) {
-        float oh = 0.0f, ol = 0.0f;  // this lane's own pair of token piece * kPerLane + j
+        float oh = 0.0f, ol = 0.0f;  // this lane's own pair of the token
 #pragma unroll
         for (int t = j; t < kRows; t += kPerLane)
           if (t / kPerLane == piece) {
@@ -598,42 +595,85 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             sl = __fadd_rn(sl, vl);
           }
         }
-        if (p.alpha != nullptr) {  // the global scale, as below
+        red_hi[j] = sh;
+        red_lo[j] = sl;
+      }
+      const float a = p.alpha != nullptr ? *p.alpha : 1.0f;
+      // The global scale and the one rounding of a finished token (as below).
+      auto finish = [&](int t_local, float sh, float sl) {
+        if (p.alpha != nullptr) {
           const float ph = __fmul_rn(a, sh);
           const float pe = __fmaf_rn(a, sh, -ph);
           sl = __fmaf_rn(a, sl, pe);
           sh = ph;
         }
-        ctile[t * kTileRows + col] = bf16_bits_from_pair(sh, sl);
+        ctile[t_local * kTileRows + col] = bf16_bits_from_pair(sh, sl);
+      };
+      if constexpr (S == 1) {
+#pragma unroll
+        for (int j = 0; j < kPerLane; ++j) finish(piece * kPerLane + j, red_hi[j], red_lo[j]);
+      } else {
+        // A lane's tokens fall in runs of kRun that one CTA owns; the receive
+        // buffer is [sender][MMA row][kRun pairs], the MMA row naming the lane.
+        constexpr int kRun = kPerLane < kShard ? kPerLane : kShard;
+        constexpr int kRuns = kPerLane / kRun;
+        static_assert(kRun % 2 == 0, "runs go out as 16-byte stores of two pairs");
+        ptx::cluster_sync();  // every peer's W ring is dead before any remote store
+        if (etid == 0)
+          ptx::mbar_arrive_expect_tx(bar_recv,
+                                     static_cast<uint32_t>((S - 1) * kTileRows * kShard * 8));
+        const int sender = static_cast<int>(split);
+#pragma unroll
+        for (int r = 0; r < kRuns; ++r) {
+          const int dest = (piece * kPerLane + r * kRun) / kShard;
+          if (dest == sender) continue;
+          const int sidx = sender < dest ? sender : sender - 1;
+          const uint32_t remote_bar = ptx::map_to_rank(bar_recv, dest);
+          const uint32_t remote =
+              ptx::map_to_rank(sbase + L.recv + (sidx * kBlockN + arow) * kRun * 8, dest);
+#pragma unroll
+          for (int j = 0; j < kRun; j += 2)
+            ptx::st_async_remote_v4(
+                remote + j * 8,
+                make_uint4(__float_as_uint(red_hi[r * kRun + j]), __float_as_uint(red_lo[r * kRun + j]),
+                           __float_as_uint(red_hi[r * kRun + j + 1]),
+                           __float_as_uint(red_lo[r * kRun + j + 1])),
+                remote_bar);
+        }
+        // This thread addresses no peer after its sends: its half of the final
+        // cluster barrier, whose wait comes before the CTA exits.
+        ptx::cluster_arrive();
+        if (!ptx::mbar_wait_cluster(bar_recv, 0, p.wait_limit_ns)) raise_flag(p.state, 0x2u);
+        const float2* recv = reinterpret_cast<const float2*>(smem + L.recv);
+#pragma unroll
+        for (int r = 0; r < kRuns; ++r) {
+          if ((piece * kPerLane + r * kRun) / kShard != sender) continue;
+#pragma unroll
+          for (int j = 0; j < kRun; ++j) {
+            float sh = 0.0f, sl = 0.0f;
+#pragma unroll
+            for (int src = 0; src < S; ++src) {
+              float vh = red_hi[r * kRun + j], vl = red_lo[r * kRun + j];
+              if (src != sender) {
+                const int sidx = src < sender ? src : src - 1;
+                const float2 v = recv[(sidx * kBlockN + arow) * kRun + j];
+                vh = v.x;
+                vl = v.y;
+              }
+              two_sum_add(sh, sl, vh);
+              sl = __fadd_rn(sl, vl);
+            }
+            finish(piece * kPerLane + r * kRun + j - sender * kShard, sh, sl);
+          }
+        }
       }
     } else {
-      if constexpr (F > 1) {
-        float2* park = reinterpret_cast<float2*>(smem + L.w + kParkOffset);
-        if (!owner) {
-#pragma unroll
-          for (int t = 0; t < kRows; ++t)
-            park[((piece - 1) * kTileRows + col) * kRows + t] = make_float2(hi[t], lo[t]);
-        }
-        epilogue_barrier();
-        if (owner) {
-#pragma unroll
-          for (int pc = 1; pc < F; ++pc)
-#pragma unroll
-            for (int t = 0; t < kRows; ++t) {
-              const float2 v = park[((pc - 1) * kTileRows + col) * kRows + t];
-              two_sum_add(hi[t], lo[t], v.x);
-              lo[t] = __fadd_rn(lo[t], v.y);
-            }
-        }
-      }
-
       // Split-K: every CTA sends the (hi, lo) pairs of the tokens it does not
       // own to their owners, then sums the S pairs of its own tokens in K-slice
       // order.  A split with no K tiles contributes zeros.  The receive buffer
       // is [sender][column][token][hi, lo]: one CTA's pairs for one column are
       // 8 * kShard contiguous bytes, sent as 16-byte stores (8-byte ones at
-      // S = 8, where each CTA owns one token).  Only the lanes of piece 0 take
-      // part (all of them unfolded).
+      // S = 8, where each CTA owns one token).
       float own_hi[kShard], own_lo[kShard];
       if constexpr (S > 1) {
         constexpr int kPairBytes = kShard * 8;
@@ -645,7 +685,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                                      static_cast<uint32_t>((S - 1) * kTileRows * kPairBytes));
 #pragma unroll
         for (int peer = 0; peer < S; ++peer) {
-          if (peer == static_cast<int>(split) || !owner) continue;
+          if (peer == static_cast<int>(split)) continue;
           const int sender = static_cast<int>(split) < peer ? static_cast<int>(split)
                                                             : static_cast<int>(split) - 1;
           const uint32_t remote_bar = ptx::map_to_rank(bar_recv, peer);
@@ -722,11 +762,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
       }
 
-      if (owner) {
 #pragma unroll
-        for (int jj = 0; jj < kShard; ++jj)
-          ctile[jj * kTileRows + col] = bf16_bits_from_pair(own_hi[jj], own_lo[jj]);
-      }
+      for (int jj = 0; jj < kShard; ++jj)
+        ctile[jj * kTileRows + col] = bf16_bits_from_pair(own_hi[jj], own_lo[jj]);
     }
     epilogue_barrier();
 
