@@ -193,6 +193,19 @@ mxfp8_status mxfp8_publish_gemm_config(const mxfp8_publish_gemm* gemm, mxfp8_gem
                                        int32_t* smem_bytes, int32_t* tmem_columns,
                                        int32_t* grid_ctas);
 
+/* The tactic mxfp8_publish_gemm_create would resolve for `desc` on a device
+ * with `sms` SMs, `smem_per_sm` bytes of shared memory per SM and
+ * `smem_per_block_optin` bytes per CTA at most (GB300: 152, 233472, 232448),
+ * with no device, memory or launch involved: the same checks and the same
+ * resolution.  *resolved receives the descriptor with every tactic field
+ * filled in; the other outputs (each may be NULL) as for
+ * mxfp8_publish_gemm_config.  Returns what create would for the descriptor,
+ * or MXFP8_ERR_INVALID for non-positive limits. */
+mxfp8_status mxfp8_publish_gemm_plan(const mxfp8_gemm_desc* desc, int32_t sms,
+                                     int32_t smem_per_sm, int32_t smem_per_block_optin,
+                                     mxfp8_gemm_desc* resolved, int32_t* smem_bytes,
+                                     int32_t* tmem_columns, int32_t* grid_ctas);
+
 /* Everything a run with m rows needs, done ahead, launching nothing
  * (publishing_gemm page, PublishingMxfp8Linear.precompile: a publish without
  * its consumer would desynchronise the mailbox).  Call before CUDA-graph

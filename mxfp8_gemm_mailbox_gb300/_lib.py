@@ -48,6 +48,9 @@ SIGNATURES = {
     "mxfp8_publish_gemm_config": (ctypes.c_int, [_vp, ctypes.POINTER(GemmDesc),
                                                  ctypes.POINTER(_i32), ctypes.POINTER(_i32),
                                                  ctypes.POINTER(_i32)]),
+    "mxfp8_publish_gemm_plan": (ctypes.c_int, [ctypes.POINTER(GemmDesc), _i32, _i32, _i32,
+                                               ctypes.POINTER(GemmDesc), ctypes.POINTER(_i32),
+                                               ctypes.POINTER(_i32), ctypes.POINTER(_i32)]),
     "mxfp8_publish_gemm_precompile": (ctypes.c_int, [_vp, _i32]),
     "mxfp8_publish_gemm_run": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, _vp]),
     "mxfp8_gemm_run_unfused": (ctypes.c_int, [_vp, _vp, _vp, _i32, _vp, _vp]),

@@ -75,6 +75,37 @@ class Mailbox:
         return st, list(words)
 
 
+def _config_dict(d: GemmDesc, smem: int, tmem: int, grid: int) -> dict:
+    return {"n": d.n, "k": d.k, "capacity_m": d.capacity_m, "split_k": d.split_k,
+            "cta_k": d.cta_k, "stages": d.stages, "acc_blocks": d.acc_blocks,
+            "w_layout": {1: "in_place", 2: "tiled"}.get(d.w_layout, d.w_layout),
+            "l2_prefetch": d.l2_prefetch, "l2_prefetch_early": d.l2_prefetch_early,
+            "pipes": d.pipes,
+            "tmem_load": {1: "32x32b", 2: "16x256b"}.get(d.tmem_load, d.tmem_load),
+            "fold": d.fold, "smem_bytes": smem, "tmem_columns": tmem, "grid_ctas": grid}
+
+
+# GB300: SMs, shared memory per SM, shared memory per CTA at most.
+GB300_LIMITS = (152, 233472, 232448)
+
+
+def plan_gemm(n: int, k: int, capacity_m: int = 8, split_k: int = 0, stages: int = 0,
+              acc_blocks: int = 0, w_layout: int = 0, l2_prefetch: int = 0, pipes: int = 0,
+              tmem_load: int = 0, fold: int = 0, l2_prefetch_early: int = 0,
+              limits: tuple = GB300_LIMITS) -> dict:
+    """The tactic PublishGemm would resolve for this shape on a device with
+    `limits` = (SMs, shared memory per SM, shared memory per CTA), as
+    PublishGemm.config() reports it; needs no GPU."""
+    desc = GemmDesc(n, k, capacity_m, split_k, 0, stages, acc_blocks, w_layout, l2_prefetch,
+                    pipes, tmem_load, fold, l2_prefetch_early)
+    out = GemmDesc()
+    smem, tmem, grid = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    check(_lib.load().mxfp8_publish_gemm_plan(ctypes.byref(desc), *limits, ctypes.byref(out),
+                                              ctypes.byref(smem), ctypes.byref(tmem),
+                                              ctypes.byref(grid)), "mxfp8_publish_gemm_plan")
+    return _config_dict(out, smem.value, tmem.value, grid.value)
+
+
 class PublishGemm:
     """One MXFP8 weight ``W [N][K]`` (E4M3 codes) with its scales ``[N][K/32]``
     (E8M0 codes), publishing into ``mailbox``.  The weight, mailbox and the
@@ -111,14 +142,7 @@ class PublishGemm:
         check(_lib.load().mxfp8_publish_gemm_config(self._handle, ctypes.byref(d),
                                                     ctypes.byref(smem), ctypes.byref(tmem),
                                                     ctypes.byref(grid)), "mxfp8_publish_gemm_config")
-        return {"n": d.n, "k": d.k, "capacity_m": d.capacity_m, "split_k": d.split_k,
-                "cta_k": d.cta_k, "stages": d.stages, "acc_blocks": d.acc_blocks,
-                "w_layout": {1: "in_place", 2: "tiled"}.get(d.w_layout, d.w_layout),
-                "l2_prefetch": d.l2_prefetch, "l2_prefetch_early": d.l2_prefetch_early,
-                "pipes": d.pipes,
-                "tmem_load": {1: "32x32b", 2: "16x256b"}.get(d.tmem_load, d.tmem_load),
-                "fold": d.fold, "smem_bytes": smem.value,
-                "tmem_columns": tmem.value, "grid_ctas": grid.value}
+        return _config_dict(d, smem.value, tmem.value, grid.value)
 
     def precompile(self, m: int) -> None:
         check(_lib.load().mxfp8_publish_gemm_precompile(self._handle, m),

@@ -468,6 +468,33 @@ mxfp8_status mxfp8_publish_gemm_config(const mxfp8_publish_gemm* gemm, mxfp8_gem
   return MXFP8_OK;
 }
 
+mxfp8_status mxfp8_publish_gemm_plan(const mxfp8_gemm_desc* desc, int32_t sms,
+                                     int32_t smem_per_sm, int32_t smem_per_block_optin,
+                                     mxfp8_gemm_desc* resolved, int32_t* smem_bytes,
+                                     int32_t* tmem_columns, int32_t* grid_ctas) {
+  mxfp8_status st = check_desc(desc);
+  if (st != MXFP8_OK) return st;
+  if (sms <= 0 || smem_per_sm <= 0 || smem_per_block_optin <= 0)
+    return fail(MXFP8_ERR_INVALID, "device limits must be positive");
+  DeviceLimits lim;
+  lim.sms = sms;
+  lim.smem_per_sm = smem_per_sm;
+  lim.smem_optin = smem_per_block_optin;
+  mxfp8_gemm_desc d = *desc;
+  st = resolve_tactic(&d, lim);
+  if (st != MXFP8_OK) return st;
+  const int k_tiles = k_tiles_for_fold(d.k, d.fold);
+  const int tiles_per_split = (k_tiles + d.split_k - 1) / d.split_k;
+  const GemmSmemLayout layout = at_most_two_per_sm(
+      gemm_smem_layout(d.stages, d.split_k, tiles_per_split, d.fold), d.split_k, lim);
+  if (resolved) *resolved = d;
+  if (smem_bytes) *smem_bytes = static_cast<int32_t>(layout.total);
+  if (tmem_columns)
+    *tmem_columns = static_cast<int32_t>(gemm_tmem_plan(d.stages, d.acc_blocks, d.fold).cols);
+  if (grid_ctas) *grid_ctas = (d.n / (kBlockN / d.fold)) * d.split_k;
+  return MXFP8_OK;
+}
+
 mxfp8_status mxfp8_publish_gemm_precompile(mxfp8_publish_gemm* gemm, int32_t m) {
   if (!gemm) return fail(MXFP8_ERR_INVALID, "gemm handle is NULL");
   mxfp8_status st = check_rows(gemm, m);

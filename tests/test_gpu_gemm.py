@@ -188,6 +188,27 @@ def test_default_fold(cuda):
         g.close()
 
 
+def test_plan_matches_create(cuda):
+    """mxfp8_publish_gemm_plan, given this device's limits, resolves every
+    tactic field, the shared memory, tensor-memory columns and grid exactly as
+    creating the handle does."""
+    from mxfp8_gemm_mailbox_gb300 import plan_gemm
+    props = torch.cuda.get_device_properties(0)
+    limits = (props.multi_processor_count,
+              getattr(props, "shared_memory_per_multiprocessor", 233472),
+              props.shared_memory_per_block_optin)
+    for n, k, kw in [(7168, 16384, dict(split_k=4)), (7168, 8192, dict(split_k=2)),
+                     (4096, 4096, dict(split_k=1)), (256, 256, dict(split_k=1)),
+                     (2048, 2048, dict()), (1024, 4096, dict(split_k=2, stages=4)),
+                     (512, 1152, dict(split_k=4, fold=2, l2_prefetch=3)),
+                     (384, 8192, dict(acc_blocks=1, tmem_load=TMEM_LOAD_16X256B))]:
+        w = torch.zeros((n, k), dtype=torch.uint8, device="cuda")
+        ws = torch.full((n, k // 32), 127, dtype=torch.uint8, device="cuda")
+        g = PublishGemm(w, ws, Mailbox(8, n), **kw)
+        assert plan_gemm(n, k, limits=limits, **kw) == g.config(), (n, k, kw)
+        g.close()
+
+
 def test_at_most_two_ctas_per_sm(cuda):
     """A clustered launch asks for more than a third of an SM's shared memory,
     short rings included, so at most two of its CTAs (each holding at most 256

@@ -1,0 +1,105 @@
+"""The tactic resolver on the CPU, through mxfp8_publish_gemm_plan: the plans
+of the benchmarked workloads on GB300's limits, the invariants every plan
+keeps over a grid of shapes and tactics (tensor memory within half an SM,
+shared memory within a CTA's limit, at most two CTAs of a clustered launch
+per SM, pipes dividing the ring, folding only where it is taken and pads K no
+further), the refusals, and how the fold follows the SM count."""
+import itertools
+
+import pytest
+
+from mxfp8_gemm_mailbox_gb300 import Mxfp8Error, plan_gemm
+from mxfp8_gemm_mailbox_gb300._lib import TMEM_LOAD_16X256B
+
+SMS, SMEM_PER_SM, SMEM_OPTIN = 152, 233472, 232448
+
+
+def test_plans_of_the_benchmarked_workloads():
+    want = {
+        (7168, 16384, 4): dict(fold=1, stages=6, pipes=2, l2_prefetch=16, l2_prefetch_early=4,
+                               smem_bytes=113280, tmem_columns=128, grid_ctas=224),
+        (7168, 8192, 2): dict(fold=1, stages=12, pipes=4, l2_prefetch=16, l2_prefetch_early=-1,
+                              smem_bytes=220896, tmem_columns=256, grid_ctas=112),
+        (4096, 4096, 1): dict(fold=4, stages=8, pipes=4, l2_prefetch=16, l2_prefetch_early=-1,
+                              smem_bytes=173728, tmem_columns=256, grid_ctas=128),
+        (256, 256, 1): dict(fold=2, stages=2, pipes=2, grid_ctas=4),
+    }
+    for (n, k, s), fields in want.items():
+        plan = plan_gemm(n, k, split_k=s)
+        got = {f: plan[f] for f in fields}
+        assert got == fields, ((n, k, s), plan)
+        assert plan["w_layout"] == "tiled" and plan["tmem_load"] == "32x32b"
+        assert plan["acc_blocks"] == 4 and plan["cta_k"] == 128
+
+
+def _k_tiles(k, fold):
+    return -(-k // (128 * fold))
+
+
+TACTICS = list(itertools.product([0, 1, 2, 4, 8], [0, 2, 3, 6, 12, 16], [0, 1, 4], [0, 1, 2, 4],
+                                 [0, 1, 2, 4], [0, TMEM_LOAD_16X256B]))
+
+
+@pytest.mark.parametrize("n", [128, 256, 1024, 2048, 4096, 7168, 16384])
+def test_every_plan_keeps_the_invariants(n):
+    accepted = 0
+    for k in (32, 96, 256, 1152, 4096, 16384, 32768):
+        for split, stages, acc, pipes, fold, load in TACTICS:
+            try:
+                p = plan_gemm(n, k, split_k=split, stages=stages, acc_blocks=acc, pipes=pipes,
+                              fold=fold, tmem_load=load)
+            except Mxfp8Error as e:
+                assert "ERR_UNSUPPORTED" in str(e), (n, k, split, stages, acc, pipes, fold, load)
+                continue
+            accepted += 1
+            where = (n, k, split, stages, acc, pipes, fold, load, p)
+            assert p["tmem_columns"] <= 256, where
+            assert p["smem_bytes"] <= SMEM_OPTIN, where
+            assert p["stages"] % p["pipes"] == 0, where
+            assert p["grid_ctas"] == n // (128 // p["fold"]) * p["split_k"], where
+            if p["split_k"] > 1:  # at most two CTAs of a clustered launch on an SM
+                assert 3 * (p["smem_bytes"] + 1024) > SMEM_PER_SM, where
+            for field, asked in (("split_k", split), ("stages", stages), ("acc_blocks", acc),
+                                 ("pipes", pipes), ("fold", fold)):
+                if asked:
+                    assert p[field] == asked, where
+            if p["fold"] > 1:
+                assert p["split_k"] <= 4 and p["acc_blocks"] == 4, where
+                assert p["tmem_load"] == "32x32b", where
+                if fold == 0:  # chosen: one CTA per SM at most, no more K padding
+                    assert p["grid_ctas"] <= SMS, where
+                    assert _k_tiles(k, p["fold"]) * p["fold"] == _k_tiles(k, 1), where
+                    assert _k_tiles(k, p["fold"]) >= p["split_k"], where
+            early = p["l2_prefetch_early"]
+            assert p["l2_prefetch"] == 16 and early == (4 if p["grid_ctas"] > SMS else -1), where
+    assert accepted > 0
+
+
+def test_refusals_match_create():
+    bad = [dict(fold=2, split_k=8), dict(fold=4, acc_blocks=1), dict(fold=2, tmem_load=2),
+           dict(fold=3), dict(split_k=3), dict(stages=6, pipes=4), dict(l2_prefetch_early=65),
+           dict(stages=1)]
+    for kw in bad:
+        with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED"):
+            plan_gemm(1024, 4096, **kw)
+    with pytest.raises(Mxfp8Error, match="ERR_INVALID"):
+        plan_gemm(200, 4096)
+    with pytest.raises(Mxfp8Error, match="ERR_INVALID"):
+        plan_gemm(1024, 4096, limits=(0, SMEM_PER_SM, SMEM_OPTIN))
+
+
+def test_the_fold_follows_the_sm_count():
+    # N=4096, K=4096, S=1: 32 tiles fold 4 ways on 152 SMs (128 CTAs); with 100
+    # SMs four ways would not fit one CTA per SM, so two.
+    assert plan_gemm(4096, 4096, split_k=1)["fold"] == 4
+    assert plan_gemm(4096, 4096, split_k=1, limits=(100, SMEM_PER_SM, SMEM_OPTIN))["fold"] == 2
+    assert plan_gemm(4096, 4096, split_k=1, limits=(40, SMEM_PER_SM, SMEM_OPTIN))["fold"] == 1
+
+
+def test_split_choice_when_left_open():
+    # S = 0: the largest of 2, 4 with at most two CTAs per SM and >= 2 K tiles
+    # per split.
+    assert plan_gemm(7168, 16384)["split_k"] == 4
+    assert plan_gemm(16384, 16384)["split_k"] == 2
+    assert plan_gemm(2048, 256)["split_k"] == 1
+    assert plan_gemm(2048, 2048)["grid_ctas"] == 2048 // 64 * 4  # S = 4, fold 2
