@@ -554,8 +554,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     // p of a column takes its tokens [p 8/F, (p+1) 8/F), parks the pairs of the
     // others ([piece][column][token]) and adds the F pieces of its own.  With
     // split-K it then sends each of its tokens that another CTA owns to the
-    // same lane of that CTA, and finishes those its own CTA owns.  The sums
-    // keep piece order, then K-slice order, as an unfolded tile does.
+    // same lane of that CTA, and finishes those its own CTA owns.  The
+    // additions run in piece order, then K-slice order, whichever lane does
+    // them.
     constexpr int kShard = kRows / S;  // tokens this CTA finishes
     static_assert(kShard * S == kRows && (kShard == 1 || kShard % 2 == 0),
                   "tokens split evenly, in pairs or one per CTA");
@@ -565,7 +566,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       float2* park = reinterpret_cast<float2*>(smem + L.w + kParkOffset);
 #pragma unroll
       for (int t = 0; t < kRows; ++t)
-        if (t / kPerLane != piece) park[(piece * kTileRows + col) * kRows + t] = make_float2(hi[t], lo[t]);
+        if (t / kPerLane != piece)
+          park[(piece * kTileRows + col) * kRows + t] = make_float2(hi[t], lo[t]);
       epilogue_barrier();
       float red_hi[kPerLane], red_lo[kPerLane];  // tokens piece * kPerLane + j
 #pragma unroll
