@@ -101,7 +101,7 @@ typedef struct mxfp8_gemm_desc {
                          column_lanes = 1 being the 32x32b case: a thread holds 4
                          columns x 2 tokens and one warp-local transpose follows the
                          main loop).  The two give identical bits.                     */
-  int32_t fold;       /* K pieces stacked in the MMA's 128 rows: 1, 2 or 4.  A CTA then
+  int32_t fold;       /* K pieces stacked in the MMA's 128 rows: 1, 2, 4 or 8.  A CTA then
                          owns 128/fold output columns, its A operand holding fold
                          consecutive 128-wide K pieces of those weight rows and its B
                          operand the matching fold groups of 8 activation columns
@@ -109,10 +109,12 @@ typedef struct mxfp8_gemm_desc {
                          kept.  Each stage stays 16 KB of W and 4 MMAs; the grid has
                          fold times more CTAs, for shapes whose N/128 x split_k CTAs
                          leave SMs idle.  fold > 1 takes split_k 1, 2 or 4, acc_blocks
-                         4 and the 32x32b read-out.  0 = choose: the largest fold
-                         that keeps the grid within one CTA per SM and >= 1 full K
-                         piece per CTA (1 when those fields ask for what it cannot
-                         take).                                                         */
+                         4 and the 32x32b read-out; fold 8 takes split_k 1 and at most
+                         2 pipes (its accumulator ring holds 2 slots of 64 tensor-memory
+                         columns).  0 = choose: the largest fold that keeps the grid
+                         within one CTA per SM, pads K no further and leaves every
+                         split a stage (fold 8 only unsplit and from 8 stages per CTA;
+                         1 when the other fields ask for what folding cannot take).   */
   int32_t l2_prefetch_early;/* W stages past the ring that each of the first 70 % of
                          the grid's CTAs warms in L2 (l2_prefetch covers the rest).
                          Those launch while the previous kernel still streams, and

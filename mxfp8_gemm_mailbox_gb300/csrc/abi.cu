@@ -142,8 +142,14 @@ mxfp8_status check_desc(const mxfp8_gemm_desc* d) {
       d->tmem_load != MXFP8_TMEM_LOAD_16X256B)
     return fail(MXFP8_ERR_UNSUPPORTED,
                 "tmem_load must be MXFP8_TMEM_LOAD_32X32B or MXFP8_TMEM_LOAD_16X256B");
-  if (d->fold != 0 && d->fold != 1 && d->fold != 2 && d->fold != 4)
-    return fail(MXFP8_ERR_UNSUPPORTED, "fold must be 1, 2 or 4 (or 0 to choose)");
+  if (d->fold != 0 && d->fold != 1 && d->fold != 2 && d->fold != 4 && d->fold != 8)
+    return fail(MXFP8_ERR_UNSUPPORTED, "fold must be 1, 2, 4 or 8 (or 0 to choose)");
+  if (d->fold == 8) {
+    if (d->split_k > 1) return fail(MXFP8_ERR_UNSUPPORTED, "fold 8 takes split_k 1");
+    if (d->pipes == 4)
+      return fail(MXFP8_ERR_UNSUPPORTED,
+                  "fold 8 takes at most 2 pipes (its accumulator ring has 2 slots)");
+  }
   if (d->fold > 1) {
     if (d->split_k == 8)
       return fail(MXFP8_ERR_UNSUPPORTED, "fold > 1 takes split_k 1, 2 or 4");
@@ -223,13 +229,20 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
     int f = 1;
     const bool foldable = d->split_k <= 4 && d->acc_blocks == 4 &&
                           d->tmem_load == MXFP8_TMEM_LOAD_32X32B;
-    for (int cand : {2, 4})
+    for (int cand : {2, 4, 8}) {
+      // Fold 8 (unsplit, two pipes at most) pays from 8 stages per CTA on
+      // (measured on GB300, N=2048, S=1: K=4096 6.29 vs 6.00 us at fold 4,
+      // K=8192 7.86 vs 8.79, K=16384 11.46 vs 13.60).
+      if (cand == 8 && (d->split_k != 1 || d->pipes == 4 || k_tiles_for_fold(d->k, 8) < 8))
+        continue;
       if (foldable && tiles * d->split_k * cand <= lim.sms &&
           k_tiles_for_fold(d->k, cand) * cand == k_tiles1 &&  // no more K padding
           k_tiles_for_fold(d->k, cand) >= d->split_k)          // a full stage per split
         f = cand;
+    }
     d->fold = f;
   }
+  if (d->fold == 8 && d->split_k != 1) return fail(MXFP8_ERR_UNSUPPORTED, "fold 8 takes split_k 1");
   const int k_tiles = k_tiles_for_fold(d->k, d->fold);
   const int tps = (k_tiles + d->split_k - 1) / d->split_k;
   if (tps * d->fold > kMaxTilesPerSplit)
@@ -261,7 +274,8 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
   if (gemm_tmem_plan(d->stages, d->acc_blocks, d->fold).cols > kMaxTmemCols)
     return fail(MXFP8_ERR_UNSUPPORTED, "the requested stages do not fit in tensor memory");
   if (d->pipes == 0) {
-    d->pipes = (per_sm == 1 && d->stages % 4 == 0) ? 4 : (d->stages % 2 == 0 ? 2 : 1);
+    d->pipes = (per_sm == 1 && d->stages % 4 == 0 && d->fold != 8) ? 4
+               : (d->stages % 2 == 0 ? 2 : 1);
   } else if (d->stages % d->pipes != 0) {
     return fail(MXFP8_ERR_UNSUPPORTED, "pipes must divide stages (stage i and its ring slots "
                                        "belong to pipe i % pipes)");
@@ -367,7 +381,9 @@ mxfp8_status mxfp8_mailbox_init(void* mailbox, int32_t* stage_state, int32_t cap
 
 size_t mxfp8_publish_gemm_workspace_bytes(const mxfp8_gemm_desc* desc) {
   if (!desc || desc->n <= 0 || desc->n % kBlockN || desc->k <= 0 || desc->k % 32) return 0;
-  if (desc->fold != 0 && desc->fold != 1 && desc->fold != 2 && desc->fold != 4) return 0;
+  if (desc->fold != 0 && desc->fold != 1 && desc->fold != 2 && desc->fold != 4 &&
+      desc->fold != 8)
+    return 0;
   const int fold = sizing_fold(desc->fold);
   if (resolved_w_layout(desc->w_layout) != MXFP8_W_TILED)
     return scale_chunk_bytes(desc->n, desc->k, fold);

@@ -73,10 +73,13 @@ GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, in
   // W stage 1 (every ring has at least two stages).
   L.ctile = L.w;
   L.recv = L.w + kWTileBytes;
-  // One 128 fold-byte x scale chunk per stage, plus the 384 bytes the copy of
-  // the last chunk reads past it (rows that feed no kept column).
+  // One x scale chunk per stage (a 16-byte row per MMA column, two columns
+  // to a row past 32 columns: 128 fold bytes, 512 at fold 8), plus the 384
+  // bytes the copy of the last chunk reads past it (rows that feed no kept
+  // column).
   L.sx = L.sfa + stages * kSfChunkBytes;
-  const uint32_t sx_bytes = static_cast<uint32_t>(tiles_per_split * 128 * fold + 384);
+  const uint32_t sx_chunk = 16u * static_cast<uint32_t>(std::min(32, kRows * fold));
+  const uint32_t sx_bytes = static_cast<uint32_t>(tiles_per_split) * sx_chunk + 384u;
   L.bars = (L.sx + sx_bytes + 7u) & ~7u;
   L.misc = L.bars + static_cast<uint32_t>(2 * stages + 2 * kMaxAccRing + 2) * 8u;
   L.total = L.misc + 16u + 1024u;
@@ -88,9 +91,11 @@ TmemPlan gemm_tmem_plan(int stages, int acc_blocks, int fold) {
   t.acc = 0;
   const uint32_t block_cols = static_cast<uint32_t>(kRows * fold);  // one MMA's N
   t.acc_slot = acc_blocks == 1 ? kSfPerTile * block_cols : block_cols;
-  // 32-column slots (fold 4) come 4 to a ring, so the plan stays within 256
-  // columns.
-  t.acc_ring = (acc_blocks == 1 || fold == 4) ? 4u : static_cast<uint32_t>(kMaxAccRing);
+  // 32-column slots (fold 4) come 4 to a ring and 64-column ones (fold 8) 2,
+  // so the plan stays within 256 columns.
+  t.acc_ring = fold == 8 ? 2u
+               : (acc_blocks == 1 || fold == 4) ? 4u
+                                                : static_cast<uint32_t>(kMaxAccRing);
   t.sfa = t.acc + t.acc_slot * t.acc_ring;
   t.sfb = t.sfa + 4u * static_cast<uint32_t>(stages);
   const uint32_t used = t.sfb + 4u * static_cast<uint32_t>(stages);

@@ -1,6 +1,7 @@
 // The folded publishing GEMM kernels (F = 2 and 4 K pieces stacked in the
-// MMA's rows; 32x32b accumulator loads; split-K 1, 2 or 4), compiled apart
-// from the unfolded ones so the two translation units build in parallel.
+// MMA's rows with split-K 1, 2 or 4; F = 8 unsplit; 32x32b accumulator
+// loads), compiled apart from the unfolded ones so the two translation units
+// build in parallel.
 #include "publish_gemm_kernel.cuh"
 
 namespace mxfp8 {
@@ -40,6 +41,7 @@ cudaError_t launch_for_fold(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x
 cudaError_t set_folded_gemm_smem_attribute(int split_k, int fold, int bytes) {
   if (fold == 2) return set_for_fold<2>(split_k, bytes);
   if (fold == 4) return set_for_fold<4>(split_k, bytes);
+  if (fold == 8 && split_k == 1) return set_smem_impl<1, false, 8>(bytes);
   return cudaErrorInvalidValue;
 }
 
@@ -48,6 +50,8 @@ cudaError_t launch_folded_publish_gemm(const CUtensorMap& tmap_w, const CUtensor
   if (p.tmem_load == MXFP8_TMEM_LOAD_16X256B) return cudaErrorInvalidValue;
   if (p.fold == 2) return launch_for_fold<2>(tmap_w, tmap_x, p, split_k, stream);
   if (p.fold == 4) return launch_for_fold<4>(tmap_w, tmap_x, p, split_k, stream);
+  if (p.fold == 8 && split_k == 1 && p.pipes <= 2)
+    return launch_impl<1, false, 8>(tmap_w, tmap_x, p, stream);
   return cudaErrorInvalidValue;
 }
 

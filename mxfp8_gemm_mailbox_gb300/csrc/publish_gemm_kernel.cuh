@@ -168,12 +168,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     publish_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_x,
                         const __grid_constant__ GemmParams p) {
-  static_assert(F == 1 || F == 2 || F == 4, "the fold divides the 4 lane quarters");
+  static_assert(F == 1 || F == 2 || F == 4 || F == 8, "the fold divides the 128 MMA rows");
   static_assert(F == 1 || !kWideLoad, "folded tiles read accumulators with 32x32b");
   constexpr int kTileRows = kBlockN / F;                 // output columns of a CTA
   constexpr uint32_t kXStageBytes = kXTileBytes * F;     // F x tiles of 8 x 128 bytes
   constexpr uint32_t kStageTxBytes = kWTileBytes + kXStageBytes + kSfChunkBytes;
-  constexpr uint32_t kSxChunkBytes = 128u * F;           // x scale rows of one stage
+  // x scale chunk of one stage: a 16-byte row per MMA column, 32 rows at most
+  // (columns n and n + 32 share row n at fold 8).
+  constexpr int kScaleRows = kRows * F < 32 ? kRows * F : 32;
+  constexpr int kColsPerScaleRow = (kRows * F + 31) / 32;
+  constexpr uint32_t kSxChunkBytes = 16u * kScaleRows;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -417,41 +421,54 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const int arow = quarter * 32 + lane;    // MMA row = TMEM lane
     const int piece = F == 1 ? 0 : arow / kTileRows;     // the K piece this lane holds
     const int col = F == 1 ? arow : arow % kTileRows;    // output column within the tile
-    // The lane's diagonal block: columns [8 piece, 8 piece + 8) of a slot.
+    // The lane's diagonal block is columns [8 piece, 8 piece + 8) of a slot.
+    // A tensor-memory load takes one address for the whole warp: up to F = 4 a
+    // warp's 32 lanes hold one piece; at F = 8 they hold two (16 rows each),
+    // so the warp loads both blocks (16 columns) and each lane keeps its own.
+    constexpr int kPiecesPerWarp = F == 8 ? 2 : 1;
+    const int warp_piece = F == 1 ? 0 : (quarter * 32) / kTileRows;  // the warp's first piece
     const uint32_t lane_base =
-        (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(kRows * piece);
+        (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(kRows * warp_piece);
     ptx::grid_dependency_wait();
     if (etid == 0) misc[1] = ptx::ld_volatile_u32(p.state + 0);
 
-    // x scales of this CTA's K range as one 128 F-byte chunk per stage: MMA
-    // column r (< 8 F: token r % 8 of piece r / 8) of stage j at byte
-    // j * 128 F + r * 16, its four E8M0 codes first and 12 zero bytes after.
-    // Tokens >= m and blocks past K take 127 (a scale of 1; those x elements
-    // are zero).  The copy of a chunk reads 32 rows; rows 8 F..31 (the next
+    // x scales of this CTA's K range as one chunk per stage: MMA column r
+    // (token r % 8 of piece r / 8) at row r % 32 of stage j's chunk (byte
+    // j * kSxChunkBytes + (r % 32) * 16), its four E8M0 codes at bytes
+    // 4 (r / 32) .. +3 of the row (the 32x128b copy's layout: at fold 8 a
+    // row holds columns r and r + 32), the rest of the row zero.  Tokens >= m
+    // and blocks past K take 127 (a scale of 1; those x elements are zero).
+    // The copy of a chunk reads 32 rows; rows past the chunk (the next
     // chunks, or the tail) feed no kept column.  (Loading every word into
     // registers before any store measured 2-6 % slower per call than this
     // loop.)
     uint8_t* sx = smem + L.sx;
     const int kblocks = p.k / 32;
-    const int words = kRows * F * nkt;  // <= 8 x kMaxTilesPerSplit (host check)
+    const int words = kScaleRows * nkt;  // <= 8 x kMaxTilesPerSplit (host check)
     constexpr int kMaxWords = kRows * kMaxTilesPerSplit / 128;  // per thread
 #pragma unroll
     for (int it = 0; it < kMaxWords; ++it) {
       const int w = etid + it * 128;
       if (w >= words) break;
-      const int r = w / nkt;
-      const int j = w - r * nkt;
-      const int t = F == 1 ? r : r % kRows;
-      uint32_t v = 0x7F7F7F7Fu;
-      if (t < p.m) {
-        const int kb0 = ((kt_begin + j) * F + (F == 1 ? 0 : r / kRows)) * kSfPerTile;
-        const uint8_t* row = p.x_scale + static_cast<size_t>(t) * kblocks;
-        uint32_t b[kSfPerTile];
+      const int n0 = w / nkt;
+      const int j = w - n0 * nkt;
+      uint32_t v[2] = {0u, 0u};
 #pragma unroll
-        for (int q = 0; q < kSfPerTile; ++q) b[q] = kb0 + q < kblocks ? row[kb0 + q] : 127u;
-        v = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+      for (int n1 = 0; n1 < kColsPerScaleRow; ++n1) {
+        const int r = n0 + 32 * n1;
+        const int t = F == 1 ? r : r % kRows;
+        v[n1] = 0x7F7F7F7Fu;
+        if (t < p.m) {
+          const int kb0 = ((kt_begin + j) * F + (F == 1 ? 0 : r / kRows)) * kSfPerTile;
+          const uint8_t* row = p.x_scale + static_cast<size_t>(t) * kblocks;
+          uint32_t b[kSfPerTile];
+#pragma unroll
+          for (int q = 0; q < kSfPerTile; ++q) b[q] = kb0 + q < kblocks ? row[kb0 + q] : 127u;
+          v[n1] = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+        }
       }
-      *reinterpret_cast<uint4*>(sx + j * kSxChunkBytes + r * 16) = make_uint4(v, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(sx + j * kSxChunkBytes + n0 * 16) =
+          make_uint4(v[0], v[1], 0u, 0u);
     }
     ptx::fence_proxy_async_smem();  // the tensor-memory copy reads them
     ptx::mbar_arrive(bar_sfb);
@@ -518,6 +535,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 #pragma unroll
           for (int t = 0; t < kRows; ++t)
             two_sum_add(hi[t], lo[t], __uint_as_float(v[kb * 8 + t]));
+      } else if constexpr (kPiecesPerWarp == 2) {
+        uint32_t v[16];
+        ptx::tmem_ld_32x32b_x16(slot, v);
+        ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_acc_empty + 8u * r);
+        const bool second = piece != warp_piece;
+#pragma unroll
+        for (int t = 0; t < kRows; ++t)
+          two_sum_add(hi[t], lo[t], __uint_as_float(second ? v[kRows + t] : v[t]));
       } else {
         uint32_t v[8];
         ptx::tmem_ld_32x32b_x8(slot, v);

@@ -74,7 +74,9 @@ def test_workspace_bytes_folded(lib):
     assert lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(d)) == 4 * 512 + 4 * 16384
     d = _lib.GemmDesc(256, 640, 8, 1, 0, 0, 0, in_place, 0, 0, 0, 4)  # K pads to 1024
     assert lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(d)) == 8 * 2 * 512
-    for fold in (3, 8, -1):
+    d = _lib.GemmDesc(256, 1152, 8, 1, 0, 0, 0, tiled, 0, 0, 0, 8)  # 16 tiles, K pads to 2048
+    assert lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(d)) == 16 * 2 * 512 + 16 * 2 * 16384
+    for fold in (3, 16, -1):
         d = _lib.GemmDesc(256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 0, fold)
         assert lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(d)) == 0
 
@@ -107,7 +109,9 @@ def _create(lib, desc, w=0x1000, ws=0x2000, mb=0x3000, st=0x4000, work=0x5000, n
     ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 0, 3), _lib.ERR_UNSUPPORTED, "fold"),
     ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 0, 0, 65), _lib.ERR_UNSUPPORTED, "l2_prefetch_early"),
     ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 0, 0, -2), _lib.ERR_UNSUPPORTED, "l2_prefetch_early"),
-    ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 0, 8), _lib.ERR_UNSUPPORTED, "fold"),
+    ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 0, 16), _lib.ERR_UNSUPPORTED, "fold"),
+    ((256, 2048, 8, 2, 0, 0, 0, 0, 0, 0, 0, 8), _lib.ERR_UNSUPPORTED, "fold 8 takes split_k 1"),
+    ((256, 2048, 8, 1, 0, 0, 0, 0, 0, 4, 0, 8), _lib.ERR_UNSUPPORTED, "2 pipes"),
     ((256, 2048, 8, 8, 0, 0, 0, 0, 0, 0, 0, 2), _lib.ERR_UNSUPPORTED, "split_k 1, 2 or 4"),
     ((256, 256, 8, 1, 0, 0, 1, 0, 0, 0, 0, 2), _lib.ERR_UNSUPPORTED, "acc_blocks 4"),
     ((256, 256, 8, 1, 0, 0, 0, 0, 0, 0, 2, 4), _lib.ERR_UNSUPPORTED, "32x32b"),

@@ -6,8 +6,8 @@ against the oracle: C, the
 published mailbox words between the two kernels, the consumer's output, the
 state words and the reset mailbox.  Combinations the library refuses (a ring
 that does not fit, pipes that do not divide it, a fold with S = 8, one slot
-per MMA or the 16x256b read-out) must be refused on the host with
-MXFP8_ERR_UNSUPPORTED."""
+per MMA or the 16x256b read-out, fold 8 with S > 1 or 4 pipes) must be
+refused on the host with MXFP8_ERR_UNSUPPORTED."""
 import numpy as np
 import pytest
 import torch
@@ -34,7 +34,7 @@ def draw(rng):
         tmem_load=int(rng.choice([0, 1, 2])),
         l2_prefetch=int(rng.choice([-1, 0, 3])),
         capacity=int(rng.integers(m, 9)),
-        fold=int(rng.choice([0, 0, 1, 2, 4])),
+        fold=int(rng.choice([0, 0, 1, 2, 4, 8])),
         l2_prefetch_early=int(rng.choice([-1, 0, 0, 2, 12])),
     )
 
@@ -42,7 +42,7 @@ def draw(rng):
 def test_random_shapes_and_tactics(cuda):
     rng = np.random.default_rng(20261202)
     ran = refused = 0
-    for case in range(64):
+    for case in range(80):
         p = draw(rng)
         n, k, m, cap = p["n"], p["k"], p["m"], p["capacity"]
         w, ws, x, xs = synthetic.integer_operands(n, k, m, seed=case)
@@ -77,4 +77,4 @@ def test_random_shapes_and_tactics(cuda):
         assert mb.status()[0] == OK
         g.close()
         ran += 1
-    assert ran >= 30 and ran + refused == 64, (ran, refused)
+    assert ran >= 30 and ran + refused == 80, (ran, refused)

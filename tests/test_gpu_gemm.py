@@ -98,6 +98,41 @@ def test_normal_inputs_within_two_ulps(cuda, n, k, m, lo, hi, split_k, w_layout,
     assert (after == oracle.SENTINEL).all()
 
 
+@pytest.mark.parametrize("w_layout", [W_IN_PLACE, W_TILED])
+@pytest.mark.parametrize("pipes", [1, 2])
+@pytest.mark.parametrize("n,k,m", [(128, 1024, 8), (256, 4096, 5), (512, 8192, 3), (128, 96, 2),
+                                   (256, 1152, 4), (384, 2048, 1), (2048, 16384, 8)])
+def test_fold_eight(cuda, n, k, m, pipes, w_layout):
+    """Fold 8 (16-row tiles, 8 K pieces per stage, N = 64 MMAs, x-scale rows
+    holding two columns, a 2-slot accumulator ring): bit-exact on integer
+    inputs, within 2 ULP on N(0, 1) inputs, with the mailbox and consumer."""
+    w, ws, x, xs = synthetic.integer_operands(n, k, m, seed=800 + n + k + m)
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    mb = Mailbox(8, n)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=1, fold=8, pipes=pipes, w_layout=w_layout)
+    cfg = g.config()
+    assert (cfg["fold"], cfg["pipes"], cfg["grid_ctas"]) == (8, pipes, n // 16), cfg
+    c = torch.full((m, n), 0x7FFF, dtype=torch.int16, device="cuda")
+    for call in range(2):
+        g.run(dev(x), dev(xs), c)
+        out = mb.consume(m)
+        torch.cuda.synchronize()
+        assert (bits(c) == want).all(), f"C, call {call}"
+        assert (bits(out) == sanitized(want)).all(), f"consumer output, call {call}"
+    assert mb.status()[0] == OK and (mailbox_words(mb) == oracle.SENTINEL).all()
+    g.close()
+    wl = synthetic.Workload("f8", n, k, m, 1, exp_lo=-4, exp_hi=2, x_zero_fraction=0.01,
+                            seed=900 + n + k + m)
+    wn, wsn = synthetic.make_weights(wl)
+    xn, xsn = synthetic.make_activations(wl)
+    c2, between, sb, out2, after, state, cfg2 = run_chain(wn, wsn, xn, xsn, 1, fold=8,
+                                                          w_layout=w_layout)
+    assert cfg2["fold"] == 8
+    assert_bf16_close(c2, oracle.gemm_bf16(wn, wsn, xn, xsn), f"N={n} K={k} m={m} fold 8")
+    check_published(between, sb, c2, 8, n)
+    assert (out2 == sanitized(c2)).all()
+
+
 def test_split_k_results_agree(cuda):
     """Every split and fold: within tolerance of the oracle on N(0, 1)
     inputs, identical bits on integer inputs."""
@@ -154,8 +189,9 @@ def test_short_rings_over_a_long_k_loop(cuda, stages, fold):
 
 def test_default_pipes_divide_the_ring(cuda):
     """Grids of at most one CTA per SM get 4 pipes on a ring that is a
-    multiple of 4; the headline's two CTAs per SM get 2."""
-    for n, k, split, pipes in [(2048, 16384, 1, 4), (4096, 4096, 1, 4), (7168, 8192, 2, 4),
+    multiple of 4 (2 at fold 8, whose accumulator ring has 2 slots); the
+    headline's two CTAs per SM get 2."""
+    for n, k, split, pipes in [(2048, 16384, 1, 2), (4096, 4096, 1, 4), (7168, 8192, 2, 4),
                                (7168, 16384, 4, 2)]:
         w = torch.zeros((n, k), dtype=torch.uint8, device="cuda")
         ws = torch.full((n, k // 32), 127, dtype=torch.uint8, device="cuda")
@@ -167,11 +203,13 @@ def test_default_pipes_divide_the_ring(cuda):
 
 def test_default_fold(cuda):
     """The largest fold that keeps the grid within one CTA per SM, pads K no
-    further and leaves every split a stage; 1 where the tactic asks for what
+    further and leaves every split a stage (fold 8 only unsplit, from 8 stages
+    per CTA, and not with 4 pipes asked for); 1 where the tactic asks for what
     folding does not take (one slot per MMA, the 16x256b read-out, S = 8)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert sms >= 128
-    for n, k, split, extra, fold in [(4096, 4096, 1, {}, 4), (2048, 16384, 1, {}, 4),
+    for n, k, split, extra, fold in [(4096, 4096, 1, {}, 4), (2048, 16384, 1, {}, 8),
+                                     (2048, 4096, 1, {}, 4), (2048, 16384, 1, {"pipes": 4}, 4),
                                      (2048, 2048, 4, {}, 2), (7168, 8192, 2, {}, 1),
                                      (7168, 16384, 4, {}, 1), (4096, 4096, 1, {"acc_blocks": 1}, 1),
                                      (4096, 4096, 1, {"tmem_load": TMEM_LOAD_16X256B}, 1),

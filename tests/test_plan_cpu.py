@@ -37,7 +37,7 @@ def _k_tiles(k, fold):
 
 
 TACTICS = list(itertools.product([0, 1, 2, 4, 8], [0, 2, 3, 6, 12, 16], [0, 1, 4], [0, 1, 2, 4],
-                                 [0, 1, 2, 4], [0, TMEM_LOAD_16X256B]))
+                                 [0, 1, 2, 4, 8], [0, TMEM_LOAD_16X256B]))
 
 
 @pytest.mark.parametrize("n", [128, 256, 1024, 2048, 4096, 7168, 16384])
@@ -63,6 +63,10 @@ def test_every_plan_keeps_the_invariants(n):
                                  ("pipes", pipes), ("fold", fold)):
                 if asked:
                     assert p[field] == asked, where
+            if p["fold"] == 8:  # its accumulator ring has 2 slots
+                assert p["split_k"] == 1 and p["pipes"] <= 2, where
+                if fold == 0:  # chosen only from 8 stages per CTA
+                    assert _k_tiles(k, 8) >= 8, where
             if p["fold"] > 1:
                 assert p["split_k"] <= 4 and p["acc_blocks"] == 4, where
                 assert p["tmem_load"] == "32x32b", where
@@ -78,7 +82,7 @@ def test_every_plan_keeps_the_invariants(n):
 def test_refusals_match_create():
     bad = [dict(fold=2, split_k=8), dict(fold=4, acc_blocks=1), dict(fold=2, tmem_load=2),
            dict(fold=3), dict(split_k=3), dict(stages=6, pipes=4), dict(l2_prefetch_early=65),
-           dict(stages=1)]
+           dict(stages=1), dict(fold=8, split_k=2), dict(fold=8, pipes=4), dict(fold=8)]
     for kw in bad:
         with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED"):
             plan_gemm(1024, 4096, **kw)
