@@ -20,7 +20,7 @@
 // The pair is rounded once to BF16 (hi + lo taken exactly, from its FP32
 // bits).
 //
-// Folding (F = 1, 2 or 4).  A grid of N/128 x S CTAs leaves most SMs idle
+// Folding (F = 1, 2, 4 or 8).  A grid of N/128 x S CTAs leaves most SMs idle
 // on small shapes, and one SM streams at most about 70-120 GB/s.  With F > 1
 // a CTA owns 128/F output columns and stacks F consecutive 128-wide K pieces
 // of its weight rows in the MMA's 128 rows (rows [p R, (p+1) R) hold piece p,
@@ -28,7 +28,10 @@
 // piece p), so one stage is still 16 KB of W and 4 MMAs.  Of the 128 x 8F
 // product only the F diagonal blocks (rows of piece p, columns of group p)
 // are kept; the epilogue adds the F pieces of each output column.  The grid
-// has F times more CTAs for the same weight bytes and MMA count.
+// has F times more CTAs for the same weight bytes and MMA count.  At F = 8
+// (16-row tiles, unsplit only) a warp's 32 lanes span two pieces, while a
+// tensor-memory load takes one column address per warp: each warp loads both
+// pieces' columns and each lane keeps its own eight.
 //
 // Warp roles (pipes = 1, 2 or 4 per launch):
 //   warp 0      TMA producer: one lane per pipe, lane l taking stages
@@ -53,7 +56,7 @@
 //
 // The kernel template lives in this header so its instantiations can be
 // spread over translation units that compile in parallel: publish_gemm.cu
-// (F = 1) and publish_gemm_fold.cu (F = 2, 4).
+// (F = 1) and publish_gemm_fold.cu (F = 2, 4, 8).
 #pragma once
 #include <cuda_bf16.h>
 
