@@ -360,9 +360,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (lane == 0 && issuer < pipes) {
       // --------------------------------------------------------- MMA issuers
       // tcgen05 instructions cost their issuing thread a fixed time each
-      // (about 65 ns per stage of 2 copies, 4 MMAs and 2 commits), which caps
-      // one thread near 65 GB/s of weight, so issuer j < pipes takes stages
-      // j, j + pipes, ...
+      // (about 260 ns per 16 KB stage of 2 copies, 4 MMAs and 2 commits),
+      // which caps one thread near 65 GB/s of weight, so issuer j < pipes
+      // takes stages j, j + pipes, ...
       ptx::grid_dependency_wait();
       bool ok = true;
       if (nkt > 0) {
