@@ -433,9 +433,8 @@ def test_grid_of_two_waves(cuda):
     g.close()
 
 
-@pytest.mark.parametrize("fold", [1, 2, 4])
+@pytest.mark.parametrize("fold,split_k", [(1, 1), (2, 1), (4, 1), (8, 1), (1, 4), (2, 4), (4, 4)])
 @pytest.mark.parametrize("shift", [100, -100, 60])
-@pytest.mark.parametrize("split_k", [1, 4])
 def test_scale_exponents_near_the_e8m0_limits(cuda, shift, split_k, fold):
     """W's scales moved up by `shift` powers of two and x's down by as many
     (E8M0 codes from 27 to 228): every product, hence every output, is
@@ -565,8 +564,10 @@ def test_bad_next_generation_is_flagged(cuda, fold):
     assert mb.status()[0] == ERR_STATE
 
 
-@pytest.mark.parametrize("fold", [1, 0])
-@pytest.mark.parametrize("alpha,split_k", [(0.25, 1), (-1.7, 2), (3.0e-3, 4), (1.0, 4)])
+@pytest.mark.parametrize("fold,alpha,split_k",
+                         [(f, a, s) for f in (1, 0) for a, s in ((0.25, 1), (-1.7, 2), (3.0e-3, 4),
+                                                                 (1.0, 4))] +
+                         [(8, 0.25, 1), (8, -1.7, 1)])
 def test_global_scale(cuda, alpha, split_k, fold):
     wl = synthetic.Workload("alpha", 768, 4096, 6, split_k, exp_lo=-4, exp_hi=2, seed=91)
     w, ws = synthetic.make_weights(wl)
