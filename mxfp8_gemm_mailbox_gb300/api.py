@@ -24,12 +24,34 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(handle)
 
 
-def _bytes_tensor(t: torch.Tensor, name: str) -> torch.Tensor:
-    if t.element_size() != 1:
-        raise TypeError(f"{name} must hold one-byte codes (uint8 / float8), got {t.dtype}")
+def _on_device(t: torch.Tensor, name: str) -> None:
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
-    return t
+
+
+def _codes(t: torch.Tensor, name: str, cols: int, min_rows: int = 0) -> int:
+    """Checks a matrix of one-byte codes (E4M3 or E8M0) ``[rows][cols]`` with
+    at least ``min_rows`` rows; returns rows.  The kernels read rows x cols
+    bytes from its address, so a smaller tensor is refused here, where its
+    size is still known."""
+    if t.element_size() != 1:
+        raise TypeError(f"{name} must hold one-byte codes (uint8 / float8), got {t.dtype}")
+    if t.dim() != 2 or t.shape[1] != cols or t.shape[0] < min_rows:
+        raise ValueError(f"{name} must be [rows >= {min_rows}][{cols}], got {tuple(t.shape)}")
+    _on_device(t, name)
+    return t.shape[0]
+
+
+def _halves(t: torch.Tensor, name: str, min_rows: int, cols: int) -> int:
+    """Checks a matrix of two-byte values (BF16 bits) ``[rows][cols]`` with at
+    least ``min_rows`` rows, which the kernels write or read row by row;
+    returns rows."""
+    if t.element_size() != 2:
+        raise TypeError(f"{name} must hold two-byte values (bfloat16 / int16), got {t.dtype}")
+    if t.dim() != 2 or t.shape[1] != cols or t.shape[0] < min_rows:
+        raise ValueError(f"{name} must be [rows >= {min_rows}][{cols}], got {tuple(t.shape)}")
+    _on_device(t, name)
+    return t.shape[0]
 
 
 class Mailbox:
@@ -54,8 +76,9 @@ class Mailbox:
 
     def publish(self, c: torch.Tensor, stream=None) -> None:
         """The unfused path's standalone publish of C [m][n] BF16."""
+        m = _halves(c, "c", 0, self.n)
         check(_lib.load().mailbox_publish(_ptr(self.words), _ptr(self.state), self.capacity,
-                                          self.n, c.shape[0], _ptr(c), _stream(stream)),
+                                          self.n, m, _ptr(c), _stream(stream)),
               "mailbox_publish")
 
     def consume(self, m: int, out: torch.Tensor | None = None, timeout_ns: int = 0,
@@ -63,6 +86,7 @@ class Mailbox:
         """The consumer: [m][n] BF16 copied out of the active generation."""
         if out is None:
             out = torch.empty((m, self.n), dtype=torch.bfloat16, device=self.words.device)
+        _halves(out, "out", m, self.n)
         check(_lib.load().mailbox_consume(_ptr(self.words), _ptr(self.state), self.capacity,
                                           self.n, m, _ptr(out), timeout_ns, _stream(stream)),
               "mailbox_consume")
@@ -117,9 +141,12 @@ class PublishGemm:
                  l2_prefetch: int = 0, pipes: int = 0, tmem_load: int = 0, fold: int = 0,
                  l2_prefetch_early: int = 0, stream=None):
         lib = _lib.load()
-        _bytes_tensor(w, "w")
-        _bytes_tensor(w_scale, "w_scale")
+        if w.dim() != 2:
+            raise ValueError(f"w must be [N][K], got {tuple(w.shape)}")
         n, k = w.shape
+        _codes(w, "w", k)
+        if k % 32 == 0:  # other K are refused by the library below
+            _codes(w_scale, "w_scale", k // 32, min_rows=n)
         self.desc = GemmDesc(n, k, mailbox.capacity, split_k, 0, stages, acc_blocks, w_layout,
                              l2_prefetch, pipes, tmem_load, fold, l2_prefetch_early)
         ws_bytes = lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(self.desc))
@@ -152,7 +179,8 @@ class PublishGemm:
             stream=None) -> torch.Tensor | None:
         """One publishing GEMM on x [m][K]; writes C [m][N] BF16 into ``c`` if
         given.  Must be followed by exactly one ``mailbox.consume``."""
-        check(_lib.load().mxfp8_publish_gemm_run(self._handle, _ptr(x), _ptr(x_scale), x.shape[0],
+        m = self._rows(x, x_scale, c)
+        check(_lib.load().mxfp8_publish_gemm_run(self._handle, _ptr(x), _ptr(x_scale), m,
                                                  _ptr(c), _stream(stream)), "mxfp8_publish_gemm_run")
         return c
 
@@ -161,17 +189,27 @@ class PublishGemm:
         """``run`` with C = alpha * (W x); alpha a one-element float32 CUDA tensor."""
         if alpha is not None and (alpha.dtype != torch.float32 or not alpha.is_cuda):
             raise TypeError("alpha must be a float32 CUDA tensor")
+        m = self._rows(x, x_scale, c)
         check(_lib.load().mxfp8_publish_gemm_run_scaled(self._handle, _ptr(x), _ptr(x_scale),
-                                                        x.shape[0], _ptr(alpha), _ptr(c),
+                                                        m, _ptr(alpha), _ptr(c),
                                                         _stream(stream)),
               "mxfp8_publish_gemm_run_scaled")
         return c
 
     def run_unfused(self, x: torch.Tensor, x_scale: torch.Tensor, c: torch.Tensor,
                     stream=None) -> torch.Tensor:
-        check(_lib.load().mxfp8_gemm_run_unfused(self._handle, _ptr(x), _ptr(x_scale), x.shape[0],
+        m = self._rows(x, x_scale, c)
+        check(_lib.load().mxfp8_gemm_run_unfused(self._handle, _ptr(x), _ptr(x_scale), m,
                                                  _ptr(c), _stream(stream)), "mxfp8_gemm_run_unfused")
         return c
+
+    def _rows(self, x: torch.Tensor, x_scale: torch.Tensor, c: torch.Tensor | None) -> int:
+        """m, after checking x [m][K], x_scale [>= m][K/32] and C [>= m][N]."""
+        m = _codes(x, "x", self.k)
+        _codes(x_scale, "x_scale", self.k // 32, min_rows=m)
+        if c is not None:
+            _halves(c, "c", m, self.n)
+        return m
 
     def close(self) -> None:
         if getattr(self, "_handle", None):
@@ -209,6 +247,10 @@ class LamportGather:
                  stream=None) -> torch.Tensor:
         if out is None:
             out = torch.empty_like(inp)
+        _on_device(inp, "inp")
+        _on_device(out, "out")
+        if out.nbytes < inp.nbytes:
+            raise ValueError(f"out holds {out.nbytes} bytes, fewer than the input's {inp.nbytes}")
         check(_lib.load().lamport_all_gather(_ptr(self.words), _ptr(self.state), self.capacity,
                                              _ptr(inp), inp.nbytes, _ptr(out), timeout_ns,
                                              _stream(stream)), "lamport_all_gather")
@@ -239,13 +281,15 @@ class TaggedMailbox:
               "tagged_mailbox_init")
 
     def publish(self, c: torch.Tensor, tag: int, stream=None) -> None:
-        check(_lib.load().tagged_publish(_ptr(self.pairs), self.capacity, self.n, c.shape[0],
+        m = _halves(c, "c", 0, self.n)
+        check(_lib.load().tagged_publish(_ptr(self.pairs), self.capacity, self.n, m,
                                          _ptr(c), tag, _stream(stream)), "tagged_publish")
 
     def consume(self, m: int, tag: int, out: torch.Tensor | None = None, timeout_ns: int = 0,
                 stream=None) -> torch.Tensor:
         if out is None:
             out = torch.empty((m, self.n), dtype=torch.bfloat16, device=self.pairs.device)
+        _halves(out, "out", m, self.n)
         check(_lib.load().tagged_consume(_ptr(self.pairs), self.capacity, self.n, m, tag,
                                          _ptr(out), timeout_ns, _ptr(self.flags),
                                          _stream(stream)), "tagged_consume")
