@@ -144,6 +144,33 @@ def test_gemm_worked_examples_golden():
         assert (c == int(expect, 16)).all(), (k, wc, xc, hex(int(c[0, 0])))
 
 
+def _terms_operands(k, w_scales, x_scales, terms, n=128, m=2):
+    """W [n][k] and x [m][k] all zero but for the listed (k, w code, x code)
+    elements, identical in every row, with the listed per-block scale codes."""
+    w = np.zeros((n, k), np.uint8)
+    x = np.zeros((m, k), np.uint8)
+    for term in terms.split(","):
+        kk, wc, xc = term.split(":")
+        w[:, int(kk)] = int(wc, 16)
+        x[:, int(kk)] = int(xc, 16)
+    ws = np.tile(np.array([int(v, 16) for v in w_scales.split(",")], np.uint8), (n, 1))
+    xs = np.tile(np.array([int(v, 16) for v in x_scales.split(",")], np.uint8), (m, 1))
+    return w, ws, x, xs
+
+
+def test_gemm_rounds_the_exact_sum_once_golden():
+    """Sums just past a BF16 midpoint by less than half an FP32 ulp: the
+    product and the scaled product round the exact sum once, not via FP32."""
+    for k, wsc, xsc, terms, expect, expect_half, *_ in _rows("gemm_double_rounding.txt"):
+        w, ws, x, xs = _terms_operands(int(k), wsc, xsc, terms)
+        wd, xd = _decoded(w[:1], ws[:1])[0], _decoded(x[:1], xs[:1])[0]
+        exact = sum(Fraction(float(a)) * Fraction(float(b)) for a, b in zip(wd, xd))
+        assert _exact_bf16_rne(exact) == int(expect, 16)  # the fixture, from a library decode
+        assert (oracle.gemm_bf16(w, ws, x, xs) == int(expect, 16)).all(), (k, terms)
+        assert (oracle.gemm_bf16_scaled(w, ws, x, xs, 1.0) == int(expect, 16)).all(), (k, terms)
+        assert (oracle.gemm_bf16_scaled(w, ws, x, xs, 0.5) == int(expect_half, 16)).all(), (k, terms)
+
+
 @pytest.mark.parametrize("n,k,m", [(128, 32, 1), (128, 96, 3), (256, 256, 8), (128, 64, 5)])
 def test_gemm_matches_exact_rational_sum(n, k, m):
     wl = synthetic.Workload("exact", n, k, m, exp_lo=-6, exp_hi=3, seed=31 + k + m)

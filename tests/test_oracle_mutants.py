@@ -67,6 +67,15 @@ MUTANTS = {
     "gather leaves its slot": (
         "    out[i] = slot[i];\n    slot[i] = ORACLE_SENTINEL;",
         "    out[i] = slot[i];"),
+    "BF16 rounding through FP32 first": (
+        "double magnitude = fabs(value);",
+        "double magnitude = fabs((double)(float)value);"),
+    "C rounded through FP32": (
+        "for (size_t i = 0; i < (size_t)m * (size_t)n; ++i) c[i] = oracle_bf16_rne(acc[i]);",
+        "for (size_t i = 0; i < (size_t)m * (size_t)n; ++i) c[i] = oracle_bf16_rne((double)(float)acc[i]);"),
+    "global scale applied in FP32": (
+        "c[i] = oracle_bf16_rne((double)alpha * acc[i]);",
+        "c[i] = oracle_bf16_rne((double)(alpha * (float)acc[i]));"),
     "global scale dropped": (
         "c[i] = oracle_bf16_rne((double)alpha * acc[i]);",
         "c[i] = oracle_bf16_rne(acc[i]);"),
@@ -87,6 +96,7 @@ PINS = [
     pins.test_bf16_rounding_golden,
     pins.test_clear_negative_zero,
     pins.test_gemm_worked_examples_golden,
+    pins.test_gemm_rounds_the_exact_sum_once_golden,
     lambda: pins.test_gemm_matches_exact_rational_sum(128, 96, 3),
     pins.test_gemm_fp64_matches_library_matmul,
     pins.test_gemm_integer_inputs_exact,
