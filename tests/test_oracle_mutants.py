@@ -76,6 +76,24 @@ MUTANTS = {
     "global scale applied in FP32": (
         "c[i] = oracle_bf16_rne((double)alpha * acc[i]);",
         "c[i] = oracle_bf16_rne((double)(alpha * (float)acc[i]));"),
+    "E8M0 bias 128": (
+        "return ldexp(1.0, (int)code - 127);",
+        "return ldexp(1.0, (int)code - 128);"),
+    "E4M3 NaN code read as a number": (
+        "if (exponent == 15 && mantissa == 7) return NAN;",
+        "if (exponent == 16 && mantissa == 7) return NAN;"),
+    "publish into the active generation": (
+        "  int g = state[0];\n  if (g < 0 || g >= ORACLE_GENERATIONS) return ORACLE_ERR_STATE;\n"
+        "  int half_n = n / 2;\n  for (int t = 0; t < m; ++t)\n    for (int w = 0; w < half_n; ++w) {\n"
+        "      uint32_t low",
+        "  int g = state[1];\n  if (g < 0 || g >= ORACLE_GENERATIONS) return ORACLE_ERR_STATE;\n"
+        "  int half_n = n / 2;\n  for (int t = 0; t < m; ++t)\n    for (int w = 0; w < half_n; ++w) {\n"
+        "      uint32_t low"),
+    "consume swaps the halves it copies out": (
+        "      out[(size_t)t * n + 2 * w] = (uint16_t)(word & 0xFFFF);\n"
+        "      out[(size_t)t * n + 2 * w + 1] = (uint16_t)(word >> 16);",
+        "      out[(size_t)t * n + 2 * w] = (uint16_t)(word >> 16);\n"
+        "      out[(size_t)t * n + 2 * w + 1] = (uint16_t)(word & 0xFFFF);"),
     "global scale dropped": (
         "c[i] = oracle_bf16_rne((double)alpha * acc[i]);",
         "c[i] = oracle_bf16_rne(acc[i]);"),
