@@ -94,6 +94,9 @@ MUTANTS = {
         "      out[(size_t)t * n + 2 * w + 1] = (uint16_t)(word >> 16);",
         "      out[(size_t)t * n + 2 * w] = (uint16_t)(word >> 16);\n"
         "      out[(size_t)t * n + 2 * w + 1] = (uint16_t)(word & 0xFFFF);"),
+    "sampled outputs read activation row 0": (
+        "x + (size_t)t * k, x_scale + (size_t)t * blocks));",
+        "x + (size_t)0 * k, x_scale + (size_t)0 * blocks));"),
     "global scale dropped": (
         "c[i] = oracle_bf16_rne((double)alpha * acc[i]);",
         "c[i] = oracle_bf16_rne(acc[i]);"),
@@ -122,6 +125,7 @@ PINS = [
     pins.test_publish_layout_and_sanitisation,
     pins.test_chain_state_sequence_and_reset,
     pins.test_scaled_gemm_closed_forms,
+    pins.test_gemm_sample_matches_full,
     gather_pins.test_gather_worked_examples_golden,
     gather_pins.test_gather_sequence_of_alternating_sizes,
     tagged_pins.test_pair_layout_and_unchanged_bits,
