@@ -1,9 +1,10 @@
 """The tactic resolver on the CPU, through mxfp8_publish_gemm_plan: the plans
 of the benchmarked workloads on GB300's limits, the invariants every plan
 keeps over a grid of shapes and tactics (tensor memory within half an SM,
-shared memory within a CTA's limit, at most two CTAs of a clustered launch
-per SM, pipes dividing the ring, folding only where it is taken and pads K no
-further), the refusals, and how the fold follows the SM count."""
+shared memory within a CTA's limit and covering every region the kernel
+addresses, at most two CTAs of a clustered launch per SM, pipes dividing the
+ring, folding only where it is taken and pads K no further), the refusals,
+and how the fold follows the SM count."""
 import itertools
 
 import pytest
@@ -36,6 +37,32 @@ def _k_tiles(k, fold):
     return -(-k // (128 * fold))
 
 
+def _kernel_smem_need(plan, k):
+    """Shared memory the kernel addresses for a plan, from its layout: the W,
+    x and W-scale rings, the x-scale staging (a 16-byte row per MMA column,
+    32 rows at most, per K tile of the split, plus the 384 bytes a 32-row
+    copy of the last 128-byte chunk reads past it), 2 barriers per stage, 2
+    per accumulator slot (8 at most) and 2 more, 16 bytes of words, and 1 KB
+    to align the base to the 128-byte swizzle's 1024-byte period."""
+    f, s, st = plan["fold"], plan["split_k"], plan["stages"]
+    tps = -(-_k_tiles(k, f) // s)
+    rings = st * (16384 + 1024 * f + 512)
+    staging = tps * 16 * min(8 * f, 32) + 384
+    return rings + staging + (2 * st + 2 * 8 + 2) * 8 + 16 + 1024
+
+
+def _epilogue_fits_the_dead_ring(plan):
+    """After the main loop the epilogue reuses the W ring: W stage 0 holds the
+    BF16 tile (below 4 KB) and, folded, the parked pairs (8 KB from 4 KB);
+    W stage 1 the split-K receive buffer."""
+    f, s = plan["fold"], plan["split_k"]
+    shard, rows = 8 // s, 128 // f
+    run = min(8 // f, shard) if f > 1 else shard
+    recv = (s - 1) * (128 if f > 1 else rows) * run * 8
+    return (plan["stages"] >= 2 and shard * rows * 2 <= 4096 and 4096 + 128 * 8 * 8 <= 16384
+            and recv <= 16384)
+
+
 TACTICS = list(itertools.product([0, 1, 2, 4, 8], [0, 2, 3, 6, 12, 16], [0, 1, 4], [0, 1, 2, 4],
                                  [0, 1, 2, 4, 8], [0, TMEM_LOAD_16X256B]))
 
@@ -57,6 +84,10 @@ def test_every_plan_keeps_the_invariants(n):
             assert p["smem_bytes"] <= SMEM_OPTIN, where
             assert p["stages"] % p["pipes"] == 0, where
             assert p["grid_ctas"] == n // (128 // p["fold"]) * p["split_k"], where
+            assert p["smem_bytes"] >= _kernel_smem_need(p, k), where
+            assert _epilogue_fits_the_dead_ring(p), where
+            # the epilogue stages at most 16 x-scale words per thread (128 threads)
+            assert min(8 * p["fold"], 32) * -(-_k_tiles(k, p["fold"]) // p["split_k"]) <= 2048, where
             if p["split_k"] > 1:  # at most two CTAs of a clustered launch on an SM
                 assert 3 * (p["smem_bytes"] + 1024) > SMEM_PER_SM, where
             for field, asked in (("split_k", split), ("stages", stages), ("acc_blocks", acc),
