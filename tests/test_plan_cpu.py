@@ -86,6 +86,14 @@ def test_every_plan_keeps_the_invariants(n):
             assert p["grid_ctas"] == n // (128 // p["fold"]) * p["split_k"], where
             assert p["smem_bytes"] >= _kernel_smem_need(p, k), where
             assert _epilogue_fits_the_dead_ring(p), where
+            # tensor memory: the accumulator ring (slots of 8 x fold columns, or
+            # 32 with one slot per MMA; 2 slots at fold 8, 4 at fold 4 or one
+            # per MMA, else 8) and a 4-column W-scale and x-scale slot per stage
+            f = p["fold"]
+            slot = 32 if p["acc_blocks"] == 1 else 8 * f
+            ring = 2 if f == 8 else 4 if (f == 4 or p["acc_blocks"] == 1) else 8
+            assert p["tmem_columns"] >= slot * ring + 8 * p["stages"], where
+            assert p["tmem_columns"] in (32, 64, 128, 256), where
             # the epilogue stages at most 16 x-scale words per thread (128 threads)
             assert min(8 * p["fold"], 32) * -(-_k_tiles(k, p["fold"]) // p["split_k"]) <= 2048, where
             if p["split_k"] > 1:  # at most two CTAs of a clustered launch on an SM
