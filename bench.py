@@ -7,13 +7,20 @@ weight-stream bandwidth: (N*K + N*K/32) bytes per call / time per call.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Timed region: K steps replayed from CUDA graphs of chained calls that rotate
-through enough weight copies (3 x 121 MB > 2 x the 129 MB L2) that every
-call streams its weight from HBM; CUDA events on the launching stream,
-barrier + synchronize on both sides, max over ranks.  Under torchrun every
-rank runs an independent replica on its own GPU (the path does not shard);
-``value`` is the weight bytes all ranks streamed / the slowest rank's time.
-The reference arm times the CPU oracle on a bounded sample of the workload.
+Timed region: exactly W untimed steps, then exactly K steps, replayed from
+CUDA graphs of chained calls that rotate through enough weight copies (more
+than 12 x the 129 MB L2) that every call streams its weight from HBM; CUDA
+events on the launching stream, barrier + synchronize on both sides, max
+over ranks.  nvidia-smi samples the clocks from the timed region through at
+least two seconds of the same calls right after it, while the CPU baseline
+(the oracle on the host cores) runs.  The same line reports the GEMM alone
+(the roofline), the end-to-end figure from pinned host buffers, and the
+other workloads of the path (N=7168 K=8192 m=8 S=2, N=4096 K=4096 m=4 S=1,
+N=256 K=256 m=1 S=1), each with its own weight rotation.
+Under torchrun every rank runs an independent replica on its own GPU (the
+path does not shard); ``value`` is the weight bytes all ranks streamed / the
+slowest rank's time.  The reference arm times the CPU oracle on a bounded
+sample of the workload.
 """
 from __future__ import annotations
 
@@ -43,12 +50,16 @@ WORKLOAD_CHOICES = {"headline": "HEADLINE", "graph": "GRAPH_8192", "chain": "CHA
                     "tiny": "TINY"}
 _WORKLOAD = "headline"
 GRAPH_STEPS = 30  # calls per captured graph (a multiple of every weight-copy count)
+SOAK_SECONDS = 2.0  # least time the clocks are sampled under the chain's load
+WORKLOAD_CALLS = 6000  # timed calls of each other workload in the headline's line
 E2E_GRAPH_STEPS = 480  # end-to-end steps per captured graph (likewise)
 E2E_BATCH = 30         # end-to-end steps per wait on the input copies (divides E2E_GRAPH_STEPS)
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("mxfp8_gemm_mailbox_gb300/csrc/publish_gemm_kernel.cuh",
                   "mxfp8_gemm_mailbox_gb300/csrc/publish_gemm.cu",
-                  "mxfp8_gemm_mailbox_gb300/csrc/ptx.cuh")
+                  "mxfp8_gemm_mailbox_gb300/csrc/publish_gemm_fold.cu",
+                  "mxfp8_gemm_mailbox_gb300/csrc/ptx.cuh",
+                  "mxfp8_gemm_mailbox_gb300/csrc/abi.cu")
 TRAFFIC_FILE = ROOT / "profiles" / "publish_gemm_headline_traffic.json"
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -62,7 +73,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=300)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
-                   help="budget of the oracle CPU-baseline sample")
+                   help="budget of the oracle CPU-baseline sample (0: skip it)")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="leave the other workloads out of the headline's line")
     p.add_argument("--workload", choices=tuple(WORKLOAD_CHOICES), default="headline",
                    help="the chain's workload: headline N=7168 K=16384 m=8 S=4 (default), "
                         "graph N=7168 K=8192 m=8 S=2, chain N=4096 K=4096 m=4 S=1, "
@@ -307,140 +320,190 @@ def oracle_baseline_all_cores(seconds_budget: float, columns: int = 1024):
 
 
 # -------------------------------------------------------------- our arm
-def run_ours(args):
-    import numpy as np
-    import torch
+class Chain:
+    """The chained calls of one workload (publishing GEMM, then the PDL
+    consumer), rotating through enough weight copies that every call streams
+    its weight from HBM: the copies, one handle each, one mailbox, and CUDA
+    graphs of GRAPH_STEPS chained calls (plus graphs of fewer calls, captured
+    on demand, so any step count can be issued exactly)."""
 
-    world, rank, local = dist_env()
-    group = False
-    if world > 1:
-        import torch.distributed as dist
+    def __init__(self, wl, device, stream):
+        import torch
 
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-        group = True
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
+        import mxfp8_gemm_mailbox_gb300 as mx
+        import synthetic
 
-    import mxfp8_gemm_mailbox_gb300 as mx
-    import synthetic
-
-    wl = workload()
-    w, ws = synthetic.make_weights(wl)
-    x, xs = synthetic.make_activations(wl)
-    W0 = torch.from_numpy(w).to(device)
-    WS = torch.from_numpy(ws).to(device)
-    X = torch.from_numpy(x).to(device)
-    XS = torch.from_numpy(xs).to(device)
-    copies = weight_copies(wl.weight_bytes)
-    weights = [W0] + [W0.clone() for _ in range(copies - 1)]
-    mb = mx.Mailbox(wl.capacity, wl.n, device=device)
-    gemms = [mx.PublishGemm(Wc, WS, mb, split_k=wl.split_k) for Wc in weights]
-    cfg = gemms[0].config()
-    for g in gemms:
-        g.precompile(wl.m)
-    out = torch.empty((wl.m, wl.n), dtype=torch.bfloat16, device=device)
-    stream = torch.cuda.Stream(device=device)
-
-    # Graphs of GRAPH_STEPS chained calls rotating through the weight copies.
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        for i in range(copies):  # eager warm-up before capture
-            gemms[i].run(X, XS)
-            mb.consume(wl.m, out)
-        stream.synchronize()
-        with torch.cuda.graph(graph, stream=stream):
-            for i in range(GRAPH_STEPS):
-                gemms[i % copies].run(X, XS)
-                mb.consume(wl.m, out)
-    replays = max(1, -(-args.steps // GRAPH_STEPS))
-    steps = replays * GRAPH_STEPS
-    warm = max(1, -(-max(args.warmup, 3) // GRAPH_STEPS))
-
-    with torch.cuda.stream(stream):
-        for _ in range(warm):
-            graph.replay()
-    stream.synchronize()
-    barrier(group)
-    torch.cuda.synchronize(device)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
+        self.wl, self.device, self.stream = wl, device, stream
+        w, ws = synthetic.make_weights(wl)
+        x, xs = synthetic.make_activations(wl)
+        self.host_x, self.host_xs = x, xs
+        W0 = torch.from_numpy(w).to(device)
+        WS = torch.from_numpy(ws).to(device)
+        self.X = torch.from_numpy(x).to(device)
+        self.XS = torch.from_numpy(xs).to(device)
+        self.copies = weight_copies(wl.weight_bytes)
+        weights = [W0] + [W0.clone() for _ in range(self.copies - 1)]
+        self.mb = mx.Mailbox(wl.capacity, wl.n, device=device)
+        self.gemms = [mx.PublishGemm(Wc, WS, self.mb, split_k=wl.split_k) for Wc in weights]
+        self.cfg = self.gemms[0].config()
+        for g in self.gemms:
+            g.precompile(wl.m)
+        self.out = torch.empty((wl.m, wl.n), dtype=torch.bfloat16, device=device)
         with torch.cuda.stream(stream):
-            e0.record(stream)
+            for i in range(self.copies):  # eager: every handle's first run before capture
+                self.gemms[i].run(self.X, self.XS)
+                self.mb.consume(wl.m, self.out)
+        stream.synchronize()
+        self._graphs = {}
+
+    def graph(self, steps: int):
+        """The captured graph of `steps` chained calls (steps <= GRAPH_STEPS)."""
+        import torch
+
+        if steps not in self._graphs:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(self.stream):
+                with torch.cuda.graph(graph, stream=self.stream):
+                    for i in range(steps):
+                        self.gemms[i % self.copies].run(self.X, self.XS)
+                        self.mb.consume(self.wl.m, self.out)
+            self._graphs[steps] = graph
+        return self._graphs[steps]
+
+    def prepare(self, *step_counts):
+        """Captures every graph that issue() will need for these counts."""
+        self.graph(GRAPH_STEPS)
+        for n in step_counts:
+            if n % GRAPH_STEPS:
+                self.graph(n % GRAPH_STEPS)
+
+    def issue(self, steps: int):
+        """Exactly `steps` chained calls on the stream, from the graphs."""
+        import torch
+
+        whole, rest = divmod(steps, GRAPH_STEPS)
+        with torch.cuda.stream(self.stream):
+            for _ in range(whole):
+                self.graph(GRAPH_STEPS).replay()
+            if rest:
+                self.graph(rest).replay()
+
+    def timed(self, steps: int) -> float:
+        """Seconds of `steps` chained calls between CUDA events on the stream."""
+        import torch
+
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        self.issue(steps)
+        e1.record(self.stream)
+        self.stream.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+
+    def soak(self, min_seconds: float, until=None):
+        """Whole graphs back to back for at least `min_seconds` and until
+        `until()` is false, at most 64 replays in flight.  Returns (calls,
+        seconds) between CUDA events."""
+        import torch
+
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        marks = []
+        replays = 0
+        t0 = time.perf_counter()
+        e0.record(self.stream)
+        with torch.cuda.stream(self.stream):
+            while (time.perf_counter() - t0 < min_seconds or (until is not None and until())
+                   or replays == 0):
+                self.graph(GRAPH_STEPS).replay()
+                replays += 1
+                ev = torch.cuda.Event()
+                ev.record(self.stream)
+                marks.append(ev)
+                if len(marks) > 64:
+                    marks.pop(0).synchronize()
+        e1.record(self.stream)
+        self.stream.synchronize()
+        return replays * GRAPH_STEPS, e0.elapsed_time(e1) / 1e3
+
+    def gemm_back_to_back_us(self, launches: int, warm: int = 3) -> float:
+        """The publishing GEMM alone (publish off: the same kernel, no consume
+        needed), GRAPH_STEPS launches per graph over the rotating weights."""
+        import torch
+
+        cbuf = torch.empty((self.wl.m, self.wl.n), dtype=torch.bfloat16, device=self.device)
+        graph = torch.cuda.CUDAGraph()
+        replays = max(1, launches // GRAPH_STEPS)
+        with torch.cuda.stream(self.stream):
+            with torch.cuda.graph(graph, stream=self.stream):
+                for i in range(GRAPH_STEPS):
+                    self.gemms[i % self.copies].run_unfused(self.X, self.XS, cbuf)
+            for _ in range(warm):
+                graph.replay()
+            g0 = torch.cuda.Event(enable_timing=True)
+            g1 = torch.cuda.Event(enable_timing=True)
+            g0.record(self.stream)
             for _ in range(replays):
                 graph.replay()
-            e1.record(stream)
-        stream.synchronize()
-    barrier(group)
-    torch.cuda.synchronize(device)
-    local_s = e0.elapsed_time(e1) / 1e3
-    if args.profile_graph:
-        # One more replay of the timed graph between the CUDA profiler's start
-        # and stop, for `ncu --profile-from-start off --graph-profiling graph`:
-        # the DRAM bytes of GRAPH_STEPS whole chained calls.
-        torch.cuda.profiler.start()
-        with torch.cuda.stream(stream):
-            graph.replay()
-        stream.synchronize()
-        torch.cuda.profiler.stop()
-    seconds, bytes_all = aggregate(local_s, float(steps * wl.weight_bytes), group)
-    us_per_call = seconds / steps * 1e6
-    value = bytes_all / seconds / 1e9
+            g1.record(self.stream)
+        self.stream.synchronize()
+        return g0.elapsed_time(g1) * 1e3 / (replays * GRAPH_STEPS)
 
-    # The dominant kernel, the publishing GEMM: launched back to back from a
-    # CUDA graph of GRAPH_STEPS launches over the same rotating weights, with
-    # its publish switched off (the same kernel; the mailbox protocol needs a
-    # consume after every publish), between CUDA events on its stream.
-    cbuf = torch.empty((wl.m, wl.n), dtype=torch.bfloat16, device=device)
-    gemm_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(gemm_graph, stream=stream):
-            for i in range(GRAPH_STEPS):
-                gemms[i % copies].run_unfused(X, XS, cbuf)
-        for _ in range(warm):
-            gemm_graph.replay()
-        g0 = torch.cuda.Event(enable_timing=True)
-        g1 = torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(replays):
-            gemm_graph.replay()
-        g1.record(stream)
-    stream.synchronize()
-    gemm_us = g0.elapsed_time(g1) * 1e3 / steps
-    # The same kernel launched alone (events around each launch: no overlap
-    # with its neighbours, so launch and ramp-up are included).
-    n_iso = min(300, steps)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_iso)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_iso)]
-    with torch.cuda.stream(stream):
-        for i in range(n_iso):
-            starts[i].record(stream)
-            gemms[i % copies].run(X, XS)
-            ends[i].record(stream)
-            mb.consume(wl.m, out)
-    stream.synchronize()
-    iso_us = statistics.mean(a.elapsed_time(b) * 1e3 for a, b in zip(starts, ends))
-    peak, peak_kind = measured_peak()
-    achieved = wl.weight_bytes / (gemm_us * 1e-6) / 1e9
+    def isolated_us(self, launches: int) -> float:
+        """The GEMM launched alone: CUDA events around each launch, so launch
+        and ramp-up are included; each followed by its consume."""
+        import torch
 
-    # End to end through the public API from pinned host buffers.  Every
-    # step copies its own x and x scales in (one stream) and its output out
-    # (another stream).  An event edge inside the chain of kernels cuts the
-    # programmatic launch between a consumer and the next GEMM (about 6 us
-    # per step, measured), so the compute stream waits on the input copies
-    # once per batch of E2E_BATCH steps: batch j+1's inputs land while batch
-    # j computes, each step's output copy forks off right after its consumer.
-    hx = torch.from_numpy(x).pin_memory()
-    hxs = torch.from_numpy(xs).pin_memory()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(launches)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(launches)]
+        with torch.cuda.stream(self.stream):
+            for i in range(launches):
+                starts[i].record(self.stream)
+                self.gemms[i % self.copies].run(self.X, self.XS)
+                ends[i].record(self.stream)
+                self.mb.consume(self.wl.m, self.out)
+        self.stream.synchronize()
+        return statistics.mean(a.elapsed_time(b) * 1e3 for a, b in zip(starts, ends))
+
+    def check(self):
+        import mxfp8_gemm_mailbox_gb300 as mx
+
+        status, words = self.mb.status(self.stream)
+        if status != mx.OK:
+            raise RuntimeError(f"mailbox status {status} after the run: state {words}")
+
+    def close(self):
+        for g in self.gemms:
+            g.close()
+        self.gemms = []
+        self._graphs = {}
+
+
+def end_to_end(chain, steps: int):
+    """The same chain through the public API from pinned host buffers: every
+    step copies its own x and x scales in (one stream) and its output out
+    (another stream).  An event edge inside the chain of kernels cuts the
+    programmatic launch between a consumer and the next GEMM (about 6 us per
+    step, measured), so the compute stream waits on the input copies once per
+    batch of E2E_BATCH steps: batch j+1's inputs land while batch j computes,
+    and each step's output copy forks off right after its consumer.  The
+    per-step host work (about twenty launches and stream operations) would
+    dominate, so E2E_GRAPH_STEPS steps are captured once and replayed; every
+    replay still copies every step's inputs in and its output back.  Returns
+    (seconds, steps, h2d bytes per step, d2h bytes per step)."""
+    import torch
+
+    wl, device, stream = chain.wl, chain.device, chain.stream
+    hx = torch.from_numpy(chain.host_x).pin_memory()
+    hxs = torch.from_numpy(chain.host_xs).pin_memory()
     nbuf = 2 * E2E_BATCH
     houts = [torch.empty((wl.m, wl.n), dtype=torch.bfloat16).pin_memory() for _ in range(nbuf)]
-    dXs = [torch.empty_like(X) for _ in range(nbuf)]
-    dXSs = [torch.empty_like(XS) for _ in range(nbuf)]
-    outs = [torch.empty_like(out) for _ in range(nbuf)]
+    dXs = [torch.empty_like(chain.X) for _ in range(nbuf)]
+    dXSs = [torch.empty_like(chain.XS) for _ in range(nbuf)]
+    outs = [torch.empty_like(chain.out) for _ in range(nbuf)]
     h2d_stream = torch.cuda.Stream(device=device)
     d2h_stream = torch.cuda.Stream(device=device)
-    n_e2e = min(3000, steps)
+    gemms, copies, mb = chain.gemms, chain.copies, chain.mb
 
     def e2e_steps(count):
         k = E2E_BATCH
@@ -481,10 +544,6 @@ def run_ours(args):
             with torch.cuda.stream(d2h_stream):
                 read[j].record(d2h_stream)
 
-    # The per-step host work (about twenty launches and stream operations)
-    # would dominate, so the pipeline of GRAPH_STEPS steps is captured once
-    # and replayed; every replay still copies every step's inputs in from
-    # pinned host memory and its output back.
     e2e_steps(4)
     torch.cuda.synchronize(device)
     e2e_graph = torch.cuda.CUDAGraph()
@@ -494,8 +553,7 @@ def run_ours(args):
         e2e_steps(E2E_GRAPH_STEPS)
         stream.wait_stream(h2d_stream)
         stream.wait_stream(d2h_stream)
-    e2e_replays = max(1, n_e2e // E2E_GRAPH_STEPS)
-    n_e2e = e2e_replays * E2E_GRAPH_STEPS
+    replays = max(1, steps // E2E_GRAPH_STEPS)
     with torch.cuda.stream(stream):
         for _ in range(2):
             e2e_graph.replay()
@@ -504,36 +562,148 @@ def run_ours(args):
     f1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         f0.record(stream)
-        for _ in range(e2e_replays):
+        for _ in range(replays):
             e2e_graph.replay()
         f1.record(stream)
     stream.synchronize()
-    if not torch.equal(houts[(E2E_GRAPH_STEPS - 1) % nbuf], outs[(E2E_GRAPH_STEPS - 1) % nbuf].cpu()):
+    last = (E2E_GRAPH_STEPS - 1) % nbuf
+    if not torch.equal(houts[last], outs[last].cpu()):
         raise RuntimeError("the end-to-end output read back differs from the device copy")
-    e2e_s, e2e_bytes = aggregate(f0.elapsed_time(f1) / 1e3, float(n_e2e * wl.weight_bytes), group)
-    status, words = mb.status(stream)
-    if status != mx.OK:
-        raise RuntimeError(f"mailbox status {status} after the run: state {words}")
+    h2d = int(chain.X.numel() + chain.XS.numel())
+    d2h = int(chain.out.numel() * chain.out.element_size())
+    return f0.elapsed_time(f1) / 1e3, replays * E2E_GRAPH_STEPS, h2d, d2h
 
-    cpu = None
-    if rank == 0 and world == 1:
-        gbs, calls, secs, sample = oracle_baseline(args.cpu_seconds)
-        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": sample, "seconds": round(secs, 2)}
-        agbs, threads, acalls, asecs = oracle_baseline_all_cores(args.cpu_seconds / 2)
-        cpu["all_cores"] = {"value": round(agbs, 4), "unit": UNIT, "cores": threads,
-                            "sample": f"{acalls} calls of the same chain on the same slice, "
-                                      f"one thread per core, over {asecs:.1f} s"}
+
+def workload_entry(wl, device, stream, peak: float, calls: int = WORKLOAD_CALLS) -> dict:
+    """µs per call, weight-stream GB/s and roofline fraction of one workload's
+    chain, with its own weight rotation, plus the GEMM alone back to back."""
+    import torch
+
+    chain = Chain(wl, device, stream)
+    try:
+        chain.prepare(calls)
+        chain.issue(10 * GRAPH_STEPS)  # warm-up
+        seconds = chain.timed(calls)
+        gemm_us = chain.gemm_back_to_back_us(calls)
+        chain.check()
+        us = seconds / calls * 1e6
+        gbs = wl.weight_bytes / (us * 1e-6) / 1e9
+        gemm_gbs = wl.weight_bytes / (gemm_us * 1e-6) / 1e9
+        cfg = chain.cfg
+        return {
+            "workload": f"N={wl.n} K={wl.k} m={wl.m} S={wl.split_k}",
+            "us_per_call": round(us, 3),
+            "gbs": round(gbs, 1),
+            "frac": round(gbs / peak, 4),
+            "gemm_us": round(gemm_us, 3),
+            "gemm_gbs": round(gemm_gbs, 1),
+            "gemm_frac": round(gemm_gbs / peak, 4),
+            "calls": calls,
+            "weight_bytes_per_call": wl.weight_bytes,
+            "weight_copies": chain.copies,
+            "l2": rotation_note(chain.copies, wl.weight_bytes),
+            "tactic": {k: cfg[k] for k in ("split_k", "fold", "stages", "pipes", "grid_ctas",
+                                           "smem_bytes")},
+        }
+    finally:
+        chain.close()
+        del chain
+        torch.cuda.synchronize(device)
+        torch.cuda.empty_cache()
+
+
+def run_ours(args):
+    import threading
+
+    import torch
+
+    world, rank, local = dist_env()
+    group = False
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        group = True
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    wl = workload()
+    stream = torch.cuda.Stream(device=device)
+    chain = Chain(wl, device, stream)
+    cfg = chain.cfg
+    steps, warmup = max(1, args.steps), max(3, args.warmup)
+    chain.prepare(steps, warmup)
+
+    # Exactly `warmup` untimed steps, then exactly `steps` timed ones.
+    chain.issue(warmup)
+    stream.synchronize()
+    barrier(group)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local) as clocks:
+        local_s = chain.timed(steps)
+        barrier(group)
+        torch.cuda.synchronize(device)
+        # The clocks: the same graphs replayed for at least SOAK_SECONDS right
+        # after the timed region, while the CPU baseline (rank 0, one GPU)
+        # runs on the host cores, so the sampler sees the GPU under this load.
+        cpu = {}
+        worker = None
+        if rank == 0 and world == 1 and args.cpu_seconds > 0:
+            worker = threading.Thread(target=lambda: cpu.update(cpu_baseline(args.cpu_seconds)))
+            worker.start()
+        soak_calls, soak_s = chain.soak(SOAK_SECONDS,
+                                        until=(worker.is_alive if worker is not None else None))
+        if worker is not None:
+            worker.join()
+    if args.profile_graph:
+        # One more replay of the timed graph between the CUDA profiler's start
+        # and stop, for `ncu --profile-from-start off --graph-profiling graph`:
+        # the DRAM bytes of GRAPH_STEPS whole chained calls.
+        torch.cuda.profiler.start()
+        chain.issue(GRAPH_STEPS)
+        stream.synchronize()
+        torch.cuda.profiler.stop()
+    seconds, bytes_all = aggregate(local_s, float(steps * wl.weight_bytes), group)
+    us_per_call = seconds / steps * 1e6
+    value = bytes_all / seconds / 1e9
+
+    # The dominant kernel, the publishing GEMM, back to back and alone.
+    gemm_us = chain.gemm_back_to_back_us(max(steps, 3000))
+    iso_us = chain.isolated_us(min(300, max(steps, 30)))
+    peak, peak_kind = measured_peak()
+    achieved = wl.weight_bytes / (gemm_us * 1e-6) / 1e9
+
+    e2e_s, n_e2e, h2d, d2h = end_to_end(chain, min(3000, max(steps, E2E_GRAPH_STEPS)))
+    e2e_s, e2e_bytes = aggregate(e2e_s, float(n_e2e * wl.weight_bytes), group)
+    chain.check()
+    chain.close()
+    del chain
+    torch.cuda.synchronize(device)
+    torch.cuda.empty_cache()
+
+    # The other workloads of the path, each with its own rotation.
+    workloads = {}
+    if _WORKLOAD == "headline" and not args.no_workloads:
+        import synthetic
+
+        for name in ("graph", "chain", "tiny"):
+            workloads[name] = workload_entry(getattr(synthetic, WORKLOAD_CHOICES[name]), device,
+                                             stream, peak)
 
     if rank == 0:
         traffic = recorded_traffic()
+        clock = clocks.summary()
+        clock["window"] = (f"the timed region and {soak_s:.2f} s of the same chained calls right "
+                           f"after it ({soak_calls} calls, "
+                           f"{soak_s / soak_calls * 1e6:.3f} us per call)")
         line = {
             "metric": METRIC,
             "value": round(value, 1),
             "unit": UNIT,
             "n_gpus": world,
             "steps": steps,
-            "warmup": warm * GRAPH_STEPS,
+            "warmup": warmup,
             "ms_per_step": round(us_per_call / 1e3, 6),
             "us_per_call": round(us_per_call, 3),
             "pct_of_peak": round(100 * (value / world) / peak, 1),
@@ -549,8 +719,9 @@ def run_ours(args):
                 "stages": cfg["stages"], "grid_ctas": cfg["grid_ctas"],
                 "smem_bytes": cfg["smem_bytes"],
                 "weight_bytes_per_call": wl.weight_bytes,
-                "l2": rotation_note(copies, wl.weight_bytes),
-                "timing": f"CUDA graphs of {GRAPH_STEPS} chained calls (GEMM -> PDL consumer)",
+                "l2": rotation_note(weight_copies(wl.weight_bytes), wl.weight_bytes),
+                "timing": f"CUDA graphs of {GRAPH_STEPS} chained calls (GEMM -> PDL consumer), "
+                          "fewer for a remainder, exactly the steps asked",
                 "parallelism": "replicas" if world > 1 else "single GPU",
             },
             "roofline": {
@@ -567,33 +738,45 @@ def run_ours(args):
                 "launch_timing": f"{GRAPH_STEPS} back-to-back launches per CUDA graph, publish off",
                 "isolated_launch_us": round(iso_us, 3),
             },
-            "cpu_baseline": cpu,
+            "cpu_baseline": cpu or None,
             "e2e": {
                 "value": round(e2e_bytes / e2e_s / 1e9, 1),
                 "unit": UNIT,
                 "us_per_call": round(e2e_s / n_e2e * 1e6, 3),
                 "steps": n_e2e,
-                "h2d_bytes_per_step": int(X.numel() + XS.numel()),
+                "h2d_bytes_per_step": h2d,
                 "pipelining": f"every step copies its inputs in (one stream) and its output "
                               f"out (another); the compute waits on the input copies once "
                               f"per {E2E_BATCH} steps, the next batch's inputs landing "
                               f"while the current one computes; {E2E_GRAPH_STEPS} steps per "
                               "captured CUDA graph",
-                "d2h_bytes_per_step": int(out.numel() * out.element_size()),
+                "d2h_bytes_per_step": d2h,
             },
             "gpu_launches": 2 * steps,
             "tactic": {k: cfg[k] for k in ("split_k", "fold", "stages", "acc_blocks", "w_layout",
                                             "l2_prefetch", "l2_prefetch_early", "pipes",
                                             "tmem_columns")},
-            "clocks": clocks.summary(),
+            "clocks": clock,
+            "workloads": workloads,
         }
         print(json.dumps(line), flush=True)
-    for g in gemms:
-        g.close()
     if group:
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+def cpu_baseline(seconds: float) -> dict:
+    """The oracle on the host cores: one thread for `seconds`, then one
+    thread per core for half as long."""
+    gbs, calls, secs, sample = oracle_baseline(seconds)
+    out = {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": sample, "seconds": round(secs, 2)}
+    agbs, threads, acalls, asecs = oracle_baseline_all_cores(seconds / 2)
+    out["all_cores"] = {"value": round(agbs, 4), "unit": UNIT, "cores": threads,
+                        "sample": f"{acalls} calls of the same chain on the same slice, "
+                                  f"one thread per core, over {asecs:.1f} s"}
+    return out
 
 
 # -------------------------------------------------------- reference arm

@@ -26,8 +26,16 @@
  *  - Argument errors are found on the host before any launch; the function
  *    then returns MXFP8_ERR_INVALID or MXFP8_ERR_UNSUPPORTED, launches
  *    nothing, and mxfp8_last_error() describes the problem.
- *  - Every device-side wait is bounded: a wait that runs out sets a bit in
- *    stage_state[3] (read with mxfp8_mailbox_status) instead of hanging.
+ *  - Device-side waits: every poll of the mailbox and every wait of the
+ *    GEMM's pipeline (mbarriers, the split-K exchange) has a time limit
+ *    (mailbox_consume's timeout_ns; the descriptor's wait_limit_ms); one that
+ *    runs out sets a bit in stage_state[3] (read with mxfp8_mailbox_status)
+ *    and the kernel drains instead of hanging.  Two waits have no time limit
+ *    in hardware: tcgen05.alloc (tensor-memory columns) and the cluster
+ *    barriers of split-K.  They are kept from depending on each other by
+ *    construction: a CTA allocates at most half of an SM's tensor memory,
+ *    and a clustered launch asks for enough shared memory that at most two
+ *    of its CTAs share an SM.
  *  - All functions are thread-compatible; mxfp8_last_error() is per thread.
  */
 #ifndef MXFP8_MAILBOX_H
@@ -123,6 +131,13 @@ typedef struct mxfp8_gemm_desc {
                          two CTAs per SM and none with one; measured on GB300: the
                          N=7168, K=16384, S=4 chain 21.44 -> 20.25 us per call
                          against 6 stages for every CTA)                              */
+  int32_t wait_limit_ms;/* how long one wait of the GEMM's pipeline (a ring slot, an
+                         accumulator slot, the split-K exchange) may last before it
+                         gives up: it then sets MXFP8_FLAG_GEMM_TIMEOUT in
+                         stage_state[3] and the kernel drains its copies in flight
+                         and exits (the values it wrote are then meaningless).
+                         1..60000, 0 = 2000.  A run that times out takes at most a
+                         few such limits before it exits.                             */
 } mxfp8_gemm_desc;
 
 /* Where the GEMM streams W from.  IN_PLACE: the caller's [N][K] buffer,
@@ -181,7 +196,13 @@ size_t mxfp8_publish_gemm_workspace_bytes(const mxfp8_gemm_desc* desc);
  * The handle borrows mailbox, stage_state and workspace until destroy, and w
  * too for MXFP8_W_IN_PLACE (w_scale, and w for MXFP8_W_TILED, are read once,
  * by kernels launched here on `stream`, and not afterwards).  On success *out
- * receives the handle. */
+ * receives the handle.
+ * Ordering: the kernels launched here write the workspace, which every run
+ * reads.  The first run (of any kind) on the handle must therefore be ordered
+ * after them: issued on the same `stream`, or on a stream made to wait for it
+ * (an event, or a synchronisation).  That first run launches with a full
+ * stream dependency; later runs overlap their weight loads with the kernel
+ * before them (see mxfp8_publish_gemm_run). */
 mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* w,
                                        const void* w_scale, void* mailbox,
                                        int32_t* stage_state, void* workspace,
@@ -224,10 +245,16 @@ mxfp8_status mxfp8_publish_gemm_precompile(mxfp8_publish_gemm* gemm, int32_t m);
  * The device current when the handle was created must be current (else
  * MXFP8_ERR_INVALID); a handle is used by one host thread at a time.
  * Publishes into generation g = stage_state[0] and sets stage_state[1] = g.
- * Launched with programmatic stream serialisation: weight loads may start
- * before the previous kernel on `stream` finishes; x, x_scale and the state
- * are read only after it has.  Every run must be followed, on the same
- * stream, by exactly one mailbox_consume before the next run. */
+ * Launched with programmatic stream serialisation (except the handle's first
+ * run, which takes a full dependency on create's kernels): weight loads may
+ * start before the previous kernel on `stream` finishes; x, x_scale, alpha
+ * and the state are read only after it has.  So the weight (w for
+ * MXFP8_W_IN_PLACE) and the workspace must not be written by the kernel
+ * right before a run on the stream, nor by one still running when that
+ * kernel starts; writes ordered before a kernel launched without
+ * programmatic serialisation, or before a synchronisation, are safe.  Every
+ * run must be followed, on the same stream, by exactly one mailbox_consume
+ * before the next run. */
 mxfp8_status mxfp8_publish_gemm_run(mxfp8_publish_gemm* gemm, const void* x,
                                     const void* x_scale, int32_t m, void* c, void* stream);
 
@@ -363,10 +390,17 @@ mxfp8_status tagged_consume(void* pairs, int32_t capacity_m, int32_t n, int32_t 
  *  mailbox, stage_state: device, as for mxfp8_mailbox_init.
  * The first call on a device resolves the scratch array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  Every call shares the one array and leaves its
- * scale chunks there; calls that overlap on the GPU (on two streams, or two
- * threads) race on it and must not be issued.  As after
- * mxfp8_publish_gemm_run, one mailbox_consume must follow on the stream. */
+ * before any stream capture.  That address is kept for the life of the
+ * process: after a cudaDeviceReset of the device it is no longer valid, and
+ * this call must not be used there again.  Every call shares the one array
+ * and leaves its scale chunks there; calls that overlap on the GPU (on two
+ * streams, or two threads) race on it and must not be issued.  The GEMM
+ * launches with a full stream dependency (the re-layout right before it
+ * writes what it reads first), so it never overlaps the kernel before it.
+ * A call that repeats the previous call's device, w and desc reuses that
+ * call's tactic and tensor map (and x's map when x and m repeat too): no
+ * re-encoding on the host.  As after mxfp8_publish_gemm_run, one
+ * mailbox_consume must follow on the stream. */
 mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* desc, const void* w,
                                             const void* w_scale, const void* x,
                                             const void* x_scale, int32_t m, void* c,

@@ -36,7 +36,7 @@ class GemmDesc(ctypes.Structure):
     _fields_ = [("n", _i32), ("k", _i32), ("capacity_m", _i32), ("split_k", _i32),
                 ("cta_k", _i32), ("stages", _i32), ("acc_blocks", _i32), ("w_layout", _i32),
                 ("l2_prefetch", _i32), ("pipes", _i32), ("tmem_load", _i32),
-                ("fold", _i32), ("l2_prefetch_early", _i32)]
+                ("fold", _i32), ("l2_prefetch_early", _i32), ("wait_limit_ms", _i32)]
 
 
 SIGNATURES = {

@@ -24,6 +24,18 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(handle)
 
 
+def _synchronize(stream, device) -> None:
+    """Waits for the work issued so far on ``stream`` (as ``_stream`` reads it)."""
+    if stream is None:
+        torch.cuda.current_stream(device).synchronize()
+    elif hasattr(stream, "synchronize"):
+        stream.synchronize()
+    elif int(stream) == 0:  # the legacy default stream waits for the whole device
+        torch.cuda.synchronize(device)
+    else:
+        torch.cuda.ExternalStream(int(stream), device=device).synchronize()
+
+
 def _on_device(t: torch.Tensor, name: str) -> None:
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
@@ -106,7 +118,8 @@ def _config_dict(d: GemmDesc, smem: int, tmem: int, grid: int) -> dict:
             "l2_prefetch": d.l2_prefetch, "l2_prefetch_early": d.l2_prefetch_early,
             "pipes": d.pipes,
             "tmem_load": {1: "32x32b", 2: "16x256b"}.get(d.tmem_load, d.tmem_load),
-            "fold": d.fold, "smem_bytes": smem, "tmem_columns": tmem, "grid_ctas": grid}
+            "fold": d.fold, "wait_limit_ms": d.wait_limit_ms, "smem_bytes": smem,
+            "tmem_columns": tmem, "grid_ctas": grid}
 
 
 # GB300: SMs, shared memory per SM, shared memory per CTA at most.
@@ -116,12 +129,12 @@ GB300_LIMITS = (152, 233472, 232448)
 def plan_gemm(n: int, k: int, capacity_m: int = 8, split_k: int = 0, stages: int = 0,
               acc_blocks: int = 0, w_layout: int = 0, l2_prefetch: int = 0, pipes: int = 0,
               tmem_load: int = 0, fold: int = 0, l2_prefetch_early: int = 0,
-              limits: tuple = GB300_LIMITS) -> dict:
+              wait_limit_ms: int = 0, limits: tuple = GB300_LIMITS) -> dict:
     """The tactic PublishGemm would resolve for this shape on a device with
     `limits` = (SMs, shared memory per SM, shared memory per CTA), as
     PublishGemm.config() reports it; needs no GPU."""
     desc = GemmDesc(n, k, capacity_m, split_k, 0, stages, acc_blocks, w_layout, l2_prefetch,
-                    pipes, tmem_load, fold, l2_prefetch_early)
+                    pipes, tmem_load, fold, l2_prefetch_early, wait_limit_ms)
     out = GemmDesc()
     smem, tmem, grid = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
     check(_lib.load().mxfp8_publish_gemm_plan(ctypes.byref(desc), *limits, ctypes.byref(out),
@@ -134,12 +147,17 @@ class PublishGemm:
     """One MXFP8 weight ``W [N][K]`` (E4M3 codes) with its scales ``[N][K/32]``
     (E8M0 codes), publishing into ``mailbox``.  The weight, mailbox and the
     workspace this object allocates stay borrowed by the native handle until
-    :meth:`close`."""
+    :meth:`close`.
+
+    The library's create launches the weight re-layout on ``stream`` (the
+    current stream by default), and a run must come after it; this
+    constructor waits for that stream, so runs may then be issued on any
+    stream."""
 
     def __init__(self, w: torch.Tensor, w_scale: torch.Tensor, mailbox: Mailbox,
                  split_k: int = 0, stages: int = 0, acc_blocks: int = 0, w_layout: int = 0,
                  l2_prefetch: int = 0, pipes: int = 0, tmem_load: int = 0, fold: int = 0,
-                 l2_prefetch_early: int = 0, stream=None):
+                 l2_prefetch_early: int = 0, wait_limit_ms: int = 0, stream=None):
         lib = _lib.load()
         if w.dim() != 2:
             raise ValueError(f"w must be [N][K], got {tuple(w.shape)}")
@@ -148,7 +166,8 @@ class PublishGemm:
         if k % 32 == 0:  # other K are refused by the library below
             _codes(w_scale, "w_scale", k // 32, min_rows=n)
         self.desc = GemmDesc(n, k, mailbox.capacity, split_k, 0, stages, acc_blocks, w_layout,
-                             l2_prefetch, pipes, tmem_load, fold, l2_prefetch_early)
+                             l2_prefetch, pipes, tmem_load, fold, l2_prefetch_early,
+                             wait_limit_ms)
         ws_bytes = lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(self.desc))
         if ws_bytes == 0:
             raise ValueError(f"invalid GEMM shape N={n}, K={k}")
@@ -162,6 +181,9 @@ class PublishGemm:
                                             _ptr(self.workspace), ws_bytes, _stream(stream),
                                             ctypes.byref(handle)), "mxfp8_publish_gemm_create")
         self._handle = handle
+        # The re-layout kernels create launched must finish before a run on
+        # another stream reads the workspace.
+        _synchronize(stream, w.device)
 
     def config(self) -> dict:
         d = GemmDesc()

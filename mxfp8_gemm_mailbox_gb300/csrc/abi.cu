@@ -14,6 +14,7 @@
 
 #include "internal.h"
 #include "mxfp8_mailbox.h"
+#include "noalloc_cache.h"
 
 using namespace mxfp8;
 
@@ -25,6 +26,11 @@ struct mxfp8_publish_gemm {
   uint16_t* mailbox;
   int32_t* state;
   int device;
+  // Set by create, whose re-layout kernels write the scale chunks and the
+  // tiled weight that the GEMM's producer reads before its grid wait: the
+  // first launch then takes a full stream dependency instead of the
+  // programmatic one.
+  bool first_launch_pending;
   int k_tiles;  // stages of K: ceil(K / (128 fold))
   int tiles_per_split;
   TmemPlan tmem;
@@ -52,7 +58,8 @@ mxfp8_status cuda_fail(cudaError_t err, const char* what) {
 bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
 constexpr uint64_t kDefaultPollTimeoutNs = 1000000000ull;
-constexpr uint64_t kGemmWaitLimitNs = 2000000000ull;
+constexpr int kDefaultGemmWaitLimitMs = 2000;
+constexpr int kMaxGemmWaitLimitMs = 60000;
 // W stages past the ring each CTA warms in L2 by default.  The first 70 % of
 // a grid's CTAs launch while the previous kernel streams and warm few; the
 // rest warm many.  Measured on GB300, chains of GEMM + consumer rotating
@@ -144,6 +151,10 @@ mxfp8_status check_desc(const mxfp8_gemm_desc* d) {
                 "tmem_load must be MXFP8_TMEM_LOAD_32X32B or MXFP8_TMEM_LOAD_16X256B");
   if (d->fold != 0 && d->fold != 1 && d->fold != 2 && d->fold != 4 && d->fold != 8)
     return fail(MXFP8_ERR_UNSUPPORTED, "fold must be 1, 2, 4 or 8 (or 0 to choose)");
+  if (d->wait_limit_ms < 0 || d->wait_limit_ms > kMaxGemmWaitLimitMs)
+    return fail(MXFP8_ERR_UNSUPPORTED, "wait_limit_ms must be in 1.." +
+                                           std::to_string(kMaxGemmWaitLimitMs) + " (or 0 for " +
+                                           std::to_string(kDefaultGemmWaitLimitMs) + ")");
   if (d->fold == 8) {
     if (d->split_k > 1) return fail(MXFP8_ERR_UNSUPPORTED, "fold 8 takes split_k 1");
     if (d->pipes == 4)
@@ -205,6 +216,33 @@ GemmSmemLayout at_most_two_per_sm(GemmSmemLayout layout, int split_k, const Devi
   return layout;
 }
 
+// The dynamic shared-memory limit of a kernel instantiation is one value per
+// device, shared by every handle (and allocation-free call) that launches it.
+// It only bounds what a launch may ask for, so it is raised to the largest
+// size any of them needs and never lowered: a handle with a shallower ring
+// must not push it below an earlier handle's launch size.  `force` sets it
+// again even when the recorded value suffices (precompile does, so a context
+// that was torn down and re-created gets it back).
+constexpr int kMaxDevicesTracked = 64;
+
+mxfp8_status ensure_smem_attribute(int device, int split_k, int fold, int bytes, bool force) {
+  static std::mutex mutex;
+  // [device][log2 split_k][log2 fold]: split_k and fold are 1, 2, 4 or 8.
+  static int raised[kMaxDevicesTracked][4][4] = {};
+  if (device < 0 || device >= kMaxDevicesTracked)
+    return fail(MXFP8_ERR_UNSUPPORTED, "device ordinal out of range for the launch table");
+  const int si = split_k == 8 ? 3 : split_k / 2;
+  const int fi = fold == 8 ? 3 : fold / 2;
+  std::lock_guard<std::mutex> lock(mutex);
+  int& have = raised[device][si][fi];
+  if (!force && have >= bytes) return MXFP8_OK;
+  const int want = std::max(have, bytes);
+  const cudaError_t e = set_gemm_smem_attribute(split_k, fold, want);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+  have = want;
+  return MXFP8_OK;
+}
+
 // Fill split_k, cta_k, stages, pipes and fold: split_k so the grid has about
 // one or two CTAs per SM; then the largest fold that keeps at most one CTA
 // per SM (one SM streams only so fast: few-CTA grids leave HBM idle); the
@@ -222,6 +260,7 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
     d->split_k = s;
   }
   d->cta_k = kTileK;
+  if (d->wait_limit_ms == 0) d->wait_limit_ms = kDefaultGemmWaitLimitMs;
   if (d->acc_blocks == 0) d->acc_blocks = 4;
   if (d->tmem_load == 0) d->tmem_load = MXFP8_TMEM_LOAD_32X32B;
   d->w_layout = resolved_w_layout(d->w_layout);
@@ -340,11 +379,13 @@ mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale,
   p.alpha = alpha;
   p.mailbox = g->mailbox;
   p.state = g->state;
-  p.wait_limit_ns = kGemmWaitLimitNs;
+  p.wait_limit_ns = static_cast<uint64_t>(g->desc.wait_limit_ms) * 1000000ull;
   p.smem = g->layout;
   cudaError_t e = launch_publish_gemm(g->tmap_w, g->tmap_x, p, g->desc.split_k,
-                                      static_cast<cudaStream_t>(stream));
+                                      static_cast<cudaStream_t>(stream),
+                                      !g->first_launch_pending);
   if (e != cudaSuccess) return cuda_fail(e, "launching the publishing GEMM");
+  g->first_launch_pending = false;
   return MXFP8_OK;
 }
 
@@ -435,6 +476,7 @@ mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* 
   g->mailbox = static_cast<uint16_t*>(mailbox);
   g->state = stage_state;
   g->device = device;
+  g->first_launch_pending = true;
   g->k_tiles = k_tiles_for_fold(desc->k, fold);
   g->tiles_per_split = (g->k_tiles + g->desc.split_k - 1) / g->desc.split_k;
   g->tmem = gemm_tmem_plan(g->desc.stages, g->desc.acc_blocks, fold);
@@ -449,10 +491,11 @@ mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* 
     delete g;
     return st;
   }
-  e = set_gemm_smem_attribute(g->desc.split_k, fold, static_cast<int>(g->layout.total));
-  if (e != cudaSuccess) {
+  st = ensure_smem_attribute(device, g->desc.split_k, fold, static_cast<int>(g->layout.total),
+                             false);
+  if (st != MXFP8_OK) {
     delete g;
-    return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+    return st;
   }
   e = launch_relayout_w_scales(static_cast<const uint8_t*>(w_scale), g->w_sf, desc->n, desc->k,
                                fold, static_cast<cudaStream_t>(stream));
@@ -516,10 +559,8 @@ mxfp8_status mxfp8_publish_gemm_precompile(mxfp8_publish_gemm* gemm, int32_t m) 
   mxfp8_status st = check_rows(gemm, m);
   if (st != MXFP8_OK) return st;
   if (!encode_tiled()) return fail(MXFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-  cudaError_t e = set_gemm_smem_attribute(gemm->desc.split_k, gemm->desc.fold,
-                                          static_cast<int>(gemm->layout.total));
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
-  return MXFP8_OK;
+  return ensure_smem_attribute(gemm->device, gemm->desc.split_k, gemm->desc.fold,
+                               static_cast<int>(gemm->layout.total), true);
 }
 
 mxfp8_status mxfp8_publish_gemm_run(mxfp8_publish_gemm* gemm, const void* x, const void* x_scale,
@@ -701,6 +742,23 @@ mxfp8_status noalloc_scratch(int device, uint8_t** out) {
   return MXFP8_OK;
 }
 
+// The set-up of an allocation-free call that depends only on the weight's
+// address and the descriptor (kept per device from the last call), plus the
+// activations' tensor map, kept while x and m repeat.
+struct NoallocPlan {
+  mxfp8_gemm_desc desc;  // resolved tactic
+  int k_tiles;
+  int tiles_per_split;
+  TmemPlan tmem;
+  GemmSmemLayout layout;
+  CUtensorMap tmap_w;
+  const void* x;
+  int m;
+  CUtensorMap tmap_x;
+};
+
+LastRequestCache<NoallocPlan, kMaxDevices> g_noalloc_plans;
+
 }  // namespace
 
 extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* desc, const void* w,
@@ -730,34 +788,59 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
                     std::to_string(need) + " scratch bytes; the allocation-free call holds " +
                     std::to_string(MXFP8_NOALLOC_SCRATCH_BYTES));
 
-  mxfp8_gemm_desc d = *desc;
-  d.w_layout = MXFP8_W_IN_PLACE;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  DeviceLimits lim;
-  st = device_limits(device, &lim);
-  if (st != MXFP8_OK) return st;
-  st = resolve_tactic(&d, lim);
-  if (st != MXFP8_OK) return st;
   uint8_t* scratch = nullptr;
   st = noalloc_scratch(device, &scratch);
   if (st != MXFP8_OK) return st;
 
-  const int k_tiles = k_tiles_for_fold(d.k, d.fold);
-  const int tiles_per_split = (k_tiles + d.split_k - 1) / d.split_k;
-  CUtensorMap tmap_w, tmap_x;
-  st = encode_rows(&tmap_w, w, static_cast<uint64_t>(d.k), static_cast<uint64_t>(d.n),
-                   kBlockN / d.fold);
+  // Resolving the tactic, encoding W's tensor map and raising the kernel's
+  // shared-memory limit happen once per (device, w, descriptor); x's map once
+  // per (x, m).
+  NoallocPlan plan;
+  auto make = [&](NoallocPlan* pl) {
+    mxfp8_gemm_desc d = *desc;
+    d.w_layout = MXFP8_W_IN_PLACE;
+    DeviceLimits lim;
+    mxfp8_status s2 = device_limits(device, &lim);
+    if (s2 != MXFP8_OK) return s2;
+    s2 = resolve_tactic(&d, lim);
+    if (s2 != MXFP8_OK) return s2;
+    pl->desc = d;
+    pl->k_tiles = k_tiles_for_fold(d.k, d.fold);
+    pl->tiles_per_split = (pl->k_tiles + d.split_k - 1) / d.split_k;
+    pl->tmem = gemm_tmem_plan(d.stages, d.acc_blocks, d.fold);
+    pl->layout = at_most_two_per_sm(
+        gemm_smem_layout(d.stages, d.split_k, pl->tiles_per_split, d.fold), d.split_k, lim);
+    s2 = encode_rows(&pl->tmap_w, w, static_cast<uint64_t>(d.k), static_cast<uint64_t>(d.n),
+                     kBlockN / d.fold);
+    if (s2 != MXFP8_OK) return s2;
+    pl->x = nullptr;
+    pl->m = 0;
+    return ensure_smem_attribute(device, d.split_k, d.fold, static_cast<int>(pl->layout.total),
+                                 false);
+  };
+  auto refresh = [&](NoallocPlan* pl) {
+    if (pl->x == x && pl->m == m) return MXFP8_OK;
+    pl->x = nullptr;
+    const mxfp8_status s2 = encode_rows(&pl->tmap_x, x, static_cast<uint64_t>(pl->desc.k),
+                                        static_cast<uint64_t>(m), kRows);
+    if (s2 != MXFP8_OK) return s2;
+    pl->x = x;
+    pl->m = m;
+    return MXFP8_OK;
+  };
+  st = g_noalloc_plans.get(device, NoallocRequest{w, *desc}, &plan, make, refresh);
   if (st != MXFP8_OK) return st;
-  st = encode_rows(&tmap_x, x, static_cast<uint64_t>(d.k), static_cast<uint64_t>(m), kRows);
-  if (st != MXFP8_OK) return st;
+
+  const mxfp8_gemm_desc& d = plan.desc;
   GemmParams p{};
   p.n = d.n;
   p.k = d.k;
   p.m = m;
-  p.k_tiles = k_tiles;
-  p.tiles_per_split = tiles_per_split;
+  p.k_tiles = plan.k_tiles;
+  p.tiles_per_split = plan.tiles_per_split;
   p.stages = d.stages;
   p.capacity = d.capacity_m;
   p.publish = 1;
@@ -768,22 +851,21 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
   p.pipes = d.pipes;
   p.tmem_load = d.tmem_load;
   p.fold = d.fold;
-  p.tmem = gemm_tmem_plan(d.stages, d.acc_blocks, d.fold);
+  p.tmem = plan.tmem;
   p.x_scale = static_cast<const uint8_t*>(x_scale);
   p.w_sf = scratch;
   p.w_tiled = nullptr;
   p.c = static_cast<uint16_t*>(c);
   p.mailbox = static_cast<uint16_t*>(mailbox);
   p.state = stage_state;
-  p.wait_limit_ns = kGemmWaitLimitNs;
-  p.smem = at_most_two_per_sm(gemm_smem_layout(d.stages, d.split_k, tiles_per_split, d.fold),
-                              d.split_k, lim);
-  e = set_gemm_smem_attribute(d.split_k, d.fold, static_cast<int>(p.smem.total));
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+  p.wait_limit_ns = static_cast<uint64_t>(d.wait_limit_ms) * 1000000ull;
+  p.smem = plan.layout;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   e = launch_relayout_w_scales(static_cast<const uint8_t*>(w_scale), scratch, d.n, d.k, d.fold, s);
   if (e != cudaSuccess) return cuda_fail(e, "launching the W scale re-layout");
-  e = launch_publish_gemm(tmap_w, tmap_x, p, d.split_k, s);
+  // The re-layout right before it writes the scale chunks the GEMM's producer
+  // reads before its grid wait, so this launch takes a full stream dependency.
+  e = launch_publish_gemm(plan.tmap_w, plan.tmap_x, p, d.split_k, s, false);
   if (e != cudaSuccess) return cuda_fail(e, "launching the publishing GEMM");
   return MXFP8_OK;
 }

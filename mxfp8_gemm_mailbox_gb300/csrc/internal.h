@@ -83,12 +83,17 @@ GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, in
 TmemPlan gemm_tmem_plan(int stages, int acc_blocks, int fold);
 int k_tiles_for_fold(int k, int fold);  // ceil(k / (128 fold))
 
-// Kernel launchers (return the CUDA error of the launch).
+// Kernel launchers (return the CUDA error of the launch).  The GEMM's
+// producer starts its weight and scale-chunk loads before the programmatic
+// grid wait, so `programmatic` must be false when the kernel right before it
+// on the stream may write those bytes.
 cudaError_t launch_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
-                                const GemmParams& p, int split_k, cudaStream_t stream);
+                                const GemmParams& p, int split_k, cudaStream_t stream,
+                                bool programmatic);
 cudaError_t set_gemm_smem_attribute(int split_k, int fold, int bytes);
 cudaError_t launch_folded_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
-                                       const GemmParams& p, int split_k, cudaStream_t stream);
+                                       const GemmParams& p, int split_k, cudaStream_t stream,
+                                       bool programmatic);
 cudaError_t set_folded_gemm_smem_attribute(int split_k, int fold, int bytes);
 cudaError_t launch_relayout_w_scales(const uint8_t* w_scale, uint8_t* w_sf, int n, int k,
                                      int fold, cudaStream_t stream);

@@ -126,22 +126,24 @@ cudaError_t set_gemm_smem_attribute(int split_k, int fold, int bytes) {
 }
 
 cudaError_t launch_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
-                                const GemmParams& p, int split_k, cudaStream_t stream) {
-  if (p.fold != 1) return launch_folded_publish_gemm(tmap_w, tmap_x, p, split_k, stream);
+                                const GemmParams& p, int split_k, cudaStream_t stream,
+                                bool programmatic) {
+  if (p.fold != 1)
+    return launch_folded_publish_gemm(tmap_w, tmap_x, p, split_k, stream, programmatic);
   const bool wide = p.tmem_load == MXFP8_TMEM_LOAD_16X256B;
   switch (split_k) {
     case 1:
-      return wide ? launch_impl<1, true, 1>(tmap_w, tmap_x, p, stream)
-                  : launch_impl<1, false, 1>(tmap_w, tmap_x, p, stream);
+      return wide ? launch_impl<1, true, 1>(tmap_w, tmap_x, p, stream, programmatic)
+                  : launch_impl<1, false, 1>(tmap_w, tmap_x, p, stream, programmatic);
     case 2:
-      return wide ? launch_impl<2, true, 1>(tmap_w, tmap_x, p, stream)
-                  : launch_impl<2, false, 1>(tmap_w, tmap_x, p, stream);
+      return wide ? launch_impl<2, true, 1>(tmap_w, tmap_x, p, stream, programmatic)
+                  : launch_impl<2, false, 1>(tmap_w, tmap_x, p, stream, programmatic);
     case 4:
-      return wide ? launch_impl<4, true, 1>(tmap_w, tmap_x, p, stream)
-                  : launch_impl<4, false, 1>(tmap_w, tmap_x, p, stream);
+      return wide ? launch_impl<4, true, 1>(tmap_w, tmap_x, p, stream, programmatic)
+                  : launch_impl<4, false, 1>(tmap_w, tmap_x, p, stream, programmatic);
     case 8:
-      return wide ? launch_impl<8, true, 1>(tmap_w, tmap_x, p, stream)
-                  : launch_impl<8, false, 1>(tmap_w, tmap_x, p, stream);
+      return wide ? launch_impl<8, true, 1>(tmap_w, tmap_x, p, stream, programmatic)
+                  : launch_impl<8, false, 1>(tmap_w, tmap_x, p, stream, programmatic);
     default:
       return cudaErrorInvalidValue;
   }

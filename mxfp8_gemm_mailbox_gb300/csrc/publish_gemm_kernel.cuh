@@ -842,9 +842,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   }
 }
 
+// programmatic: launched with programmatic stream serialisation, so the
+// kernel may start (and stream W) before the previous kernel on the stream
+// has finished.  Off where that kernel writes what the producer reads before
+// its grid wait (the weight or its scale chunks).
 template <int S, bool kWideLoad, int F>
 cudaError_t launch_impl(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, const GemmParams& p,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool programmatic) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((p.n / (kBlockN / F)) * S), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(threads_for_pipes(p.pipes)), 1, 1);
@@ -852,9 +856,11 @@ cudaError_t launch_impl(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, co
   cfg.stream = stream;
   cudaLaunchAttribute attrs[2];
   int count = 0;
-  attrs[count].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attrs[count].val.programmaticStreamSerializationAllowed = 1;
-  ++count;
+  if (programmatic) {
+    attrs[count].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[count].val.programmaticStreamSerializationAllowed = 1;
+    ++count;
+  }
   if (S > 1) {
     attrs[count].id = cudaLaunchAttributeClusterDimension;
     attrs[count].val.clusterDim.x = S;

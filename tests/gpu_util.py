@@ -28,15 +28,23 @@ def ordered(b: np.ndarray) -> np.ndarray:
     return np.where(b & 0x8000, -(b & 0x7FFF), b)
 
 
+def is_nan(b: np.ndarray) -> np.ndarray:
+    """BF16 NaN codes: exponent all ones, mantissa not zero."""
+    b = np.asarray(b, dtype=np.uint16)
+    return ((b & 0x7F80) == 0x7F80) & ((b & 0x007F) != 0)
+
+
 def bf16_mismatches(got: np.ndarray, want: np.ndarray) -> np.ndarray:
-    """Boolean mask of positions outside the tolerance."""
+    """Boolean mask of positions outside the tolerance.  A NaN on either side
+    is a mismatch, even beside a NaN (two NaN codes can be 0 or 1 apart in the
+    ordered encoding)."""
     got = np.asarray(got, dtype=np.uint16)
     want = np.asarray(want, dtype=np.uint16)
     ulp = np.abs(ordered(got) - ordered(want))
     gv = oracle.bf16_bits_to_float(got)
     wv = oracle.bf16_bits_to_float(want)
     small_ok = (np.abs(wv) < SMALL) & (np.abs(gv - wv) <= ABS_TOL)
-    return ~((ulp <= ULP_TOL) | small_ok)
+    return ~((ulp <= ULP_TOL) | small_ok) | is_nan(got) | is_nan(want)
 
 
 def describe(got: np.ndarray, want: np.ndarray, limit: int = 8) -> str:

@@ -1,6 +1,7 @@
 """bench.py end to end on the GPU, on the tiny workload: one JSON line with
 every key of the contract (roofline, CPU baseline, end-to-end, launches,
-clocks), a clean mailbox and sane values."""
+clocks), exactly the steps and warm-up asked, a clean mailbox and sane
+values."""
 import json
 import subprocess
 import sys
@@ -22,7 +23,8 @@ def test_bench_line_has_every_contract_key(cuda):
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
                 "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
         assert key in line, key
-    assert line["n_gpus"] == 1 and line["steps"] == 60 and line["value"] > 0
+    assert line["n_gpus"] == 1 and line["steps"] == 60 and line["warmup"] == 3
+    assert line["value"] > 0
     assert line["higher_is_better"] is True and line["scaling"] == "weak"
     roof = line["roofline"]
     for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
@@ -36,4 +38,6 @@ def test_bench_line_has_every_contract_key(cuda):
     assert e2e["d2h_bytes_per_step"] == 256 * 2  # out [1][256] BF16
     assert line["gpu_launches"] == 2 * 60
     assert "sm_mhz" in line["clocks"] and "reasons" in line["clocks"]
+    assert "window" in line["clocks"]
+    assert line["workloads"] == {}  # the other workloads ride on the headline's line only
     assert "L2" in line["config"]["l2"]

@@ -9,6 +9,7 @@ import torch
 
 import oracle
 from mxfp8_gemm_mailbox_gb300 import ERR_STATE, OK, LamportGather
+from tests import stress_schedule as ss
 from tests.gpu_util import dev
 
 pytestmark = pytest.mark.gpu
@@ -17,7 +18,7 @@ CAP = 256 * 1024  # "a few hundred kilobytes at most"
 
 
 def _words(n, seed, sentinel_share=0.05):
-    rng = np.random.default_rng(seed)
+    rng = np.random.default_rng(list(seed) if isinstance(seed, tuple) else seed)
     w = rng.integers(0, 2**32, size=n, dtype=np.uint64).astype(np.uint32)
     w[rng.random(n) < sentinel_share] = oracle.SENTINEL
     return w
@@ -45,34 +46,51 @@ def test_gather_matches_oracle_over_alternating_sizes(cuda):
 
 
 def test_gather_stale_word_stress_in_graphs(cuda):
-    # Back-to-back gathers of alternating sizes replayed from CUDA graphs: a
-    # word left behind by one call would show up in a later call of another
-    # size.  Every output is compared on the device with its expected value.
+    # Back-to-back gathers of alternating sizes replayed from CUDA graphs (the
+    # all-gather page's stress).  The sizes cycle with a period of 4 over the
+    # 3 generations and each size has 5 inputs, so every use of a generation
+    # gets another size and other bytes: a word that one call left in a slot
+    # differs from what a later call reading it should return.  Every call
+    # writes its own output, poisoned before each replay, and is compared on
+    # the device with the oracle's answer for its input: 10,000 calls.
     g = LamportGather(CAP)
-    sizes = (16, 4112, CAP)
-    inputs = {s: dev(_words(s // 4, seed=s).view(np.int32)) for s in sizes}
-    expect = {s: torch.where(inputs[s] == -(2**31), torch.zeros_like(inputs[s]), inputs[s])
-              for s in sizes}
-    outs = {s: torch.empty_like(inputs[s]) for s in sizes}
+    ref = oracle.Gather(CAP)
+    sizes, variants = (16, 4112, CAP, 48), 5
+    per_graph = ss.period(len(sizes), variants, 3)  # 60 calls
+    schedule = ss.gather_schedule(per_graph, sizes, variants)
+    inputs, expect = {}, {}
+    for nbytes in sizes:
+        for v in range(variants):
+            words = _words(nbytes // 4, seed=(nbytes, v))
+            st, want = ref(words)
+            assert st == oracle.OK
+            inputs[(nbytes, v)] = dev(words.view(np.int32))
+            expect[(nbytes, v)] = dev(want.view(np.int32))
+    outs = [torch.empty(nbytes // 4, dtype=torch.int32, device="cuda") for nbytes, _ in schedule]
     stream = torch.cuda.Stream()
-    graphs = {}
-    for s in sizes:
-        graphs[s] = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graphs[s], stream=stream):
-            g(inputs[s], outs[s])
+    with torch.cuda.stream(stream):
+        for j, key in enumerate(schedule):  # eager warm-up
+            g(inputs[key], outs[j])
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for j, key in enumerate(schedule):
+                g(inputs[key], outs[j])
     torch.cuda.synchronize()
-    calls = 0
+    calls = 10_020  # 167 replays of 60 calls
     mismatches = torch.zeros((), dtype=torch.int64, device="cuda")
     with torch.cuda.stream(stream):
-        for _ in range(3000):
-            for s in sizes:
-                graphs[s].replay()
-                calls += 1
-                mismatches += (outs[s] != expect[s]).sum()
+        for _ in range(calls // per_graph):
+            for o in outs:
+                o.fill_(-(2**31))  # the sentinel word: never an output word
+            graph.replay()
+            for j, key in enumerate(schedule):
+                mismatches += (outs[j] != expect[key]).sum()
     torch.cuda.synchronize()
     assert int(mismatches) == 0
     assert (_mailbox(g) == oracle.SENTINEL).all()
-    assert [int(v) for v in g.state.cpu()] == [calls % 3, 0, 0, 0]
+    total = per_graph + calls
+    assert [int(v) for v in g.state.cpu()] == [total % 3, 0, 0, 0]
     assert g.status()[0] == OK
 
 

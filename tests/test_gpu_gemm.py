@@ -594,3 +594,45 @@ def test_global_scale(cuda, alpha, split_k, fold):
     mb.consume(6)
     torch.cuda.synchronize()
     assert_bf16_close(bits(c), oracle.gemm_bf16(w, ws, x, xs))
+
+
+@pytest.mark.parametrize("w_layout", [W_TILED, W_IN_PLACE])
+def test_first_run_right_after_create_on_one_stream(cuda, w_layout):
+    # Through the C ABI with no host synchronisation between create and the
+    # first run: create's re-layout kernels write the scale chunks (and the
+    # tiled weight) that the GEMM's producer reads before its grid wait, so
+    # the handle's first launch takes a full stream dependency.  Several fresh
+    # handles, each run once right away, must all match the oracle.
+    import ctypes
+
+    from mxfp8_gemm_mailbox_gb300 import _lib
+
+    lib = _lib.load()
+    stream = torch.cuda.Stream()
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    n, k, m = 2048, 4096, 8
+    for seed in range(4):
+        wl = synthetic.Workload("first-run", n, k, m, 2, exp_lo=-4, exp_hi=2, seed=900 + seed)
+        w, ws = synthetic.make_weights(wl)
+        x, xs = synthetic.make_activations(wl)
+        W, WS, X, XS = dev(w), dev(ws), dev(x), dev(xs)
+        mb = Mailbox(8, n)
+        desc = _lib.GemmDesc(n, k, 8, 2, 0, 0, 0, w_layout)
+        ws_bytes = lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(desc))
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        c = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+        out = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+        torch.cuda.synchronize()  # inputs and the armed mailbox are in place
+        handle = ctypes.c_void_p()
+        ptr = lambda t: ctypes.c_void_p(t.data_ptr())
+        assert lib.mxfp8_publish_gemm_create(ctypes.byref(desc), ptr(W), ptr(WS), ptr(mb.words),
+                                             ptr(mb.state), ptr(workspace), ws_bytes, sp,
+                                             ctypes.byref(handle)) == OK
+        assert lib.mxfp8_publish_gemm_run(handle, ptr(X), ptr(XS), m, ptr(c), sp) == OK
+        assert lib.mailbox_consume(ptr(mb.words), ptr(mb.state), 8, n, m, ptr(out), 0, sp) == OK
+        stream.synchronize()
+        lib.mxfp8_publish_gemm_destroy(handle)
+        want = oracle.gemm_bf16(w, ws, x, xs)
+        assert_bf16_close(bits(c), want, f"seed {seed}")
+        assert (bits(out) == sanitized(bits(c))).all()
+        assert state_words(mb) == [1, 0, 0, 0]

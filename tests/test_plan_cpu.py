@@ -146,3 +146,19 @@ def test_split_choice_when_left_open():
     assert plan_gemm(16384, 16384)["split_k"] == 2
     assert plan_gemm(2048, 256)["split_k"] == 1
     assert plan_gemm(2048, 2048)["grid_ctas"] == 2048 // 64 * 4  # S = 4, fold 2
+
+
+def test_gemm_wait_limit_field():
+    # The GEMM's pipeline waits give up after wait_limit_ms: 0 asks for the
+    # default of 2 s, an explicit value is kept, values outside 1..60000 are
+    # refused before anything launches.
+    assert plan_gemm(7168, 16384, split_k=4)["wait_limit_ms"] == 2000
+    assert plan_gemm(7168, 16384, split_k=4, wait_limit_ms=1)["wait_limit_ms"] == 1
+    assert plan_gemm(4096, 4096, wait_limit_ms=60000)["wait_limit_ms"] == 60000
+    for bad in (-1, 60001):
+        with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED.*wait_limit_ms"):
+            plan_gemm(4096, 4096, wait_limit_ms=bad)
+    # the limit changes nothing else of the plan
+    a, b = plan_gemm(7168, 8192, split_k=2), plan_gemm(7168, 8192, split_k=2, wait_limit_ms=5)
+    assert {k: v for k, v in a.items() if k != "wait_limit_ms"} == \
+        {k: v for k, v in b.items() if k != "wait_limit_ms"}

@@ -37,3 +37,7 @@ def test_absolute_tolerance_only_below_two_to_the_minus_six():
 
 def test_nan_never_matches():
     assert _bad(0x7FC0, 0x3F80) and _bad(0x7FC0, 0x0000) and _bad(0x3F80, 0x7FC0)
+    # not even another NaN, whose code may lie 0 or 1 apart in the ordered encoding
+    assert _bad(0x7FC0, 0x7FC0) and _bad(0x7FC1, 0x7FC0) and _bad(0xFFC0, 0xFFC0)
+    assert _bad(0x7F81, 0x7F80)                                    # NaN beside infinity
+    assert not _bad(0x7F80, 0x7F80) and not _bad(0xFF80, 0xFF80)   # infinity is a value

@@ -18,7 +18,8 @@ import torch
 import oracle
 import synthetic
 from mxfp8_gemm_mailbox_gb300 import OK, Mailbox, PublishGemm, _lib
-from tests.gpu_util import assert_bf16_close, bits, dev, mailbox_words, state_words
+from tests.gpu_util import (assert_bf16_close, bits, dev, mailbox_words, pack_words, sanitized,
+                            state_words)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,16 +34,20 @@ def _ptr(t):
 
 @pytest.mark.parametrize("fold", [1, 0])
 def test_noalloc_matches_the_handle_path_on_two_calls(cuda, fold):
+    # Two calls in a row, each with its own weight scales: the second call's
+    # re-layout overwrites the scratch the first call's GEMM read, and its
+    # GEMM must see the new chunks.  Both paths run the same kernel with the
+    # same tactic and summation order, so they agree bit for bit.
     lib = _lib.load()
     n, k, m, split = 1024, 4096, 5, 2
-    wl = synthetic.Workload("noalloc", n, k, m, split, exp_lo=-4, exp_hi=2, seed=4242)
-    w, ws = synthetic.make_weights(wl)
-    W, WS = dev(w), dev(ws)
-    handle_mb, noalloc_mb = Mailbox(8, n), Mailbox(8, n)
-    gemm = PublishGemm(W, WS, handle_mb, split_k=split, w_layout=_lib.W_IN_PLACE, fold=fold)
-    assert gemm.config()["fold"] == (fold or 4)  # 8 tiles x 2 splits fold 4 ways by default
     desc = _lib.GemmDesc(n, k, 8, split, 0, 0, 0, 0, 0, 0, 0, fold)
+    handle_mb, noalloc_mb = Mailbox(8, n), Mailbox(8, n)
     for call in range(2):
+        wl = synthetic.Workload("noalloc", n, k, m, split, exp_lo=-4, exp_hi=2, seed=4242 + call)
+        w, ws = synthetic.make_weights(wl)
+        W, WS = dev(w), dev(ws)
+        gemm = PublishGemm(W, WS, handle_mb, split_k=split, w_layout=_lib.W_IN_PLACE, fold=fold)
+        assert gemm.config()["fold"] == (fold or 4)  # 8 tiles x 2 splits fold 4 ways by default
         x, xs = synthetic.make_activations(wl, salt=call)
         X, XS = dev(x), dev(xs)
         c_handle = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
@@ -53,15 +58,17 @@ def test_noalloc_matches_the_handle_path_on_two_calls(cuda, fold):
             ctypes.byref(desc), _ptr(W), _ptr(WS), _ptr(X), _ptr(XS), m, _ptr(c_noalloc),
             _ptr(noalloc_mb.words), _ptr(noalloc_mb.state), _stream())
         assert status == OK, lib.mxfp8_last_error().decode()
+        between = mailbox_words(noalloc_mb)
         out_noalloc = noalloc_mb.consume(m)
         torch.cuda.synchronize()
-        assert_bf16_close(bits(c_noalloc), bits(c_handle), f"C, call {call}")
-        assert_bf16_close(bits(out_noalloc), bits(out_handle), f"consumer output, call {call}")
+        assert (bits(c_noalloc) == bits(c_handle)).all(), f"C differs, call {call}"
+        assert (bits(out_noalloc) == bits(out_handle)).all(), f"consumer output differs, call {call}"
+        assert (between[call % 3, :m] == pack_words(sanitized(bits(c_handle)))).all(), call
         assert_bf16_close(bits(c_noalloc), oracle.gemm_bf16(w, ws, x, xs), f"vs oracle, call {call}")
         assert state_words(noalloc_mb) == state_words(handle_mb) == [(call + 1) % 3, call % 3, 0, 0]
         assert (mailbox_words(noalloc_mb) == oracle.SENTINEL).all()
+        gemm.close()
     assert noalloc_mb.status()[0] == OK
-    gemm.close()
 
 
 def test_noalloc_refuses_what_does_not_fit(cuda):
