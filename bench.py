@@ -51,6 +51,7 @@ WORKLOAD_CHOICES = {"headline": "HEADLINE", "graph": "GRAPH_8192", "chain": "CHA
 _WORKLOAD = "headline"
 GRAPH_STEPS = 30  # calls per captured graph (a multiple of every weight-copy count)
 SOAK_SECONDS = 2.0  # least time the clocks are sampled under the chain's load
+GATE_CYCLES = 100_000  # the spin before a timed region: about 50 us at 2 GHz
 WORKLOAD_CALLS = 6000  # timed calls of each other workload in the headline's line
 E2E_GRAPH_STEPS = 480  # end-to-end steps per captured graph (likewise)
 E2E_BATCH = 30         # end-to-end steps per wait on the input copies (divides E2E_GRAPH_STEPS)
@@ -371,11 +372,16 @@ class Chain:
         return self._graphs[steps]
 
     def prepare(self, *step_counts):
-        """Captures every graph that issue() will need for these counts."""
-        self.graph(GRAPH_STEPS)
-        for n in step_counts:
-            if n % GRAPH_STEPS:
-                self.graph(n % GRAPH_STEPS)
+        """Captures every graph that issue() will need for these counts and
+        replays each once, so no graph's first launch (which uploads it to
+        the device) falls inside a timed region."""
+        import torch
+
+        counts = {GRAPH_STEPS} | {n % GRAPH_STEPS for n in step_counts if n % GRAPH_STEPS}
+        with torch.cuda.stream(self.stream):
+            for n in sorted(counts):
+                self.graph(n).replay()
+        self.stream.synchronize()
 
     def issue(self, steps: int):
         """Exactly `steps` chained calls on the stream, from the graphs."""
@@ -389,11 +395,17 @@ class Chain:
                 self.graph(rest).replay()
 
     def timed(self, steps: int) -> float:
-        """Seconds of `steps` chained calls between CUDA events on the stream."""
+        """Seconds of `steps` chained calls between CUDA events on the stream.
+        A short spin kernel (about 50 us) holds the stream before the start
+        event, so the host has queued the first graph by the time the event
+        is reached: the device-side time then holds the calls' own work, not
+        the host's launch of the first graph onto an idle stream."""
         import torch
 
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.stream):
+            torch.cuda._sleep(GATE_CYCLES)
         e0.record(self.stream)
         self.issue(steps)
         e1.record(self.stream)
