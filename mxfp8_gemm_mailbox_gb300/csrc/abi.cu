@@ -39,6 +39,7 @@ struct mxfp8_publish_gemm {
   // Tensor map of the last activation buffer seen (x pointer, m).
   const void* x_cached;
   int m_cached;
+  int32_t x_pieces;  // tmap_x is the 3-D piece view (encode_x)
   CUtensorMap tmap_x;
 };
 
@@ -117,6 +118,34 @@ mxfp8_status encode_rows(CUtensorMap* map, const void* base, uint64_t inner, uin
   if (r != CUDA_SUCCESS)
     return fail(MXFP8_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(r));
   return MXFP8_OK;
+}
+
+// The activations' tensor map.  Folded tiles (fold > 1) read a stage's fold
+// consecutive 128-wide K pieces of the 8 rows; when K is a multiple of 128 a
+// 3-D view of x -- (k within a piece, row, piece), strides K and 128 bytes --
+// loads them in one box of 128 x 8 x fold, landing piece-major exactly as
+// fold boxes of the 2-D view would, so a stage costs one TMA request instead
+// of fold.  *pieces tells which view was encoded (the driver may refuse the
+// overlapping strides; the 2-D view serves then).
+mxfp8_status encode_x(CUtensorMap* map, const void* x, int k, int m, int fold, int32_t* pieces) {
+  *pieces = 0;
+  if (fold > 1 && k % kTileK == 0) {
+    EncodeTiled fn = encode_tiled();
+    if (!fn) return fail(MXFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kTileK), static_cast<cuuint64_t>(m),
+                          static_cast<cuuint64_t>(k / kTileK)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(kTileK)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(kRows),
+                         static_cast<cuuint32_t>(fold)};
+    cuuint32_t elem[3] = {1, 1, 1};
+    if (fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(x), dims, strides, box, elem,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+      *pieces = 1;
+      return MXFP8_OK;
+    }
+  }
+  return encode_rows(map, x, static_cast<uint64_t>(k), static_cast<uint64_t>(m), kRows);
 }
 
 mxfp8_status check_desc(const mxfp8_gemm_desc* d) {
@@ -350,7 +379,7 @@ mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale,
     return fail(MXFP8_ERR_INVALID, "the handle was created on device " + std::to_string(g->device) +
                                        ", the current device is " + std::to_string(device));
   if (g->x_cached != x || g->m_cached != m) {
-    st = encode_rows(&g->tmap_x, x, static_cast<uint64_t>(g->desc.k), static_cast<uint64_t>(m), kRows);
+    st = encode_x(&g->tmap_x, x, g->desc.k, m, g->desc.fold, &g->x_pieces);
     if (st != MXFP8_OK) return st;
     g->x_cached = x;
     g->m_cached = m;
@@ -371,6 +400,7 @@ mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale,
   p.pipes = g->desc.pipes;
   p.tmem_load = g->desc.tmem_load;
   p.fold = g->desc.fold;
+  p.x_pieces = g->x_pieces;
   p.tmem = g->tmem;
   p.x_scale = static_cast<const uint8_t*>(x_scale);
   p.w_sf = g->w_sf;
@@ -754,6 +784,7 @@ struct NoallocPlan {
   CUtensorMap tmap_w;
   const void* x;
   int m;
+  int32_t x_pieces;
   CUtensorMap tmap_x;
 };
 
@@ -824,8 +855,7 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
   auto refresh = [&](NoallocPlan* pl) {
     if (pl->x == x && pl->m == m) return MXFP8_OK;
     pl->x = nullptr;
-    const mxfp8_status s2 = encode_rows(&pl->tmap_x, x, static_cast<uint64_t>(pl->desc.k),
-                                        static_cast<uint64_t>(m), kRows);
+    const mxfp8_status s2 = encode_x(&pl->tmap_x, x, pl->desc.k, m, pl->desc.fold, &pl->x_pieces);
     if (s2 != MXFP8_OK) return s2;
     pl->x = x;
     pl->m = m;
@@ -851,6 +881,7 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
   p.pipes = d.pipes;
   p.tmem_load = d.tmem_load;
   p.fold = d.fold;
+  p.x_pieces = plan.x_pieces;
   p.tmem = plan.tmem;
   p.x_scale = static_cast<const uint8_t*>(x_scale);
   p.w_sf = scratch;

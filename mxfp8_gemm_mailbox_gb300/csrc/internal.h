@@ -67,6 +67,8 @@ struct GemmParams {
   int32_t tmem_load;        // MXFP8_TMEM_LOAD_32X32B or MXFP8_TMEM_LOAD_16X256B
   int32_t fold;             // K pieces stacked in the MMA's 128 rows: 1, 2, 4 (128/fold
                             // output columns per CTA)
+  int32_t x_pieces;         // 1: tmap_x is the 3-D piece view of x (a stage's F pieces
+                            // in one box); 0: the 2-D [m][k] view (one box per piece)
   TmemPlan tmem;
   const uint8_t* x_scale;   // [m][k/32]
   const uint8_t* w_sf;      // [n/R][k_tiles][512] tiled W scales (R = 128 / fold)

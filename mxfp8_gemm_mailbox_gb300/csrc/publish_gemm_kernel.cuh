@@ -272,12 +272,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                              tile * kTileRows, bar, pol_stream);
         }
       };
-      // The F activation tiles of a stage, rows >= m read as zero.
+      // The F activation tiles of a stage, rows >= m read as zero: one box of
+      // the 3-D piece view (128 K x 8 rows x F pieces, piece-major in shared
+      // memory, as F boxes of the 2-D view would land), or F 2-D boxes.
       auto load_x_tile = [&](uint32_t dst, int kt, uint32_t bar) {
+        if (F > 1 && p.x_pieces) {
+          ptx::tma_load_3d(dst, &tmap_x, 0, 0, kt * F, bar, pol_keep);
+        } else {
 #pragma unroll
-        for (int pc = 0; pc < F; ++pc)
-          ptx::tma_load_2d(dst + pc * kXTileBytes, &tmap_x, (kt * F + pc) * kTileK, 0, bar,
-                           pol_keep);
+          for (int pc = 0; pc < F; ++pc)
+            ptx::tma_load_2d(dst + pc * kXTileBytes, &tmap_x, (kt * F + pc) * kTileK, 0, bar,
+                             pol_keep);
+        }
       };
       // W and its scales do not depend on the previous kernel: start them now.
       for (int i = lane; i < npre; i += producers) {
