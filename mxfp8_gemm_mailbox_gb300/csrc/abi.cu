@@ -272,6 +272,24 @@ mxfp8_status ensure_smem_attribute(int device, int split_k, int fold, int bytes,
   return MXFP8_OK;
 }
 
+// The launch's shared-memory layout for a resolved descriptor.  With split-K
+// the partials from peers get a region of their own when it fits beside the
+// resolved ring (within the same per-SM budget the ring was sized for): a CTA
+// then sends its partials as soon as its main loop is done instead of waiting
+// at a cluster barrier until every peer's ring is dead.
+GemmSmemLayout launch_layout(const mxfp8_gemm_desc& d, int tiles_per_split,
+                             const DeviceLimits& lim) {
+  GemmSmemLayout layout = gemm_smem_layout(d.stages, d.split_k, tiles_per_split, d.fold);
+  if (d.split_k > 1) {
+    const int ctas = d.n / (kBlockN / d.fold) * d.split_k;
+    const int budget = ctas > lim.sms ? lim.smem_per_sm / 2 - 1024 : lim.smem_optin;
+    const GemmSmemLayout own =
+        gemm_smem_layout(d.stages, d.split_k, tiles_per_split, d.fold, true);
+    if (static_cast<int>(own.total) <= budget) layout = own;
+  }
+  return at_most_two_per_sm(layout, d.split_k, lim);
+}
+
 // Fill split_k, cta_k, stages, pipes and fold: split_k so the grid has about
 // one or two CTAs per SM; then the largest fold that keeps at most one CTA
 // per SM (one SM streams only so fast: few-CTA grids leave HBM idle); the
@@ -510,9 +528,7 @@ mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* 
   g->k_tiles = k_tiles_for_fold(desc->k, fold);
   g->tiles_per_split = (g->k_tiles + g->desc.split_k - 1) / g->desc.split_k;
   g->tmem = gemm_tmem_plan(g->desc.stages, g->desc.acc_blocks, fold);
-  g->layout = at_most_two_per_sm(
-      gemm_smem_layout(g->desc.stages, g->desc.split_k, g->tiles_per_split, fold),
-      g->desc.split_k, lim);
+  g->layout = launch_layout(g->desc, g->tiles_per_split, lim);
   g->x_cached = nullptr;
   g->m_cached = 0;
   st = encode_rows(&g->tmap_w, w, static_cast<uint64_t>(desc->k), static_cast<uint64_t>(desc->n),
@@ -574,8 +590,7 @@ mxfp8_status mxfp8_publish_gemm_plan(const mxfp8_gemm_desc* desc, int32_t sms,
   if (st != MXFP8_OK) return st;
   const int k_tiles = k_tiles_for_fold(d.k, d.fold);
   const int tiles_per_split = (k_tiles + d.split_k - 1) / d.split_k;
-  const GemmSmemLayout layout = at_most_two_per_sm(
-      gemm_smem_layout(d.stages, d.split_k, tiles_per_split, d.fold), d.split_k, lim);
+  const GemmSmemLayout layout = launch_layout(d, tiles_per_split, lim);
   if (resolved) *resolved = d;
   if (smem_bytes) *smem_bytes = static_cast<int32_t>(layout.total);
   if (tmem_columns)
@@ -842,8 +857,7 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
     pl->k_tiles = k_tiles_for_fold(d.k, d.fold);
     pl->tiles_per_split = (pl->k_tiles + d.split_k - 1) / d.split_k;
     pl->tmem = gemm_tmem_plan(d.stages, d.acc_blocks, d.fold);
-    pl->layout = at_most_two_per_sm(
-        gemm_smem_layout(d.stages, d.split_k, pl->tiles_per_split, d.fold), d.split_k, lim);
+    pl->layout = launch_layout(d, pl->tiles_per_split, lim);
     s2 = encode_rows(&pl->tmap_w, w, static_cast<uint64_t>(d.k), static_cast<uint64_t>(d.n),
                      kBlockN / d.fold);
     if (s2 != MXFP8_OK) return s2;

@@ -34,7 +34,9 @@ struct GemmSmemLayout {
   uint32_t x;         // stages x 1 KB activation tiles
   uint32_t sfa;       // stages x 512 B W scale chunks
   uint32_t ctile;     // 8 x 128 BF16 epilogue staging (inside the dead W ring)
-  uint32_t recv;      // split-K partials received from peers (inside the dead W ring)
+  uint32_t recv;      // split-K partials received from peers: in the dead W ring, or
+                      // a region of its own when recv_dedicated
+  uint32_t recv_dedicated;  // 1: peers may send before this CTA's main loop ends
   uint32_t sx;        // x scale chunks of this CTA's K range
   uint32_t bars;      // mbarriers
   uint32_t misc;      // tensor-memory base, generation broadcast
@@ -81,7 +83,8 @@ struct GemmParams {
   GemmSmemLayout smem;
 };
 
-GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, int fold);
+GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, int fold,
+                                bool dedicated_recv = false);
 TmemPlan gemm_tmem_plan(int stages, int acc_blocks, int fold);
 int k_tiles_for_fold(int k, int fold);  // ceil(k / (128 fold))
 

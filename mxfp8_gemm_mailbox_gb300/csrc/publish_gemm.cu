@@ -62,8 +62,8 @@ __global__ void tile_weights_kernel(const uint8_t* __restrict__ w, uint8_t* __re
 
 }  // namespace
 
-GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, int fold) {
-  (void)split_k;
+GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, int fold,
+                                bool dedicated_recv) {
   GemmSmemLayout L{};
   L.w = 0;
   L.x = L.w + stages * kWTileBytes;
@@ -83,6 +83,14 @@ GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, in
   L.bars = (L.sx + sx_bytes + 7u) & ~7u;
   L.misc = L.bars + static_cast<uint32_t>(2 * stages + 2 * kMaxAccRing + 2) * 8u;
   L.total = L.misc + 16u + 1024u;
+  if (dedicated_recv && split_k > 1) {
+    // The partials' own region ((S-1) x 128 x 8/S pairs of 8 bytes, at most
+    // 7 KB), so a peer can send them as soon as its own main loop is done.
+    L.recv = L.misc + 16u;
+    L.recv_dedicated = 1;
+    L.total = L.recv + static_cast<uint32_t>((split_k - 1) * kBlockN * (kRows / split_k) * 8) +
+              1024u;
+  }
   return L;
 }
 

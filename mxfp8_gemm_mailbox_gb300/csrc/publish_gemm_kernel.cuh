@@ -420,7 +420,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   if (warp < 2 || warp >= 6) {
     __syncwarp();
     if (S > 1) {
-      ptx::cluster_sync();    // matches the epilogue's barrier before the exchange
+      if (!p.smem.recv_dedicated)
+        ptx::cluster_sync();  // matches the epilogue's barrier before the exchange
       ptx::cluster_arrive();  // these warps address no peer: the final barrier's arrival
     }
   } else {
@@ -656,7 +657,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         constexpr int kRun = kPerLane < kShard ? kPerLane : kShard;
         constexpr int kRuns = kPerLane / kRun;
         static_assert(kRun % 2 == 0, "runs go out as 16-byte stores of two pairs");
-        ptx::cluster_sync();  // every peer's W ring is dead before any remote store
+        // A receive buffer in the W ring is dead only once every CTA of the
+        // cluster has finished its main loop; one of its own needs no barrier
+        // (a peer's bytes may land before this CTA's expect: the transaction
+        // count runs negative until then).
+        if (!p.smem.recv_dedicated) ptx::cluster_sync();
         if (etid == 0)
           ptx::mbar_arrive_expect_tx(bar_recv,
                                      static_cast<uint32_t>((S - 1) * kTileRows * kShard * 8));
@@ -715,9 +720,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       float own_hi[kShard], own_lo[kShard];
       if constexpr (S > 1) {
         constexpr int kPairBytes = kShard * 8;
-        // The receive buffer lives in the W ring, which is dead only once every
-        // CTA of the cluster has finished its main loop.
-        ptx::cluster_sync();
+        // A receive buffer in the W ring is dead only once every CTA of the
+        // cluster has finished its main loop; one of its own needs no barrier
+        // (a peer's bytes may land before this CTA's expect: the transaction
+        // count runs negative until then).
+        if (!p.smem.recv_dedicated) ptx::cluster_sync();
         if (etid == 0)
           ptx::mbar_arrive_expect_tx(bar_recv,
                                      static_cast<uint32_t>((S - 1) * kTileRows * kPairBytes));

@@ -20,7 +20,7 @@ def test_plans_of_the_benchmarked_workloads():
         (7168, 16384, 4): dict(fold=1, stages=6, pipes=2, l2_prefetch=16, l2_prefetch_early=4,
                                smem_bytes=113280, tmem_columns=128, grid_ctas=224),
         (7168, 8192, 2): dict(fold=1, stages=12, pipes=4, l2_prefetch=16, l2_prefetch_early=-1,
-                              smem_bytes=220896, tmem_columns=256, grid_ctas=112),
+                              smem_bytes=224992, tmem_columns=256, grid_ctas=112),
         (4096, 4096, 1): dict(fold=4, stages=8, pipes=4, l2_prefetch=16, l2_prefetch_early=-1,
                               smem_bytes=173728, tmem_columns=256, grid_ctas=128),
         (256, 256, 1): dict(fold=2, stages=2, pipes=2, grid_ctas=4),
@@ -162,3 +162,16 @@ def test_gemm_wait_limit_field():
     a, b = plan_gemm(7168, 8192, split_k=2), plan_gemm(7168, 8192, split_k=2, wait_limit_ms=5)
     assert {k: v for k, v in a.items() if k != "wait_limit_ms"} == \
         {k: v for k, v in b.items() if k != "wait_limit_ms"}
+
+
+def test_split_k_receive_buffer_of_its_own_where_it_fits():
+    # With split-K the peers' partials get a region of their own (so a CTA can
+    # send as soon as its main loop is done) when it fits beside the resolved
+    # ring within the ring's per-SM budget: N=7168, K=8192, S=2 (one CTA per
+    # SM) takes (2-1) x 128 x 4 x 8 = 4096 more bytes than its ring layout; the
+    # headline (two CTAs per SM, 6-stage ring) has no room for 6144 and keeps
+    # the partials in its dead W ring.
+    assert plan_gemm(7168, 8192, split_k=2)["smem_bytes"] == 220896 + 4096
+    assert plan_gemm(7168, 16384, split_k=4)["smem_bytes"] == 113280
+    # unsplit launches have no partials to exchange
+    assert plan_gemm(4096, 4096, split_k=1)["smem_bytes"] == 173728
