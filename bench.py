@@ -59,6 +59,7 @@ FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("mxfp8_gemm_mailbox_gb300/csrc/publish_gemm_kernel.cuh",
                   "mxfp8_gemm_mailbox_gb300/csrc/publish_gemm.cu",
                   "mxfp8_gemm_mailbox_gb300/csrc/publish_gemm_fold.cu",
+                  "mxfp8_gemm_mailbox_gb300/csrc/publish_gemm_k256.cu",
                   "mxfp8_gemm_mailbox_gb300/csrc/ptx.cuh",
                   "mxfp8_gemm_mailbox_gb300/csrc/abi.cu")
 TRAFFIC_FILE = ROOT / "profiles" / "publish_gemm_headline_traffic.json"

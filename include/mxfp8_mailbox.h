@@ -89,7 +89,18 @@ typedef struct mxfp8_gemm_desc {
                          4 where both fit, so never chosen); 0 = choose among 1, 2,
                          4: the largest with at most two CTAs per SM and >= 2 K
                          tiles per split                                               */
-  int32_t cta_k;      /* K elements per pipeline stage: 128 (0 = 128)                */
+  int32_t cta_k;      /* K per pipeline stage, in units of fold: 128 (0 = 128) or 256.
+                         With 256 a stage holds two 128-wide K tiles (128 fold K each)
+                         that share one full and one empty barrier and come in one W
+                         copy, one W-scale copy and one x load; accumulator and scale
+                         slots stay per tile, so the results are bit-identical to
+                         128's.  256 takes fold 1, 2 or 4, split_k 1, 2 or 4,
+                         acc_blocks 4, the 32x32b read-out, and pipes such that
+                         2 x pipes divides the accumulator ring (8 slots; 4 at fold 4,
+                         so at most 2 pipes there).  `stages` then counts 256-wide
+                         stages.  Measured on GB300: 2-6 % less GEMM time at
+                         K = 2048, slower at K >= 4096 (fold 4's 2 pipes, shorter
+                         rings), so 0 chooses 128.                                     */
   int32_t stages;     /* shared-memory ring depth: 2..16 (0 = choose)                */
   int32_t acc_blocks; /* K blocks per promoted partial sum: 1 or 4 (0 = 4)           */
   int32_t w_layout;   /* MXFP8_W_IN_PLACE or MXFP8_W_TILED (0 = choose)              */

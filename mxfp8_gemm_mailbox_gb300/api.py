@@ -129,11 +129,11 @@ GB300_LIMITS = (152, 233472, 232448)
 def plan_gemm(n: int, k: int, capacity_m: int = 8, split_k: int = 0, stages: int = 0,
               acc_blocks: int = 0, w_layout: int = 0, l2_prefetch: int = 0, pipes: int = 0,
               tmem_load: int = 0, fold: int = 0, l2_prefetch_early: int = 0,
-              wait_limit_ms: int = 0, limits: tuple = GB300_LIMITS) -> dict:
+              wait_limit_ms: int = 0, cta_k: int = 0, limits: tuple = GB300_LIMITS) -> dict:
     """The tactic PublishGemm would resolve for this shape on a device with
     `limits` = (SMs, shared memory per SM, shared memory per CTA), as
     PublishGemm.config() reports it; needs no GPU."""
-    desc = GemmDesc(n, k, capacity_m, split_k, 0, stages, acc_blocks, w_layout, l2_prefetch,
+    desc = GemmDesc(n, k, capacity_m, split_k, cta_k, stages, acc_blocks, w_layout, l2_prefetch,
                     pipes, tmem_load, fold, l2_prefetch_early, wait_limit_ms)
     out = GemmDesc()
     smem, tmem, grid = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
@@ -157,7 +157,8 @@ class PublishGemm:
     def __init__(self, w: torch.Tensor, w_scale: torch.Tensor, mailbox: Mailbox,
                  split_k: int = 0, stages: int = 0, acc_blocks: int = 0, w_layout: int = 0,
                  l2_prefetch: int = 0, pipes: int = 0, tmem_load: int = 0, fold: int = 0,
-                 l2_prefetch_early: int = 0, wait_limit_ms: int = 0, stream=None):
+                 l2_prefetch_early: int = 0, wait_limit_ms: int = 0, cta_k: int = 0,
+                 stream=None):
         lib = _lib.load()
         if w.dim() != 2:
             raise ValueError(f"w must be [N][K], got {tuple(w.shape)}")
@@ -165,8 +166,8 @@ class PublishGemm:
         _codes(w, "w", k)
         if k % 32 == 0:  # other K are refused by the library below
             _codes(w_scale, "w_scale", k // 32, min_rows=n)
-        self.desc = GemmDesc(n, k, mailbox.capacity, split_k, 0, stages, acc_blocks, w_layout,
-                             l2_prefetch, pipes, tmem_load, fold, l2_prefetch_early,
+        self.desc = GemmDesc(n, k, mailbox.capacity, split_k, cta_k, stages, acc_blocks,
+                             w_layout, l2_prefetch, pipes, tmem_load, fold, l2_prefetch_early,
                              wait_limit_ms)
         ws_bytes = lib.mxfp8_publish_gemm_workspace_bytes(ctypes.byref(self.desc))
         if ws_bytes == 0:

@@ -19,8 +19,8 @@ CSRC = PACKAGE / "csrc"
 INCLUDE = ROOT / "include"
 BUILD_DIR = PACKAGE / "_build"
 LIBRARY = PACKAGE / "libmxfp8_mailbox.so"
-SOURCES = ("publish_gemm.cu", "publish_gemm_fold.cu", "mailbox.cu", "lamport_gather.cu",
-           "tagged_mailbox.cu", "abi.cu")
+SOURCES = ("publish_gemm.cu", "publish_gemm_fold.cu", "publish_gemm_k256.cu", "mailbox.cu",
+           "lamport_gather.cu", "tagged_mailbox.cu", "abi.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

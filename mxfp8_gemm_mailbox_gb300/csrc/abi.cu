@@ -129,7 +129,7 @@ mxfp8_status encode_rows(CUtensorMap* map, const void* base, uint64_t inner, uin
 // overlapping strides; the 2-D view serves then).
 mxfp8_status encode_x(CUtensorMap* map, const void* x, int k, int m, int fold, int32_t* pieces) {
   *pieces = 0;
-  if (fold > 1 && k % kTileK == 0) {
+  if (fold > 1 && k % kTileK == 0) {  // fold here: the pieces of one stage (fold x K tiles)
     EncodeTiled fn = encode_tiled();
     if (!fn) return fail(MXFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kTileK), static_cast<cuuint64_t>(m),
@@ -160,7 +160,16 @@ mxfp8_status check_desc(const mxfp8_gemm_desc* d) {
   if (d->split_k != 0 && d->split_k != 1 && d->split_k != 2 && d->split_k != 4 &&
       d->split_k != 8)
     return fail(MXFP8_ERR_UNSUPPORTED, "split_k must be 1, 2, 4 or 8 (or 0 to choose)");
-  if (d->cta_k != 0 && d->cta_k != kTileK) return fail(MXFP8_ERR_UNSUPPORTED, "cta_k must be 128");
+  if (d->cta_k != 0 && d->cta_k != kTileK && d->cta_k != 2 * kTileK)
+    return fail(MXFP8_ERR_UNSUPPORTED, "cta_k must be 128 or 256 (or 0 for 128)");
+  if (d->cta_k == 2 * kTileK) {
+    if (d->fold == 8) return fail(MXFP8_ERR_UNSUPPORTED, "cta_k 256 takes fold 1, 2 or 4");
+    if (d->split_k == 8) return fail(MXFP8_ERR_UNSUPPORTED, "cta_k 256 takes split_k 1, 2 or 4");
+    if (d->acc_blocks == 1)
+      return fail(MXFP8_ERR_UNSUPPORTED, "cta_k 256 takes acc_blocks 4 (one slot per K tile)");
+    if (d->tmem_load == MXFP8_TMEM_LOAD_16X256B)
+      return fail(MXFP8_ERR_UNSUPPORTED, "cta_k 256 reads accumulators with 32x32b");
+  }
   if (d->stages != 0 && (d->stages < 2 || d->stages > kMaxStages))
     return fail(MXFP8_ERR_UNSUPPORTED, "stages must be in 2..16 (or 0 to choose)");
   if (d->acc_blocks != 0 && d->acc_blocks != 1 && d->acc_blocks != 4)
@@ -254,19 +263,21 @@ GemmSmemLayout at_most_two_per_sm(GemmSmemLayout layout, int split_k, const Devi
 // that was torn down and re-created gets it back).
 constexpr int kMaxDevicesTracked = 64;
 
-mxfp8_status ensure_smem_attribute(int device, int split_k, int fold, int bytes, bool force) {
+mxfp8_status ensure_smem_attribute(int device, int split_k, int fold, int tiles_per_stage,
+                                   int bytes, bool force) {
   static std::mutex mutex;
-  // [device][log2 split_k][log2 fold]: split_k and fold are 1, 2, 4 or 8.
-  static int raised[kMaxDevicesTracked][4][4] = {};
+  // [device][log2 split_k][log2 fold][tiles per stage - 1]: split_k and fold
+  // are 1, 2, 4 or 8, tiles per stage 1 or 2.
+  static int raised[kMaxDevicesTracked][4][4][2] = {};
   if (device < 0 || device >= kMaxDevicesTracked)
     return fail(MXFP8_ERR_UNSUPPORTED, "device ordinal out of range for the launch table");
   const int si = split_k == 8 ? 3 : split_k / 2;
   const int fi = fold == 8 ? 3 : fold / 2;
   std::lock_guard<std::mutex> lock(mutex);
-  int& have = raised[device][si][fi];
+  int& have = raised[device][si][fi][tiles_per_stage == 2 ? 1 : 0];
   if (!force && have >= bytes) return MXFP8_OK;
   const int want = std::max(have, bytes);
-  const cudaError_t e = set_gemm_smem_attribute(split_k, fold, want);
+  const cudaError_t e = set_gemm_smem_attribute(split_k, fold, want, tiles_per_stage);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
   have = want;
   return MXFP8_OK;
@@ -279,12 +290,13 @@ mxfp8_status ensure_smem_attribute(int device, int split_k, int fold, int bytes,
 // at a cluster barrier until every peer's ring is dead.
 GemmSmemLayout launch_layout(const mxfp8_gemm_desc& d, int tiles_per_split,
                              const DeviceLimits& lim) {
-  GemmSmemLayout layout = gemm_smem_layout(d.stages, d.split_k, tiles_per_split, d.fold);
+  const int T = d.cta_k / kTileK;
+  GemmSmemLayout layout = gemm_smem_layout(d.stages, d.split_k, tiles_per_split, d.fold, false, T);
   if (d.split_k > 1) {
     const int ctas = d.n / (kBlockN / d.fold) * d.split_k;
     const int budget = ctas > lim.sms ? lim.smem_per_sm / 2 - 1024 : lim.smem_optin;
     const GemmSmemLayout own =
-        gemm_smem_layout(d.stages, d.split_k, tiles_per_split, d.fold, true);
+        gemm_smem_layout(d.stages, d.split_k, tiles_per_split, d.fold, true, T);
     if (static_cast<int>(own.total) <= budget) layout = own;
   }
   return at_most_two_per_sm(layout, d.split_k, lim);
@@ -306,7 +318,8 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
       if (tiles * cand <= 2 * lim.sms && k_tiles1 >= 2 * cand) s = cand;
     d->split_k = s;
   }
-  d->cta_k = kTileK;
+  if (d->cta_k == 0) d->cta_k = kTileK;
+  const int T = d->cta_k / kTileK;  // K tiles per pipeline stage
   if (d->wait_limit_ms == 0) d->wait_limit_ms = kDefaultGemmWaitLimitMs;
   if (d->acc_blocks == 0) d->acc_blocks = 4;
   if (d->tmem_load == 0) d->tmem_load = MXFP8_TMEM_LOAD_32X32B;
@@ -319,7 +332,8 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
       // Fold 8 (unsplit, two pipes at most) pays from 8 stages per CTA on
       // (measured on GB300, N=2048, S=1: K=4096 6.29 vs 6.00 us at fold 4,
       // K=8192 7.86 vs 8.79, K=16384 11.46 vs 13.60).
-      if (cand == 8 && (d->split_k != 1 || d->pipes == 4 || k_tiles_for_fold(d->k, 8) < 8))
+      if (cand == 8 &&
+          (d->split_k != 1 || d->pipes == 4 || k_tiles_for_fold(d->k, 8) < 8 || T != 1))
         continue;
       if (foldable && tiles * d->split_k * cand <= lim.sms &&
           k_tiles_for_fold(d->k, cand) * cand == k_tiles1 &&  // no more K padding
@@ -344,27 +358,38 @@ mxfp8_status resolve_tactic(mxfp8_gemm_desc* d, const DeviceLimits& lim) {
   if (d->stages == 0) {
     int best = 0;
     for (int s = 2; s <= kMaxStages; ++s) {
-      if (static_cast<int>(gemm_smem_layout(s, d->split_k, tps, d->fold).total) > budget) break;
-      if (gemm_tmem_plan(s, d->acc_blocks, d->fold).cols > kMaxTmemCols) break;
+      if (static_cast<int>(gemm_smem_layout(s, d->split_k, tps, d->fold, false, T).total) >
+          budget)
+        break;
+      if (gemm_tmem_plan(s, d->acc_blocks, d->fold, T).cols > kMaxTmemCols) break;
       best = s;
-      if (s >= tps) break;  // more stages than K tiles buy nothing
+      if (s * T >= tps) break;  // more stages than K tiles buy nothing
     }
     if (best == 0) return fail(MXFP8_ERR_UNSUPPORTED, "no stage count fits in shared memory");
     const int unit = (per_sm == 1 && best >= 4) ? 4 : (best >= 2 ? 2 : 1);
     best -= best % unit;
     d->stages = best;
   }
-  if (static_cast<int>(gemm_smem_layout(d->stages, d->split_k, tps, d->fold).total) >
+  if (static_cast<int>(gemm_smem_layout(d->stages, d->split_k, tps, d->fold, false, T).total) >
       lim.smem_optin)
     return fail(MXFP8_ERR_UNSUPPORTED, "the requested stages do not fit in shared memory");
-  if (gemm_tmem_plan(d->stages, d->acc_blocks, d->fold).cols > kMaxTmemCols)
+  const TmemPlan tmem = gemm_tmem_plan(d->stages, d->acc_blocks, d->fold, T);
+  if (tmem.cols > kMaxTmemCols)
     return fail(MXFP8_ERR_UNSUPPORTED, "the requested stages do not fit in tensor memory");
+  // Every accumulator slot keeps one issuer: the ring (of K tiles) is a
+  // multiple of the K tiles the issuers take per round, T pipes.
+  const int acc_ring = static_cast<int>(tmem.acc_ring);
   if (d->pipes == 0) {
     d->pipes = (per_sm == 1 && d->stages % 4 == 0 && d->fold != 8) ? 4
                : (d->stages % 2 == 0 ? 2 : 1);
+    while (d->pipes > 1 && acc_ring % (T * d->pipes) != 0) d->pipes /= 2;
   } else if (d->stages % d->pipes != 0) {
     return fail(MXFP8_ERR_UNSUPPORTED, "pipes must divide stages (stage i and its ring slots "
                                        "belong to pipe i % pipes)");
+  } else if (acc_ring % (T * d->pipes) != 0) {
+    return fail(MXFP8_ERR_UNSUPPORTED,
+                "with cta_k 256 the accumulator ring (" + std::to_string(acc_ring) +
+                    " slots) must be a multiple of 2 x pipes");
   }
   return MXFP8_OK;
 }
@@ -397,7 +422,8 @@ mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale,
     return fail(MXFP8_ERR_INVALID, "the handle was created on device " + std::to_string(g->device) +
                                        ", the current device is " + std::to_string(device));
   if (g->x_cached != x || g->m_cached != m) {
-    st = encode_x(&g->tmap_x, x, g->desc.k, m, g->desc.fold, &g->x_pieces);
+    st = encode_x(&g->tmap_x, x, g->desc.k, m, g->desc.fold * (g->desc.cta_k / kTileK),
+                  &g->x_pieces);
     if (st != MXFP8_OK) return st;
     g->x_cached = x;
     g->m_cached = m;
@@ -419,6 +445,7 @@ mxfp8_status run_gemm(mxfp8_publish_gemm* g, const void* x, const void* x_scale,
   p.tmem_load = g->desc.tmem_load;
   p.fold = g->desc.fold;
   p.x_pieces = g->x_pieces;
+  p.tiles_per_stage = g->desc.cta_k / kTileK;
   p.tmem = g->tmem;
   p.x_scale = static_cast<const uint8_t*>(x_scale);
   p.w_sf = g->w_sf;
@@ -527,7 +554,7 @@ mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* 
   g->first_launch_pending = true;
   g->k_tiles = k_tiles_for_fold(desc->k, fold);
   g->tiles_per_split = (g->k_tiles + g->desc.split_k - 1) / g->desc.split_k;
-  g->tmem = gemm_tmem_plan(g->desc.stages, g->desc.acc_blocks, fold);
+  g->tmem = gemm_tmem_plan(g->desc.stages, g->desc.acc_blocks, fold, g->desc.cta_k / kTileK);
   g->layout = launch_layout(g->desc, g->tiles_per_split, lim);
   g->x_cached = nullptr;
   g->m_cached = 0;
@@ -537,8 +564,8 @@ mxfp8_status mxfp8_publish_gemm_create(const mxfp8_gemm_desc* desc, const void* 
     delete g;
     return st;
   }
-  st = ensure_smem_attribute(device, g->desc.split_k, fold, static_cast<int>(g->layout.total),
-                             false);
+  st = ensure_smem_attribute(device, g->desc.split_k, fold, g->desc.cta_k / kTileK,
+                             static_cast<int>(g->layout.total), false);
   if (st != MXFP8_OK) {
     delete g;
     return st;
@@ -594,7 +621,8 @@ mxfp8_status mxfp8_publish_gemm_plan(const mxfp8_gemm_desc* desc, int32_t sms,
   if (resolved) *resolved = d;
   if (smem_bytes) *smem_bytes = static_cast<int32_t>(layout.total);
   if (tmem_columns)
-    *tmem_columns = static_cast<int32_t>(gemm_tmem_plan(d.stages, d.acc_blocks, d.fold).cols);
+    *tmem_columns =
+        static_cast<int32_t>(gemm_tmem_plan(d.stages, d.acc_blocks, d.fold, d.cta_k / kTileK).cols);
   if (grid_ctas) *grid_ctas = (d.n / (kBlockN / d.fold)) * d.split_k;
   return MXFP8_OK;
 }
@@ -605,7 +633,8 @@ mxfp8_status mxfp8_publish_gemm_precompile(mxfp8_publish_gemm* gemm, int32_t m) 
   if (st != MXFP8_OK) return st;
   if (!encode_tiled()) return fail(MXFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   return ensure_smem_attribute(gemm->device, gemm->desc.split_k, gemm->desc.fold,
-                               static_cast<int>(gemm->layout.total), true);
+                               gemm->desc.cta_k / kTileK, static_cast<int>(gemm->layout.total),
+                               true);
 }
 
 mxfp8_status mxfp8_publish_gemm_run(mxfp8_publish_gemm* gemm, const void* x, const void* x_scale,
@@ -856,20 +885,21 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
     pl->desc = d;
     pl->k_tiles = k_tiles_for_fold(d.k, d.fold);
     pl->tiles_per_split = (pl->k_tiles + d.split_k - 1) / d.split_k;
-    pl->tmem = gemm_tmem_plan(d.stages, d.acc_blocks, d.fold);
+    pl->tmem = gemm_tmem_plan(d.stages, d.acc_blocks, d.fold, d.cta_k / kTileK);
     pl->layout = launch_layout(d, pl->tiles_per_split, lim);
     s2 = encode_rows(&pl->tmap_w, w, static_cast<uint64_t>(d.k), static_cast<uint64_t>(d.n),
                      kBlockN / d.fold);
     if (s2 != MXFP8_OK) return s2;
     pl->x = nullptr;
     pl->m = 0;
-    return ensure_smem_attribute(device, d.split_k, d.fold, static_cast<int>(pl->layout.total),
-                                 false);
+    return ensure_smem_attribute(device, d.split_k, d.fold, d.cta_k / kTileK,
+                                 static_cast<int>(pl->layout.total), false);
   };
   auto refresh = [&](NoallocPlan* pl) {
     if (pl->x == x && pl->m == m) return MXFP8_OK;
     pl->x = nullptr;
-    const mxfp8_status s2 = encode_x(&pl->tmap_x, x, pl->desc.k, m, pl->desc.fold, &pl->x_pieces);
+    const mxfp8_status s2 = encode_x(&pl->tmap_x, x, pl->desc.k, m,
+                                     pl->desc.fold * (pl->desc.cta_k / kTileK), &pl->x_pieces);
     if (s2 != MXFP8_OK) return s2;
     pl->x = x;
     pl->m = m;
@@ -896,6 +926,7 @@ extern "C" mxfp8_status mxfp8_publish_gemm_run_noalloc(const mxfp8_gemm_desc* de
   p.tmem_load = d.tmem_load;
   p.fold = d.fold;
   p.x_pieces = plan.x_pieces;
+  p.tiles_per_stage = d.cta_k / kTileK;
   p.tmem = plan.tmem;
   p.x_scale = static_cast<const uint8_t*>(x_scale);
   p.w_sf = scratch;

@@ -56,7 +56,7 @@ struct TmemPlan {
 
 struct GemmParams {
   int32_t n, k, m;
-  int32_t k_tiles;          // stages of K: ceil(k / (128 fold))
+  int32_t k_tiles;          // K tiles: ceil(k / (128 fold))
   int32_t tiles_per_split;  // ceil(k_tiles / split_k)
   int32_t stages;
   int32_t capacity;
@@ -69,8 +69,10 @@ struct GemmParams {
   int32_t tmem_load;        // MXFP8_TMEM_LOAD_32X32B or MXFP8_TMEM_LOAD_16X256B
   int32_t fold;             // K pieces stacked in the MMA's 128 rows: 1, 2, 4 (128/fold
                             // output columns per CTA)
-  int32_t x_pieces;         // 1: tmap_x is the 3-D piece view of x (a stage's F pieces
-                            // in one box); 0: the 2-D [m][k] view (one box per piece)
+  int32_t x_pieces;         // 1: tmap_x is the 3-D piece view of x (a stage's F x
+                            // tiles_per_stage pieces in one box); 0: the 2-D [m][k]
+                            // view (one box per piece)
+  int32_t tiles_per_stage;  // K tiles per pipeline stage: 1 (cta_k 128) or 2 (256)
   TmemPlan tmem;
   const uint8_t* x_scale;   // [m][k/32]
   const uint8_t* w_sf;      // [n/R][k_tiles][512] tiled W scales (R = 128 / fold)
@@ -83,9 +85,11 @@ struct GemmParams {
   GemmSmemLayout smem;
 };
 
+// tiles_per_stage: 128-wide K tiles (of 128 fold K each) in one pipeline
+// stage: 1 (cta_k 128) or 2 (cta_k 256).
 GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, int fold,
-                                bool dedicated_recv = false);
-TmemPlan gemm_tmem_plan(int stages, int acc_blocks, int fold);
+                                bool dedicated_recv = false, int tiles_per_stage = 1);
+TmemPlan gemm_tmem_plan(int stages, int acc_blocks, int fold, int tiles_per_stage = 1);
 int k_tiles_for_fold(int k, int fold);  // ceil(k / (128 fold))
 
 // Kernel launchers (return the CUDA error of the launch).  The GEMM's
@@ -95,11 +99,17 @@ int k_tiles_for_fold(int k, int fold);  // ceil(k / (128 fold))
 cudaError_t launch_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
                                 const GemmParams& p, int split_k, cudaStream_t stream,
                                 bool programmatic);
-cudaError_t set_gemm_smem_attribute(int split_k, int fold, int bytes);
+cudaError_t set_gemm_smem_attribute(int split_k, int fold, int bytes, int tiles_per_stage);
 cudaError_t launch_folded_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
                                        const GemmParams& p, int split_k, cudaStream_t stream,
                                        bool programmatic);
 cudaError_t set_folded_gemm_smem_attribute(int split_k, int fold, int bytes);
+// The cta_k 256 kernels (two K tiles per pipeline stage): fold 1, 2 or 4,
+// split_k 1, 2 or 4, the 32x32b read-out.
+cudaError_t launch_wide_stage_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
+                                           const GemmParams& p, int split_k, cudaStream_t stream,
+                                           bool programmatic);
+cudaError_t set_wide_stage_gemm_smem_attribute(int split_k, int fold, int bytes);
 cudaError_t launch_relayout_w_scales(const uint8_t* w_scale, uint8_t* w_sf, int n, int k,
                                      int fold, cudaStream_t stream);
 cudaError_t launch_tile_weights(const uint8_t* w, uint8_t* w_tiled, int n, int k, int fold,

@@ -63,11 +63,12 @@ __global__ void tile_weights_kernel(const uint8_t* __restrict__ w, uint8_t* __re
 }  // namespace
 
 GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, int fold,
-                                bool dedicated_recv) {
+                                bool dedicated_recv, int tiles_per_stage) {
   GemmSmemLayout L{};
+  const int ring_tiles = stages * tiles_per_stage;  // K tiles the rings hold
   L.w = 0;
-  L.x = L.w + stages * kWTileBytes;
-  L.sfa = L.x + stages * kXTileBytes * fold;
+  L.x = L.w + ring_tiles * kWTileBytes;
+  L.sfa = L.x + ring_tiles * kXTileBytes * fold;
   // Written only after the main loop: the epilogue's BF16 tile in W stage 0,
   // the split-K partials from peers ((S-1) x 8/S x 128 x 8 bytes <= 6 KB) in
   // W stage 1 (every ring has at least two stages).
@@ -77,7 +78,7 @@ GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, in
   // to a row past 32 columns: 128 fold bytes, 512 at fold 8), plus the 384
   // bytes the copy of the last chunk reads past it (rows that feed no kept
   // column).
-  L.sx = L.sfa + stages * kSfChunkBytes;
+  L.sx = L.sfa + ring_tiles * kSfChunkBytes;
   const uint32_t sx_chunk = 16u * static_cast<uint32_t>(std::min(32, kRows * fold));
   const uint32_t sx_bytes = static_cast<uint32_t>(tiles_per_split) * sx_chunk + 384u;
   L.bars = (L.sx + sx_bytes + 7u) & ~7u;
@@ -94,7 +95,7 @@ GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, in
   return L;
 }
 
-TmemPlan gemm_tmem_plan(int stages, int acc_blocks, int fold) {
+TmemPlan gemm_tmem_plan(int stages, int acc_blocks, int fold, int tiles_per_stage) {
   TmemPlan t{};
   t.acc = 0;
   const uint32_t block_cols = static_cast<uint32_t>(kRows * fold);  // one MMA's N
@@ -104,15 +105,18 @@ TmemPlan gemm_tmem_plan(int stages, int acc_blocks, int fold) {
   t.acc_ring = fold == 8 ? 2u
                : (acc_blocks == 1 || fold == 4) ? 4u
                                                 : static_cast<uint32_t>(kMaxAccRing);
+  // One 4-column W-scale and x-scale slot per K tile the ring holds.
+  const uint32_t ring_tiles = static_cast<uint32_t>(stages * tiles_per_stage);
   t.sfa = t.acc + t.acc_slot * t.acc_ring;
-  t.sfb = t.sfa + 4u * static_cast<uint32_t>(stages);
-  const uint32_t used = t.sfb + 4u * static_cast<uint32_t>(stages);
+  t.sfb = t.sfa + 4u * ring_tiles;
+  const uint32_t used = t.sfb + 4u * ring_tiles;
   t.cols = 32;
   while (t.cols < used) t.cols <<= 1;
   return t;
 }
 
-cudaError_t set_gemm_smem_attribute(int split_k, int fold, int bytes) {
+cudaError_t set_gemm_smem_attribute(int split_k, int fold, int bytes, int tiles_per_stage) {
+  if (tiles_per_stage == 2) return set_wide_stage_gemm_smem_attribute(split_k, fold, bytes);
   if (fold != 1) return set_folded_gemm_smem_attribute(split_k, fold, bytes);
   cudaError_t e = cudaSuccess;
   switch (split_k) {
@@ -136,6 +140,8 @@ cudaError_t set_gemm_smem_attribute(int split_k, int fold, int bytes) {
 cudaError_t launch_publish_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x,
                                 const GemmParams& p, int split_k, cudaStream_t stream,
                                 bool programmatic) {
+  if (p.tiles_per_stage == 2)
+    return launch_wide_stage_publish_gemm(tmap_w, tmap_x, p, split_k, stream, programmatic);
   if (p.fold != 1)
     return launch_folded_publish_gemm(tmap_w, tmap_x, p, split_k, stream, programmatic);
   const bool wide = p.tmem_load == MXFP8_TMEM_LOAD_16X256B;

@@ -50,9 +50,15 @@
 //
 // Tensor-memory columns: [acc, +acc_ring * acc_slot) the accumulator ring (FP32,
 // lane = MMA row, column = block * 8 F + piece * 8 + token); then the W and x
-// scale rings, one 4-column slot per stage each, filled by tcgen05.cp
-// (32x128b, multicast to the four lane quarters) from 16-byte-row scale chunks
-// in shared memory.  Every scale address is 4-column aligned.
+// scale rings, one 4-column slot per K tile of the shared-memory ring each,
+// filled by tcgen05.cp (32x128b, multicast to the four lane quarters) from
+// 16-byte-row scale chunks in shared memory.  Every scale address is 4-column
+// aligned.
+//
+// Stages of two K tiles (T = 2, cta_k 256): a stage's two tiles share one
+// full and one empty barrier and arrive with one W copy, one W-scale copy and
+// one x load; each tile keeps its own accumulator slot and scale slots, so
+// the sums run in the same order and the bits match T = 1.
 //
 // The kernel template lives in this header so its instantiations can be
 // spread over translation units that compile in parallel: publish_gemm.cu
@@ -165,17 +171,24 @@ struct RingCursor {
 
 // kWideLoad: accumulators read with tcgen05.ld 16x256b (else 32x32b); a
 // template parameter so each read-out compiles to its own kernel.  F: the
-// fold (K pieces stacked in the MMA's rows).
-template <int S, bool kWideLoad, int F>
+// fold (K pieces stacked in the MMA's rows).  T: K tiles (of 128 F K each)
+// per pipeline stage, 1 or 2 (cta_k 128 or 256): a stage's tiles share one
+// full and one empty barrier and come in one W copy, one W-scale copy and
+// one x load; accumulator slots, scale slots and the epilogue stay per tile.
+template <int S, bool kWideLoad, int F, int T>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     publish_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_x,
                         const __grid_constant__ GemmParams p) {
   static_assert(F == 1 || F == 2 || F == 4 || F == 8, "the fold divides the 128 MMA rows");
   static_assert(F == 1 || !kWideLoad, "folded tiles read accumulators with 32x32b");
+  static_assert(T == 1 || (T == 2 && !kWideLoad && F <= 4),
+                "two K tiles per stage: folds 1, 2, 4 with the 32x32b read-out");
   constexpr int kTileRows = kBlockN / F;                 // output columns of a CTA
   constexpr uint32_t kXStageBytes = kXTileBytes * F;     // F x tiles of 8 x 128 bytes
-  constexpr uint32_t kStageTxBytes = kWTileBytes + kXStageBytes + kSfChunkBytes;
+  constexpr uint32_t kStageWBytes = kWTileBytes * T;     // a stage's slot in the W ring
+  constexpr uint32_t kStageXBytes = kXStageBytes * T;    // ... in the x ring
+  constexpr uint32_t kStageSfBytes = kSfChunkBytes * T;  // ... in the W-scale ring
   // x scale chunk of one stage: a 16-byte row per MMA column, 32 rows at most
   // (columns n and n + 32 share row n at fold 8).
   constexpr int kScaleRows = kRows * F < 32 ? kRows * F : 32;
@@ -194,7 +207,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
   const int tile = blockIdx.x / S;
   const int kt_begin = static_cast<int>(split) * p.tiles_per_split;
   const int kt_end = min(p.k_tiles, kt_begin + p.tiles_per_split);
-  const int nkt = max(0, kt_end - kt_begin);
+  const int nkt = max(0, kt_end - kt_begin);  // K tiles of this split
+  const int nst = (nkt + T - 1) / T;          // its pipeline stages
   const int stages = p.stages;
   // One accumulator slot per MMA only unfolded (tensor memory holds no ring
   // of 4 x 8F-column slots for F > 1; the host refuses it).
@@ -257,43 +271,55 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (lane < producers) {
       const uint64_t pol_stream = ptx::policy_evict_first();
       const uint64_t pol_keep = ptx::policy_evict_last();
-      const int npre = min(stages, nkt);
-      // One 16 KB W stage (F pieces of R rows x 128 bytes, 128 rows in all):
-      // a contiguous image from the tiled copy, or F 2-D TMA boxes (with the
-      // same 128-byte swizzle) of W in place.
-      auto load_w_tile = [&](uint32_t dst, int kt, uint32_t bar) {
+      const int npre = min(stages, nst);
+      // A stage's W: nt 16 KB tiles (F pieces of R rows x 128 bytes, 128 rows
+      // each), a contiguous image from the tiled copy, or F 2-D TMA boxes per
+      // tile (with the same 128-byte swizzle) of W in place; and their scale
+      // chunks, contiguous in the re-laid copy.
+      auto load_w_stage = [&](uint32_t slot, int kt0, int nt, uint32_t bar) {
         if (p.w_tiled != nullptr) {
-          ptx::bulk_load(dst, p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt) * kWTileBytes,
-                         kWTileBytes, bar, pol_stream);
+          ptx::bulk_load(sbase + L.w + slot * kStageWBytes,
+                         p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt0) * kWTileBytes,
+                         static_cast<uint32_t>(nt) * kWTileBytes, bar, pol_stream);
         } else {
+          for (int t = 0; t < nt; ++t)
 #pragma unroll
-          for (int pc = 0; pc < F; ++pc)
-            ptx::tma_load_2d(dst + pc * (kTileRows * kTileK), &tmap_w, (kt * F + pc) * kTileK,
-                             tile * kTileRows, bar, pol_stream);
+            for (int pc = 0; pc < F; ++pc)
+              ptx::tma_load_2d(sbase + L.w + slot * kStageWBytes + t * kWTileBytes +
+                                   pc * (kTileRows * kTileK),
+                               &tmap_w, ((kt0 + t) * F + pc) * kTileK, tile * kTileRows, bar,
+                               pol_stream);
         }
+        ptx::bulk_load(sbase + L.sfa + slot * kStageSfBytes,
+                       p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt0) * kSfChunkBytes,
+                       static_cast<uint32_t>(nt) * kSfChunkBytes, bar, pol_stream);
       };
-      // The F activation tiles of a stage, rows >= m read as zero: one box of
-      // the 3-D piece view (128 K x 8 rows x F pieces, piece-major in shared
-      // memory, as F boxes of the 2-D view would land), or F 2-D boxes.
-      auto load_x_tile = [&](uint32_t dst, int kt, uint32_t bar) {
-        if (F > 1 && p.x_pieces) {
-          ptx::tma_load_3d(dst, &tmap_x, 0, 0, kt * F, bar, pol_keep);
+      // A stage's x: its T tiles of F pieces each (T x F 8 x 128-byte boxes,
+      // rows >= m and pieces past K read as zero): one box of the 3-D piece
+      // view (128 K x 8 rows x T F pieces, piece-major in shared memory, as
+      // the 2-D boxes would land), or T F boxes of the 2-D view.  A stage
+      // with fewer than T tiles left still loads T tiles of x (zeros, or the
+      // next split's, unused), so its byte count is fixed.
+      auto load_x_stage = [&](uint32_t slot, int kt0, uint32_t bar) {
+        const uint32_t dst = sbase + L.x + slot * kStageXBytes;
+        if (F * T > 1 && p.x_pieces) {
+          ptx::tma_load_3d(dst, &tmap_x, 0, 0, kt0 * F, bar, pol_keep);
         } else {
 #pragma unroll
-          for (int pc = 0; pc < F; ++pc)
-            ptx::tma_load_2d(dst + pc * kXTileBytes, &tmap_x, (kt * F + pc) * kTileK, 0, bar,
+          for (int pc = 0; pc < F * T; ++pc)
+            ptx::tma_load_2d(dst + pc * kXTileBytes, &tmap_x, (kt0 * F + pc) * kTileK, 0, bar,
                              pol_keep);
         }
+      };
+      auto stage_tiles = [&](int i) { return min(T, nkt - i * T); };
+      auto stage_bytes = [&](int nt) {
+        return static_cast<uint32_t>(nt) * (kWTileBytes + kSfChunkBytes) + kStageXBytes;
       };
       // W and its scales do not depend on the previous kernel: start them now.
       for (int i = lane; i < npre; i += producers) {
         const uint32_t full = bar_full + 8u * i;
-        const int kt = kt_begin + i;
-        ptx::mbar_arrive_expect_tx(full, kStageTxBytes);
-        load_w_tile(sbase + L.w + i * kWTileBytes, kt, full);
-        ptx::bulk_load(sbase + L.sfa + i * kSfChunkBytes,
-                       p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt) * kSfChunkBytes,
-                       kSfChunkBytes, full, pol_stream);
+        ptx::mbar_arrive_expect_tx(full, stage_bytes(stage_tiles(i)));
+        load_w_stage(i, kt_begin + i * T, stage_tiles(i), full);
       }
       // Warm L2 with the stages that come after the ring, so HBM keeps
       // streaming while the previous kernel finishes and the grid wait holds.
@@ -303,27 +329,28 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       // as its CTAs exit, warm more and bridge the hand-over.
       const int depth = static_cast<int>(blockIdx.x) < p.early_ctas ? p.l2_prefetch_early
                                                                      : p.l2_prefetch;
-      const int nwarm = min(nkt, npre + depth);
-      if (lane == 0 && nwarm > npre) {
+      const int warm_begin = npre * T;                       // K tiles of the split
+      const int warm_end = min(nkt, (npre + depth) * T);
+      if (lane == 0 && warm_end > warm_begin) {
         if (p.w_tiled != nullptr) {
-          ptx::prefetch_l2(p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt_begin + npre) *
-                                           kWTileBytes,
-                           static_cast<uint32_t>(nwarm - npre) * kWTileBytes);
+          ptx::prefetch_l2(p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt_begin +
+                                        warm_begin) * kWTileBytes,
+                           static_cast<uint32_t>(warm_end - warm_begin) * kWTileBytes);
         } else {
-          for (int i = npre; i < nwarm; ++i)
+          for (int i = warm_begin; i < warm_end; ++i)
 #pragma unroll
             for (int pc = 0; pc < F; ++pc)
               ptx::prefetch_l2_tile(&tmap_w, ((kt_begin + i) * F + pc) * kTileK,
                                     tile * kTileRows);
         }
-        ptx::prefetch_l2(p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt_begin + npre) *
-                                      kSfChunkBytes,
-                         static_cast<uint32_t>(nwarm - npre) * kSfChunkBytes);
+        ptx::prefetch_l2(p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt_begin +
+                                   warm_begin) * kSfChunkBytes,
+                         static_cast<uint32_t>(warm_end - warm_begin) * kSfChunkBytes);
       }
       // The activations follow the programmatic grid wait.
       ptx::grid_dependency_wait();
       for (int i = lane; i < npre; i += producers)
-        load_x_tile(sbase + L.x + i * kXStageBytes, kt_begin + i, bar_full + 8u * i);
+        load_x_stage(i, kt_begin + i * T, bar_full + 8u * i);
       // From here every slot is on its second or later use: wait until the
       // MMAs of its previous use released it.  This lane's stages advance the
       // ring by `producers` slots at a time.
@@ -331,20 +358,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       for (int i = lane; i < npre; i += producers) issued = i;
       const int first = npre + ((lane - npre % producers) % producers + producers) % producers;
       RingCursor ring{first - npre, 1u};  // npre == stages whenever this loop runs
-      for (int i = first; i < nkt; i += producers) {
+      for (int i = first; i < nst; i += producers) {
         const int s = ring.slot;
         if (!ptx::mbar_wait(bar_empty + 8u * s, ring.phase ^ 1u, p.wait_limit_ns)) {
           raise_flag(p.state, 0x2u);
           break;
         }
         const uint32_t full = bar_full + 8u * s;
-        const int kt = kt_begin + i;
-        ptx::mbar_arrive_expect_tx(full, kStageTxBytes);
-        load_w_tile(sbase + L.w + s * kWTileBytes, kt, full);
-        ptx::bulk_load(sbase + L.sfa + s * kSfChunkBytes,
-                       p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt) * kSfChunkBytes,
-                       kSfChunkBytes, full, pol_stream);
-        load_x_tile(sbase + L.x + s * kXStageBytes, kt, full);
+        const int kt0 = kt_begin + i * T;
+        ptx::mbar_arrive_expect_tx(full, stage_bytes(stage_tiles(i)));
+        load_w_stage(s, kt0, stage_tiles(i), full);
+        load_x_stage(s, kt0, full);
         issued = i;
         ring.slot += producers;
         if (ring.slot >= stages) {
@@ -357,7 +381,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       // its stages among the last `stages` of the split, the latest use of
       // their slots (no stage past nkt - 1 reuses them, so each wait is on
       // the phase of this lane's own copy).
-      for (int i = issued; i >= max(0, nkt - stages); i -= producers)
+      for (int i = issued; i >= max(0, nst - stages); i -= producers)
         ptx::mbar_wait(bar_full + 8u * (i % stages), static_cast<uint32_t>(i / stages) & 1u,
                        p.wait_limit_ns);
     }
@@ -376,44 +400,55 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         if (!ok) raise_flag(p.state, 0x2u);
         ptx::tc_fence_after();
       }
+      // Issuer j takes stages j, j + pipes, ...; a stage's tiles take
+      // consecutive accumulator slots and scale slots (the accumulator ring is
+      // a multiple of T pipes, so every slot keeps one issuer).
       RingCursor stage{0, 0u}, acc{0, 0u};
-      for (int q = 0; q < issuer; ++q) {
-        stage.next(stages);
-        acc.next(acc_ring);
-      }
-      for (int i = issuer; i < nkt && ok; i += pipes) {
+      for (int q = 0; q < issuer; ++q) stage.next(stages);
+      for (int q = 0; q < issuer * T; ++q) acc.next(acc_ring);
+      for (int i = issuer; i < nst && ok; i += pipes) {
         const int s = stage.slot;
-        const int r = acc.slot;
-        if (!ptx::mbar_wait(bar_full + 8u * s, stage.phase, p.wait_limit_ns) ||
-            (i >= acc_ring &&
-             !ptx::mbar_wait(bar_acc_empty + 8u * r, acc.phase ^ 1u, p.wait_limit_ns))) {
+        if (!ptx::mbar_wait(bar_full + 8u * s, stage.phase, p.wait_limit_ns)) {
           raise_flag(p.state, 0x2u);
           ok = false;
           break;
         }
-        ptx::tc_fence_after();
-        const uint32_t sfa_t = tmem + p.tmem.sfa + 4u * s;
-        const uint32_t sfb_t = tmem + p.tmem.sfb + 4u * s;
-        ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::desc_rows16(sbase + L.sfa + s * kSfChunkBytes));
-        ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::desc_rows16(sbase + L.sx + i * kSxChunkBytes));
-        const uint32_t a0 = sbase + L.w + s * kWTileBytes;
-        const uint32_t b0 = sbase + L.x + s * kXStageBytes;
-        const uint32_t d0 = tmem + p.tmem.acc + p.tmem.acc_slot * static_cast<uint32_t>(r);
+        const int nt = min(T, nkt - i * T);
 #pragma unroll
-        for (uint32_t kb = 0; kb < kSfPerTile; ++kb) {
-          // One 8-column accumulator per block, or one per stage.
-          const uint32_t d = per_block ? d0 + 8u * kb : d0;
-          const uint32_t accumulate = per_block ? 0u : (kb > 0 ? 1u : 0u);
-          ptx::mma_mxf8(d, ptx::desc_kmajor_sw128(a0 + 32u * kb),
-                        ptx::desc_kmajor_sw128(b0 + 32u * kb), idesc_for_block<F>(kb),
-                        accumulate, sfa_t, sfb_t);
-        }
-        ptx::mma_commit(bar_empty + 8u * s);
-        ptx::mma_commit(bar_acc_full + 8u * r);
-        for (int q = 0; q < pipes; ++q) {
-          stage.next(stages);
+        for (int t = 0; t < T; ++t) {
+          if (t >= nt) break;
+          const int j = i * T + t;  // K tile of the split
+          const int r = acc.slot;
+          if (j >= acc_ring &&
+              !ptx::mbar_wait(bar_acc_empty + 8u * r, acc.phase ^ 1u, p.wait_limit_ns)) {
+            raise_flag(p.state, 0x2u);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sc = static_cast<uint32_t>(s * T + t);  // scale slot of the tile
+          const uint32_t sfa_t = tmem + p.tmem.sfa + 4u * sc;
+          const uint32_t sfb_t = tmem + p.tmem.sfb + 4u * sc;
+          ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::desc_rows16(sbase + L.sfa + sc * kSfChunkBytes));
+          ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::desc_rows16(sbase + L.sx + j * kSxChunkBytes));
+          const uint32_t a0 = sbase + L.w + s * kStageWBytes + t * kWTileBytes;
+          const uint32_t b0 = sbase + L.x + s * kStageXBytes + t * kXStageBytes;
+          const uint32_t d0 = tmem + p.tmem.acc + p.tmem.acc_slot * static_cast<uint32_t>(r);
+#pragma unroll
+          for (uint32_t kb = 0; kb < kSfPerTile; ++kb) {
+            // One 8-column accumulator per block, or one per tile.
+            const uint32_t d = per_block ? d0 + 8u * kb : d0;
+            const uint32_t accumulate = per_block ? 0u : (kb > 0 ? 1u : 0u);
+            ptx::mma_mxf8(d, ptx::desc_kmajor_sw128(a0 + 32u * kb),
+                          ptx::desc_kmajor_sw128(b0 + 32u * kb), idesc_for_block<F>(kb),
+                          accumulate, sfa_t, sfb_t);
+          }
+          if (t + 1 == nt) ptx::mma_commit(bar_empty + 8u * s);  // the stage's last tile
+          ptx::mma_commit(bar_acc_full + 8u * r);
           acc.next(acc_ring);
         }
+        for (int q = 0; q < pipes; ++q) stage.next(stages);
+        for (int q = nt; q < pipes * T; ++q) acc.next(acc_ring);  // the other issuers' tiles
       }
     }
   }
@@ -859,7 +894,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 // kernel may start (and stream W) before the previous kernel on the stream
 // has finished.  Off where that kernel writes what the producer reads before
 // its grid wait (the weight or its scale chunks).
-template <int S, bool kWideLoad, int F>
+template <int S, bool kWideLoad, int F, int T = 1>
 cudaError_t launch_impl(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, const GemmParams& p,
                         cudaStream_t stream, bool programmatic) {
   cudaLaunchConfig_t cfg = {};
@@ -883,12 +918,12 @@ cudaError_t launch_impl(const CUtensorMap& tmap_w, const CUtensorMap& tmap_x, co
   }
   cfg.attrs = attrs;
   cfg.numAttrs = count;
-  return cudaLaunchKernelEx(&cfg, publish_gemm_kernel<S, kWideLoad, F>, tmap_w, tmap_x, p);
+  return cudaLaunchKernelEx(&cfg, publish_gemm_kernel<S, kWideLoad, F, T>, tmap_w, tmap_x, p);
 }
 
-template <int S, bool kWideLoad, int F>
+template <int S, bool kWideLoad, int F, int T = 1>
 cudaError_t set_smem_impl(int bytes) {
-  return cudaFuncSetAttribute(publish_gemm_kernel<S, kWideLoad, F>,
+  return cudaFuncSetAttribute(publish_gemm_kernel<S, kWideLoad, F, T>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 

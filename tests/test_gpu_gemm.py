@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 
 
 def run_chain(w, ws, x, xs, split_k, capacity=8, stages=0, mailbox=None, acc_blocks=0,
-              w_layout=0, fold=0):
+              w_layout=0, fold=0, **tactic):
     """GEMM (C requested) -> snapshot of mailbox + state -> consume.  Returns
     (C bits, mailbox words between the two kernels, state then, out bits,
     mailbox words after, state after, handle config)."""
@@ -27,7 +27,7 @@ def run_chain(w, ws, x, xs, split_k, capacity=8, stages=0, mailbox=None, acc_blo
     m = x.shape[0]
     mb = mailbox or Mailbox(capacity, n)
     g = PublishGemm(dev(w), dev(ws), mb, split_k=split_k, stages=stages, acc_blocks=acc_blocks,
-                    w_layout=w_layout, fold=fold)
+                    w_layout=w_layout, fold=fold, **tactic)
     c = torch.full((m, n), 0x7FFF, dtype=torch.int16, device="cuda")
     g.run(dev(x), dev(xs), c)
     torch.cuda.synchronize()
@@ -636,3 +636,83 @@ def test_first_run_right_after_create_on_one_stream(cuda, w_layout):
         assert_bf16_close(bits(c), want, f"seed {seed}")
         assert (bits(out) == sanitized(bits(c))).all()
         assert state_words(mb) == [1, 0, 0, 0]
+
+
+# cta_k 256: two K tiles per pipeline stage.  Each tile's MMAs still fill one
+# accumulator slot and the epilogue adds the slots in tile order, so every
+# result is bit-identical to cta_k 128's.  Cases: a partial last stage (odd
+# tile counts, ragged K), rings refilled many times, split-K 2 and 4, folds 2
+# and 4 (whose 4-slot accumulator ring takes at most 2 pipes), 4 pipes at
+# fold 2, both weight layouts.
+K256_CASES = [
+    # n, k, m, split_k, fold, w_layout, stages, pipes
+    (256, 384, 3, 1, 1, W_TILED, 0, 0),
+    (256, 352, 8, 1, 1, W_IN_PLACE, 0, 0),
+    (512, 4096, 8, 1, 1, W_TILED, 2, 0),
+    (512, 4096, 5, 2, 1, W_IN_PLACE, 4, 2),
+    (768, 3072, 8, 4, 1, W_TILED, 0, 0),
+    (1024, 4096, 4, 1, 4, W_TILED, 0, 0),
+    (1024, 4096, 8, 2, 2, W_IN_PLACE, 0, 0),
+    (256, 1536, 8, 1, 4, W_TILED, 0, 0),
+    (256, 1664, 6, 2, 4, W_IN_PLACE, 2, 1),
+    (2048, 16384, 8, 1, 2, W_TILED, 4, 4),
+    (1024, 8192, 8, 4, 2, W_TILED, 3, 1),
+]
+
+
+@pytest.mark.parametrize("case", K256_CASES, ids=lambda c: "n%d-k%d-m%d-s%d-f%d-w%d-st%d-p%d" % c)
+def test_cta_k_256_matches_cta_k_128(cuda, case):
+    n, k, m, split_k, fold, w_layout, stages, pipes = case
+    wl = synthetic.Workload("cta_k", n, k, m, split_k, exp_lo=-4, exp_hi=2, seed=n + k + m)
+    w, ws = synthetic.make_weights(wl)
+    x, xs = synthetic.make_activations(wl)
+    ref = run_chain(w, ws, x, xs, split_k, w_layout=w_layout, fold=fold)
+    got = run_chain(w, ws, x, xs, split_k, w_layout=w_layout, fold=fold, stages=stages,
+                    pipes=pipes, cta_k=256)
+    cfg = got[-1]
+    assert cfg["cta_k"] == 256 and cfg["fold"] == fold and cfg["split_k"] == split_k
+    if stages:
+        assert cfg["stages"] == stages
+    ring = 4 if fold == 4 else 8
+    assert ring % (2 * cfg["pipes"]) == 0 and cfg["stages"] % cfg["pipes"] == 0
+    for a, b, what in ((ref[0], got[0], "C"), (ref[1], got[1], "mailbox"),
+                       (ref[3], got[3], "consumer output"), (ref[4], got[4], "mailbox after")):
+        assert (a == b).all(), what
+    assert ref[2] == got[2] and ref[5] == got[5]
+    assert_bf16_close(got[0], oracle.gemm_bf16(w, ws, x, xs), "C vs oracle")
+
+
+@pytest.mark.parametrize("case", K256_CASES[:6], ids=lambda c: "n%d-k%d-m%d-s%d-f%d-w%d-st%d-p%d" % c)
+def test_cta_k_256_integer_inputs_bit_exact(cuda, case):
+    n, k, m, split_k, fold, w_layout, stages, pipes = case
+    w, ws, x, xs = synthetic.integer_operands(n, k, m, seed=k + 7)
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    c, between, state_between, out, after, state_after, cfg = run_chain(
+        w, ws, x, xs, split_k, w_layout=w_layout, fold=fold, stages=stages, pipes=pipes,
+        cta_k=256)
+    assert cfg["cta_k"] == 256
+    assert (c == want).all()
+    check_published(between, state_between, c, 8, n)
+    assert (out == sanitized(want)).all()
+    assert (after == oracle.SENTINEL).all() and state_after == [1, 0, 0, 0]
+
+
+def test_cta_k_256_chained_calls(cuda):
+    # Ten chained calls through one handle: the two-tile stages' barriers,
+    # slots and ring refills hold across calls.
+    n, k = 1024, 16384
+    w, ws, x, xs = synthetic.integer_operands(n, k, 8, seed=256)
+    want = oracle.gemm_bf16(w, ws, x, xs)
+    mb = Mailbox(8, n)
+    g = PublishGemm(dev(w), dev(ws), mb, split_k=1, cta_k=256, stages=3, fold=2)
+    assert (g.config()["cta_k"], g.config()["stages"]) == (256, 3)
+    X, XS = dev(x), dev(xs)
+    for call in range(10):
+        c = torch.full((8, n), 0x7FFF, dtype=torch.int16, device="cuda")
+        g.run(X, XS, c)
+        out = mb.consume(8)
+        torch.cuda.synchronize()
+        assert (bits(c) == want).all(), f"C, call {call}"
+        assert (bits(out) == sanitized(want)).all(), f"consumer output, call {call}"
+    assert mb.status()[0] == OK and state_words(mb) == [10 % 3, 9 % 3, 0, 0]
+    g.close()

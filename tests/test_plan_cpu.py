@@ -175,3 +175,51 @@ def test_split_k_receive_buffer_of_its_own_where_it_fits():
     assert plan_gemm(7168, 16384, split_k=4)["smem_bytes"] == 113280
     # unsplit launches have no partials to exchange
     assert plan_gemm(4096, 4096, split_k=1)["smem_bytes"] == 173728
+
+
+
+@pytest.mark.parametrize("n", [256, 2048, 4096, 7168])
+def test_cta_k_256_plans_keep_the_invariants(n):
+    # Two K tiles per stage: rings of 2 x stages tiles, a 4-column W-scale and
+    # x-scale slot per tile, and every accumulator slot owned by one issuer
+    # (the ring of 8 slots, 4 at fold 4, a multiple of 2 x pipes).
+    accepted = 0
+    for k in (256, 384, 1536, 4096, 16384):
+        for split, stages, pipes, fold in itertools.product([0, 1, 2, 4], [0, 2, 3, 4, 6, 8],
+                                                            [0, 1, 2, 4], [0, 1, 2, 4]):
+            try:
+                p = plan_gemm(n, k, split_k=split, stages=stages, pipes=pipes, fold=fold,
+                              cta_k=256)
+            except Mxfp8Error as e:
+                assert "ERR_UNSUPPORTED" in str(e), (n, k, split, stages, pipes, fold)
+                continue
+            accepted += 1
+            where = (n, k, split, stages, pipes, fold, p)
+            f, st = p["fold"], p["stages"]
+            assert p["cta_k"] == 256 and f in (1, 2, 4), where
+            ring = 4 if f == 4 else 8
+            assert ring % (2 * p["pipes"]) == 0 and st % p["pipes"] == 0, where
+            assert p["tmem_columns"] <= 256, where
+            assert p["tmem_columns"] >= 8 * f * ring + 2 * 4 * 2 * st, where
+            tps = -(-_k_tiles(k, f) // p["split_k"])
+            rings = 2 * st * (16384 + 1024 * f + 512)
+            staging = tps * 16 * min(8 * f, 32) + 384
+            assert p["smem_bytes"] >= rings + staging + (2 * st + 2 * 8 + 2) * 8 + 16 + 1024, where
+            for field, asked in (("split_k", split), ("stages", stages), ("pipes", pipes),
+                                 ("fold", fold)):
+                if asked:
+                    assert p[field] == asked, where
+    assert accepted > 0
+
+
+def test_cta_k_refusals():
+    for kw in (dict(cta_k=384), dict(cta_k=64), dict(cta_k=256, fold=8),
+               dict(cta_k=256, split_k=8), dict(cta_k=256, acc_blocks=1),
+               dict(cta_k=256, tmem_load=TMEM_LOAD_16X256B),
+               dict(cta_k=256, fold=4, stages=4, pipes=4)):  # 4 slots cannot serve 4 pipes x 2
+        with pytest.raises(Mxfp8Error, match="ERR_UNSUPPORTED"):
+            plan_gemm(1024, 4096, **kw)
+    # the default stays 128, and 256 resolves with the pipes its ring allows
+    assert plan_gemm(4096, 4096)["cta_k"] == 128
+    p = plan_gemm(4096, 4096, split_k=1, cta_k=256)
+    assert p["cta_k"] == 256 and p["fold"] == 4 and p["pipes"] <= 2
