@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 "two K tiles per stage: folds 1, 2, 4 with the 32x32b read-out");
   constexpr int kTileRows = kBlockN / F;                 // output columns of a CTA
   constexpr uint32_t kXStageBytes = kXTileBytes * F;     // F x tiles of 8 x 128 bytes
+  constexpr uint32_t kStageTxBytes = kWTileBytes + kXStageBytes + kSfChunkBytes;  // one K tile
   constexpr uint32_t kStageWBytes = kWTileBytes * T;     // a stage's slot in the W ring
   constexpr uint32_t kStageXBytes = kXStageBytes * T;    // ... in the x ring
   constexpr uint32_t kStageSfBytes = kSfChunkBytes * T;  // ... in the W-scale ring
@@ -269,121 +270,229 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const int producers = pipes;
     if (lane == 0) ptx::launch_dependents();
     if (lane < producers) {
-      const uint64_t pol_stream = ptx::policy_evict_first();
-      const uint64_t pol_keep = ptx::policy_evict_last();
-      const int npre = min(stages, nst);
-      // A stage's W: nt 16 KB tiles (F pieces of R rows x 128 bytes, 128 rows
-      // each), a contiguous image from the tiled copy, or F 2-D TMA boxes per
-      // tile (with the same 128-byte swizzle) of W in place; and their scale
-      // chunks, contiguous in the re-laid copy.
-      auto load_w_stage = [&](uint32_t slot, int kt0, int nt, uint32_t bar) {
-        if (p.w_tiled != nullptr) {
-          ptx::bulk_load(sbase + L.w + slot * kStageWBytes,
-                         p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt0) * kWTileBytes,
-                         static_cast<uint32_t>(nt) * kWTileBytes, bar, pol_stream);
-        } else {
-          for (int t = 0; t < nt; ++t)
-#pragma unroll
+      if constexpr (T == 1) {
+        const uint64_t pol_stream = ptx::policy_evict_first();
+        const uint64_t pol_keep = ptx::policy_evict_last();
+        const int npre = min(stages, nkt);
+        // One 16 KB W stage (F pieces of R rows x 128 bytes, 128 rows in all):
+        // a contiguous image from the tiled copy, or F 2-D TMA boxes (with the
+        // same 128-byte swizzle) of W in place.
+        auto load_w_tile = [&](uint32_t dst, int kt, uint32_t bar) {
+          if (p.w_tiled != nullptr) {
+            ptx::bulk_load(dst, p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt) * kWTileBytes,
+                           kWTileBytes, bar, pol_stream);
+          } else {
+  #pragma unroll
             for (int pc = 0; pc < F; ++pc)
-              ptx::tma_load_2d(sbase + L.w + slot * kStageWBytes + t * kWTileBytes +
-                                   pc * (kTileRows * kTileK),
-                               &tmap_w, ((kt0 + t) * F + pc) * kTileK, tile * kTileRows, bar,
-                               pol_stream);
-        }
-        ptx::bulk_load(sbase + L.sfa + slot * kStageSfBytes,
-                       p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt0) * kSfChunkBytes,
-                       static_cast<uint32_t>(nt) * kSfChunkBytes, bar, pol_stream);
-      };
-      // A stage's x: its T tiles of F pieces each (T x F 8 x 128-byte boxes,
-      // rows >= m and pieces past K read as zero): one box of the 3-D piece
-      // view (128 K x 8 rows x T F pieces, piece-major in shared memory, as
-      // the 2-D boxes would land), or T F boxes of the 2-D view.  A stage
-      // with fewer than T tiles left still loads T tiles of x (zeros, or the
-      // next split's, unused), so its byte count is fixed.
-      auto load_x_stage = [&](uint32_t slot, int kt0, uint32_t bar) {
-        const uint32_t dst = sbase + L.x + slot * kStageXBytes;
-        if (F * T > 1 && p.x_pieces) {
-          ptx::tma_load_3d(dst, &tmap_x, 0, 0, kt0 * F, bar, pol_keep);
-        } else {
-#pragma unroll
-          for (int pc = 0; pc < F * T; ++pc)
-            ptx::tma_load_2d(dst + pc * kXTileBytes, &tmap_x, (kt0 * F + pc) * kTileK, 0, bar,
-                             pol_keep);
-        }
-      };
-      auto stage_tiles = [&](int i) { return min(T, nkt - i * T); };
-      auto stage_bytes = [&](int nt) {
-        return static_cast<uint32_t>(nt) * (kWTileBytes + kSfChunkBytes) + kStageXBytes;
-      };
-      // W and its scales do not depend on the previous kernel: start them now.
-      for (int i = lane; i < npre; i += producers) {
-        const uint32_t full = bar_full + 8u * i;
-        ptx::mbar_arrive_expect_tx(full, stage_bytes(stage_tiles(i)));
-        load_w_stage(i, kt_begin + i * T, stage_tiles(i), full);
-      }
-      // Warm L2 with the stages that come after the ring, so HBM keeps
-      // streaming while the previous kernel finishes and the grid wait holds.
-      // The first CTAs of the grid launch while the previous kernel still
-      // streams (its dependents launch as soon as it starts), so they warm
-      // fewer stages and leave it the bandwidth; the later ones, which start
-      // as its CTAs exit, warm more and bridge the hand-over.
-      const int depth = static_cast<int>(blockIdx.x) < p.early_ctas ? p.l2_prefetch_early
-                                                                     : p.l2_prefetch;
-      const int warm_begin = npre * T;                       // K tiles of the split
-      const int warm_end = min(nkt, (npre + depth) * T);
-      if (lane == 0 && warm_end > warm_begin) {
-        if (p.w_tiled != nullptr) {
-          ptx::prefetch_l2(p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt_begin +
-                                        warm_begin) * kWTileBytes,
-                           static_cast<uint32_t>(warm_end - warm_begin) * kWTileBytes);
-        } else {
-          for (int i = warm_begin; i < warm_end; ++i)
-#pragma unroll
+              ptx::tma_load_2d(dst + pc * (kTileRows * kTileK), &tmap_w, (kt * F + pc) * kTileK,
+                               tile * kTileRows, bar, pol_stream);
+          }
+        };
+        // The F activation tiles of a stage, rows >= m read as zero: one box of
+        // the 3-D piece view (128 K x 8 rows x F pieces, piece-major in shared
+        // memory, as F boxes of the 2-D view would land), or F 2-D boxes.
+        auto load_x_tile = [&](uint32_t dst, int kt, uint32_t bar) {
+          if (F > 1 && p.x_pieces) {
+            ptx::tma_load_3d(dst, &tmap_x, 0, 0, kt * F, bar, pol_keep);
+          } else {
+  #pragma unroll
             for (int pc = 0; pc < F; ++pc)
-              ptx::prefetch_l2_tile(&tmap_w, ((kt_begin + i) * F + pc) * kTileK,
-                                    tile * kTileRows);
+              ptx::tma_load_2d(dst + pc * kXTileBytes, &tmap_x, (kt * F + pc) * kTileK, 0, bar,
+                               pol_keep);
+          }
+        };
+        // W and its scales do not depend on the previous kernel: start them now.
+        for (int i = lane; i < npre; i += producers) {
+          const uint32_t full = bar_full + 8u * i;
+          const int kt = kt_begin + i;
+          ptx::mbar_arrive_expect_tx(full, kStageTxBytes);
+          load_w_tile(sbase + L.w + i * kWTileBytes, kt, full);
+          ptx::bulk_load(sbase + L.sfa + i * kSfChunkBytes,
+                         p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt) * kSfChunkBytes,
+                         kSfChunkBytes, full, pol_stream);
         }
-        ptx::prefetch_l2(p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt_begin +
-                                   warm_begin) * kSfChunkBytes,
-                         static_cast<uint32_t>(warm_end - warm_begin) * kSfChunkBytes);
+        // Warm L2 with the stages that come after the ring, so HBM keeps
+        // streaming while the previous kernel finishes and the grid wait holds.
+        // The first CTAs of the grid launch while the previous kernel still
+        // streams (its dependents launch as soon as it starts), so they warm
+        // fewer stages and leave it the bandwidth; the later ones, which start
+        // as its CTAs exit, warm more and bridge the hand-over.
+        const int depth = static_cast<int>(blockIdx.x) < p.early_ctas ? p.l2_prefetch_early
+                                                                       : p.l2_prefetch;
+        const int nwarm = min(nkt, npre + depth);
+        if (lane == 0 && nwarm > npre) {
+          if (p.w_tiled != nullptr) {
+            ptx::prefetch_l2(p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt_begin + npre) *
+                                             kWTileBytes,
+                             static_cast<uint32_t>(nwarm - npre) * kWTileBytes);
+          } else {
+            for (int i = npre; i < nwarm; ++i)
+  #pragma unroll
+              for (int pc = 0; pc < F; ++pc)
+                ptx::prefetch_l2_tile(&tmap_w, ((kt_begin + i) * F + pc) * kTileK,
+                                      tile * kTileRows);
+          }
+          ptx::prefetch_l2(p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt_begin + npre) *
+                                        kSfChunkBytes,
+                           static_cast<uint32_t>(nwarm - npre) * kSfChunkBytes);
+        }
+        // The activations follow the programmatic grid wait.
+        ptx::grid_dependency_wait();
+        for (int i = lane; i < npre; i += producers)
+          load_x_tile(sbase + L.x + i * kXStageBytes, kt_begin + i, bar_full + 8u * i);
+        // From here every slot is on its second or later use: wait until the
+        // MMAs of its previous use released it.  This lane's stages advance the
+        // ring by `producers` slots at a time.
+        int issued = -1;  // the last stage this lane issued
+        for (int i = lane; i < npre; i += producers) issued = i;
+        const int first = npre + ((lane - npre % producers) % producers + producers) % producers;
+        RingCursor ring{first - npre, 1u};  // npre == stages whenever this loop runs
+        for (int i = first; i < nkt; i += producers) {
+          const int s = ring.slot;
+          if (!ptx::mbar_wait(bar_empty + 8u * s, ring.phase ^ 1u, p.wait_limit_ns)) {
+            raise_flag(p.state, 0x2u);
+            break;
+          }
+          const uint32_t full = bar_full + 8u * s;
+          const int kt = kt_begin + i;
+          ptx::mbar_arrive_expect_tx(full, kStageTxBytes);
+          load_w_tile(sbase + L.w + s * kWTileBytes, kt, full);
+          ptx::bulk_load(sbase + L.sfa + s * kSfChunkBytes,
+                         p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt) * kSfChunkBytes,
+                         kSfChunkBytes, full, pol_stream);
+          load_x_tile(sbase + L.x + s * kXStageBytes, kt, full);
+          issued = i;
+          ring.slot += producers;
+          if (ring.slot >= stages) {
+            ring.slot -= stages;
+            ring.phase ^= 1u;
+          }
+        }
+        // This lane's copies still in flight land before the CTA leaves
+        // (immediate when the MMAs consumed them, which is the normal case):
+        // its stages among the last `stages` of the split, the latest use of
+        // their slots (no stage past nkt - 1 reuses them, so each wait is on
+        // the phase of this lane's own copy).
+        for (int i = issued; i >= max(0, nkt - stages); i -= producers)
+          ptx::mbar_wait(bar_full + 8u * (i % stages), static_cast<uint32_t>(i / stages) & 1u,
+                         p.wait_limit_ns);
+      } else {
+        const uint64_t pol_stream = ptx::policy_evict_first();
+        const uint64_t pol_keep = ptx::policy_evict_last();
+        const int npre = min(stages, nst);
+        // A stage's W: nt 16 KB tiles (F pieces of R rows x 128 bytes, 128 rows
+        // each), a contiguous image from the tiled copy, or F 2-D TMA boxes per
+        // tile (with the same 128-byte swizzle) of W in place; and their scale
+        // chunks, contiguous in the re-laid copy.
+        auto load_w_stage = [&](uint32_t slot, int kt0, int nt, uint32_t bar) {
+          if (p.w_tiled != nullptr) {
+            ptx::bulk_load(sbase + L.w + slot * kStageWBytes,
+                           p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt0) * kWTileBytes,
+                           static_cast<uint32_t>(nt) * kWTileBytes, bar, pol_stream);
+          } else {
+            for (int t = 0; t < nt; ++t)
+  #pragma unroll
+              for (int pc = 0; pc < F; ++pc)
+                ptx::tma_load_2d(sbase + L.w + slot * kStageWBytes + t * kWTileBytes +
+                                     pc * (kTileRows * kTileK),
+                                 &tmap_w, ((kt0 + t) * F + pc) * kTileK, tile * kTileRows, bar,
+                                 pol_stream);
+          }
+          ptx::bulk_load(sbase + L.sfa + slot * kStageSfBytes,
+                         p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt0) * kSfChunkBytes,
+                         static_cast<uint32_t>(nt) * kSfChunkBytes, bar, pol_stream);
+        };
+        // A stage's x: its T tiles of F pieces each (T x F 8 x 128-byte boxes,
+        // rows >= m and pieces past K read as zero): one box of the 3-D piece
+        // view (128 K x 8 rows x T F pieces, piece-major in shared memory, as
+        // the 2-D boxes would land), or T F boxes of the 2-D view.  A stage
+        // with fewer than T tiles left still loads T tiles of x (zeros, or the
+        // next split's, unused), so its byte count is fixed.
+        auto load_x_stage = [&](uint32_t slot, int kt0, uint32_t bar) {
+          const uint32_t dst = sbase + L.x + slot * kStageXBytes;
+          if (F * T > 1 && p.x_pieces) {
+            ptx::tma_load_3d(dst, &tmap_x, 0, 0, kt0 * F, bar, pol_keep);
+          } else {
+  #pragma unroll
+            for (int pc = 0; pc < F * T; ++pc)
+              ptx::tma_load_2d(dst + pc * kXTileBytes, &tmap_x, (kt0 * F + pc) * kTileK, 0, bar,
+                               pol_keep);
+          }
+        };
+        auto stage_tiles = [&](int i) { return min(T, nkt - i * T); };
+        auto stage_bytes = [&](int nt) {
+          return static_cast<uint32_t>(nt) * (kWTileBytes + kSfChunkBytes) + kStageXBytes;
+        };
+        // W and its scales do not depend on the previous kernel: start them now.
+        for (int i = lane; i < npre; i += producers) {
+          const uint32_t full = bar_full + 8u * i;
+          ptx::mbar_arrive_expect_tx(full, stage_bytes(stage_tiles(i)));
+          load_w_stage(i, kt_begin + i * T, stage_tiles(i), full);
+        }
+        // Warm L2 with the stages that come after the ring, so HBM keeps
+        // streaming while the previous kernel finishes and the grid wait holds.
+        // The first CTAs of the grid launch while the previous kernel still
+        // streams (its dependents launch as soon as it starts), so they warm
+        // fewer stages and leave it the bandwidth; the later ones, which start
+        // as its CTAs exit, warm more and bridge the hand-over.
+        const int depth = static_cast<int>(blockIdx.x) < p.early_ctas ? p.l2_prefetch_early
+                                                                       : p.l2_prefetch;
+        const int warm_begin = npre * T;                       // K tiles of the split
+        const int warm_end = min(nkt, (npre + depth) * T);
+        if (lane == 0 && warm_end > warm_begin) {
+          if (p.w_tiled != nullptr) {
+            ptx::prefetch_l2(p.w_tiled + (static_cast<size_t>(tile) * p.k_tiles + kt_begin +
+                                          warm_begin) * kWTileBytes,
+                             static_cast<uint32_t>(warm_end - warm_begin) * kWTileBytes);
+          } else {
+            for (int i = warm_begin; i < warm_end; ++i)
+  #pragma unroll
+              for (int pc = 0; pc < F; ++pc)
+                ptx::prefetch_l2_tile(&tmap_w, ((kt_begin + i) * F + pc) * kTileK,
+                                      tile * kTileRows);
+          }
+          ptx::prefetch_l2(p.w_sf + (static_cast<size_t>(tile) * p.k_tiles + kt_begin +
+                                     warm_begin) * kSfChunkBytes,
+                           static_cast<uint32_t>(warm_end - warm_begin) * kSfChunkBytes);
+        }
+        // The activations follow the programmatic grid wait.
+        ptx::grid_dependency_wait();
+        for (int i = lane; i < npre; i += producers)
+          load_x_stage(i, kt_begin + i * T, bar_full + 8u * i);
+        // From here every slot is on its second or later use: wait until the
+        // MMAs of its previous use released it.  This lane's stages advance the
+        // ring by `producers` slots at a time.
+        int issued = -1;  // the last stage this lane issued
+        for (int i = lane; i < npre; i += producers) issued = i;
+        const int first = npre + ((lane - npre % producers) % producers + producers) % producers;
+        RingCursor ring{first - npre, 1u};  // npre == stages whenever this loop runs
+        for (int i = first; i < nst; i += producers) {
+          const int s = ring.slot;
+          if (!ptx::mbar_wait(bar_empty + 8u * s, ring.phase ^ 1u, p.wait_limit_ns)) {
+            raise_flag(p.state, 0x2u);
+            break;
+          }
+          const uint32_t full = bar_full + 8u * s;
+          const int kt0 = kt_begin + i * T;
+          ptx::mbar_arrive_expect_tx(full, stage_bytes(stage_tiles(i)));
+          load_w_stage(s, kt0, stage_tiles(i), full);
+          load_x_stage(s, kt0, full);
+          issued = i;
+          ring.slot += producers;
+          if (ring.slot >= stages) {
+            ring.slot -= stages;
+            ring.phase ^= 1u;
+          }
+        }
+        // This lane's copies still in flight land before the CTA leaves
+        // (immediate when the MMAs consumed them, which is the normal case):
+        // its stages among the last `stages` of the split, the latest use of
+        // their slots (no stage past nkt - 1 reuses them, so each wait is on
+        // the phase of this lane's own copy).
+        for (int i = issued; i >= max(0, nst - stages); i -= producers)
+          ptx::mbar_wait(bar_full + 8u * (i % stages), static_cast<uint32_t>(i / stages) & 1u,
+                         p.wait_limit_ns);
       }
-      // The activations follow the programmatic grid wait.
-      ptx::grid_dependency_wait();
-      for (int i = lane; i < npre; i += producers)
-        load_x_stage(i, kt_begin + i * T, bar_full + 8u * i);
-      // From here every slot is on its second or later use: wait until the
-      // MMAs of its previous use released it.  This lane's stages advance the
-      // ring by `producers` slots at a time.
-      int issued = -1;  // the last stage this lane issued
-      for (int i = lane; i < npre; i += producers) issued = i;
-      const int first = npre + ((lane - npre % producers) % producers + producers) % producers;
-      RingCursor ring{first - npre, 1u};  // npre == stages whenever this loop runs
-      for (int i = first; i < nst; i += producers) {
-        const int s = ring.slot;
-        if (!ptx::mbar_wait(bar_empty + 8u * s, ring.phase ^ 1u, p.wait_limit_ns)) {
-          raise_flag(p.state, 0x2u);
-          break;
-        }
-        const uint32_t full = bar_full + 8u * s;
-        const int kt0 = kt_begin + i * T;
-        ptx::mbar_arrive_expect_tx(full, stage_bytes(stage_tiles(i)));
-        load_w_stage(s, kt0, stage_tiles(i), full);
-        load_x_stage(s, kt0, full);
-        issued = i;
-        ring.slot += producers;
-        if (ring.slot >= stages) {
-          ring.slot -= stages;
-          ring.phase ^= 1u;
-        }
-      }
-      // This lane's copies still in flight land before the CTA leaves
-      // (immediate when the MMAs consumed them, which is the normal case):
-      // its stages among the last `stages` of the split, the latest use of
-      // their slots (no stage past nkt - 1 reuses them, so each wait is on
-      // the phase of this lane's own copy).
-      for (int i = issued; i >= max(0, nst - stages); i -= producers)
-        ptx::mbar_wait(bar_full + 8u * (i % stages), static_cast<uint32_t>(i / stages) & 1u,
-                       p.wait_limit_ns);
     }
   } else if (warp == 1 || warp >= 6) {
     const int issuer = warp == 1 ? 0 : warp - 5;
@@ -400,55 +509,97 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         if (!ok) raise_flag(p.state, 0x2u);
         ptx::tc_fence_after();
       }
-      // Issuer j takes stages j, j + pipes, ...; a stage's tiles take
-      // consecutive accumulator slots and scale slots (the accumulator ring is
-      // a multiple of T pipes, so every slot keeps one issuer).
-      RingCursor stage{0, 0u}, acc{0, 0u};
-      for (int q = 0; q < issuer; ++q) stage.next(stages);
-      for (int q = 0; q < issuer * T; ++q) acc.next(acc_ring);
-      for (int i = issuer; i < nst && ok; i += pipes) {
-        const int s = stage.slot;
-        if (!ptx::mbar_wait(bar_full + 8u * s, stage.phase, p.wait_limit_ns)) {
-          raise_flag(p.state, 0x2u);
-          ok = false;
-          break;
+      if constexpr (T == 1) {
+        RingCursor stage{0, 0u}, acc{0, 0u};
+        for (int q = 0; q < issuer; ++q) {
+          stage.next(stages);
+          acc.next(acc_ring);
         }
-        const int nt = min(T, nkt - i * T);
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-          if (t >= nt) break;
-          const int j = i * T + t;  // K tile of the split
+        for (int i = issuer; i < nkt && ok; i += pipes) {
+          const int s = stage.slot;
           const int r = acc.slot;
-          if (j >= acc_ring &&
-              !ptx::mbar_wait(bar_acc_empty + 8u * r, acc.phase ^ 1u, p.wait_limit_ns)) {
+          if (!ptx::mbar_wait(bar_full + 8u * s, stage.phase, p.wait_limit_ns) ||
+              (i >= acc_ring &&
+               !ptx::mbar_wait(bar_acc_empty + 8u * r, acc.phase ^ 1u, p.wait_limit_ns))) {
             raise_flag(p.state, 0x2u);
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sc = static_cast<uint32_t>(s * T + t);  // scale slot of the tile
-          const uint32_t sfa_t = tmem + p.tmem.sfa + 4u * sc;
-          const uint32_t sfb_t = tmem + p.tmem.sfb + 4u * sc;
-          ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::desc_rows16(sbase + L.sfa + sc * kSfChunkBytes));
-          ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::desc_rows16(sbase + L.sx + j * kSxChunkBytes));
-          const uint32_t a0 = sbase + L.w + s * kStageWBytes + t * kWTileBytes;
-          const uint32_t b0 = sbase + L.x + s * kStageXBytes + t * kXStageBytes;
+          const uint32_t sfa_t = tmem + p.tmem.sfa + 4u * s;
+          const uint32_t sfb_t = tmem + p.tmem.sfb + 4u * s;
+          ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::desc_rows16(sbase + L.sfa + s * kSfChunkBytes));
+          ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::desc_rows16(sbase + L.sx + i * kSxChunkBytes));
+          const uint32_t a0 = sbase + L.w + s * kWTileBytes;
+          const uint32_t b0 = sbase + L.x + s * kXStageBytes;
           const uint32_t d0 = tmem + p.tmem.acc + p.tmem.acc_slot * static_cast<uint32_t>(r);
-#pragma unroll
+  #pragma unroll
           for (uint32_t kb = 0; kb < kSfPerTile; ++kb) {
-            // One 8-column accumulator per block, or one per tile.
+            // One 8-column accumulator per block, or one per stage.
             const uint32_t d = per_block ? d0 + 8u * kb : d0;
             const uint32_t accumulate = per_block ? 0u : (kb > 0 ? 1u : 0u);
             ptx::mma_mxf8(d, ptx::desc_kmajor_sw128(a0 + 32u * kb),
                           ptx::desc_kmajor_sw128(b0 + 32u * kb), idesc_for_block<F>(kb),
                           accumulate, sfa_t, sfb_t);
           }
-          if (t + 1 == nt) ptx::mma_commit(bar_empty + 8u * s);  // the stage's last tile
+          ptx::mma_commit(bar_empty + 8u * s);
           ptx::mma_commit(bar_acc_full + 8u * r);
-          acc.next(acc_ring);
+          for (int q = 0; q < pipes; ++q) {
+            stage.next(stages);
+            acc.next(acc_ring);
+          }
         }
-        for (int q = 0; q < pipes; ++q) stage.next(stages);
-        for (int q = nt; q < pipes * T; ++q) acc.next(acc_ring);  // the other issuers' tiles
+      } else {
+        // Issuer j takes stages j, j + pipes, ...; a stage's tiles take
+        // consecutive accumulator slots and scale slots (the accumulator ring is
+        // a multiple of T pipes, so every slot keeps one issuer).
+        RingCursor stage{0, 0u}, acc{0, 0u};
+        for (int q = 0; q < issuer; ++q) stage.next(stages);
+        for (int q = 0; q < issuer * T; ++q) acc.next(acc_ring);
+        for (int i = issuer; i < nst && ok; i += pipes) {
+          const int s = stage.slot;
+          if (!ptx::mbar_wait(bar_full + 8u * s, stage.phase, p.wait_limit_ns)) {
+            raise_flag(p.state, 0x2u);
+            ok = false;
+            break;
+          }
+          const int nt = min(T, nkt - i * T);
+  #pragma unroll
+          for (int t = 0; t < T; ++t) {
+            if (t >= nt) break;
+            const int j = i * T + t;  // K tile of the split
+            const int r = acc.slot;
+            if (j >= acc_ring &&
+                !ptx::mbar_wait(bar_acc_empty + 8u * r, acc.phase ^ 1u, p.wait_limit_ns)) {
+              raise_flag(p.state, 0x2u);
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t sc = static_cast<uint32_t>(s * T + t);  // scale slot of the tile
+            const uint32_t sfa_t = tmem + p.tmem.sfa + 4u * sc;
+            const uint32_t sfb_t = tmem + p.tmem.sfb + 4u * sc;
+            ptx::tmem_cp_32x128b_warpx4(sfa_t, ptx::desc_rows16(sbase + L.sfa + sc * kSfChunkBytes));
+            ptx::tmem_cp_32x128b_warpx4(sfb_t, ptx::desc_rows16(sbase + L.sx + j * kSxChunkBytes));
+            const uint32_t a0 = sbase + L.w + s * kStageWBytes + t * kWTileBytes;
+            const uint32_t b0 = sbase + L.x + s * kStageXBytes + t * kXStageBytes;
+            const uint32_t d0 = tmem + p.tmem.acc + p.tmem.acc_slot * static_cast<uint32_t>(r);
+  #pragma unroll
+            for (uint32_t kb = 0; kb < kSfPerTile; ++kb) {
+              // One 8-column accumulator per block, or one per tile.
+              const uint32_t d = per_block ? d0 + 8u * kb : d0;
+              const uint32_t accumulate = per_block ? 0u : (kb > 0 ? 1u : 0u);
+              ptx::mma_mxf8(d, ptx::desc_kmajor_sw128(a0 + 32u * kb),
+                            ptx::desc_kmajor_sw128(b0 + 32u * kb), idesc_for_block<F>(kb),
+                            accumulate, sfa_t, sfb_t);
+            }
+            if (t + 1 == nt) ptx::mma_commit(bar_empty + 8u * s);  // the stage's last tile
+            ptx::mma_commit(bar_acc_full + 8u * r);
+            acc.next(acc_ring);
+          }
+          for (int q = 0; q < pipes; ++q) stage.next(stages);
+          for (int q = nt; q < pipes * T; ++q) acc.next(acc_ring);  // the other issuers' tiles
+        }
       }
     }
   }
