@@ -85,6 +85,10 @@ def parse_args(argv=None):
     p.add_argument("--profile-graph", action="store_true",
                    help="after the timed region, replay the chain's graph once more between "
                         "cudaProfilerStart and cudaProfilerStop (for ncu's graph profiling)")
+    p.add_argument("--cta-k", type=int, default=0, choices=(0, 128, 256),
+                   help="sweep: the tactic's K per pipeline stage (0: the library's choice)")
+    p.add_argument("--sweep-k", type=str, default="",
+                   help="sweep: comma-separated K values to run (default: every K of the sweep)")
     p.add_argument("--path", choices=("chain", "protocols", "sweep"), default="chain",
                    help="chain: the headline (default); protocols: the output hand-off "
                         "protocols on their own (sentinel mailbox, tagged pairs, all-gather); "
@@ -957,8 +961,9 @@ def run_sweep(args):
     stream = torch.cuda.Stream(device=device)
     rows = []
     calls_target = max(GRAPH_STEPS, args.steps)
+    ks = [int(v) for v in args.sweep_k.split(",") if v] or list(synthetic.SWEEP_K)
     for n in synthetic.SWEEP_N:
-        for k in synthetic.SWEEP_K:
+        for k in ks:
             base = synthetic.sweep_workload(8, n, k, 1)
             w, ws = synthetic.make_weights(base)
             W = torch.from_numpy(w).to(device)
@@ -967,7 +972,7 @@ def run_sweep(args):
             copies = min(64, max(3, -(-ROTATION_L2_MULTIPLE * L2_BYTES // weight_bytes)))
             for s in synthetic.SWEEP_S:
                 mb = mx.Mailbox(8, n, device=device)
-                gemms = [mx.PublishGemm(W, WS, mb, split_k=s, stream=stream)
+                gemms = [mx.PublishGemm(W, WS, mb, split_k=s, cta_k=args.cta_k, stream=stream)
                          for _ in range(copies)]
                 cfg = gemms[0].config()
                 out = torch.empty((8, n), dtype=torch.bfloat16, device=device)
@@ -1008,6 +1013,7 @@ def run_sweep(args):
                     rows.append({"m": m, "n": n, "k": k, "split_k": s, "us_per_call": round(us, 3),
                                  "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                                  "stages": cfg["stages"], "fold": cfg["fold"],
+                                 "cta_k": cfg["cta_k"], "pipes": cfg["pipes"],
                                  "grid_ctas": cfg["grid_ctas"], "copies": copies})
                     del graph
                 for g in gemms:
@@ -1025,8 +1031,9 @@ def run_sweep(args):
         "dtype": "e4m3",
         "data": "synthetic (sweep recipe: signed x row pairs, duplicated and zero W rows, "
                 "scale exponents in [-6, 3])",
-        "config": {"workload": "sweep m 1..8 x N {2048, 4096, 7168} x K {2048, 4096, 8192, "
-                               "16384} x S {1, 2, 4}",
+        "config": {"workload": "sweep m 1..8 x N {2048, 4096, 7168} x K "
+                               + "{" + ", ".join(map(str, ks)) + "} x S {1, 2, 4}",
+                   "cta_k": args.cta_k or "library's choice",
                    "timing": "one CUDA graph of >= 30 chained calls per case, rotating "
                              f"min(64, {ROTATION_L2_MULTIPLE} x L2 / weight bytes) weight "
                              "copies (rows give the count)"},
