@@ -180,7 +180,7 @@ size_t mxfp8_mailbox_bytes(int32_t capacity_m, int32_t n);
  * aligned, mxfp8_mailbox_bytes(capacity_m, n) bytes.  stage_state: device,
  * 16-byte aligned int32[4]: [0] next generation (written by the consumer,
  * read by the GEMM), [1] active generation (written by the GEMM, read by the
- * consumer), [2] the consumer's arrival count, [3] error flags.  Launches one
+ * consumer), [2] zero (unused by this protocol), [3] error flags.  Launches one
  * kernel on `stream`. */
 mxfp8_status mxfp8_mailbox_init(void* mailbox, int32_t* stage_state, int32_t capacity_m,
                                 int32_t n, void* stream);
@@ -296,8 +296,9 @@ mxfp8_status mailbox_publish(void* mailbox, int32_t* stage_state, int32_t capaci
  * rank), launched as the previous kernel's programmatic dependent: reads
  * g = stage_state[1]; polls mailbox[g][t][*] for t < m until no 32-bit word
  * is the sentinel; writes out[t][*] (device, 16-byte aligned, [m][n] BF16);
- * stores the sentinel back; the last CTA to arrive sets stage_state[0] =
- * (g + 1) mod 3 and clears stage_state[2].  A poll still unsatisfied after
+ * stores the sentinel back; one CTA sets stage_state[0] = (g + 1) mod 3 (no
+ * CTA of the consumer reads that word; the next publisher reads it after the
+ * consumer has completed).  A poll still unsatisfied after
  * timeout_ns nanoseconds (0 = one second) gives up: it sets
  * MXFP8_FLAG_POLL_TIMEOUT, still copies and resets its slot, and the
  * generation still advances, so the stream drains. */

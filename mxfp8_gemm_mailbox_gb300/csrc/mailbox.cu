@@ -5,11 +5,11 @@
 // cute_dsl.all_gather" (module description, steps 1-3), with one rank: the
 // mailbox holds three generations of 16-byte packs; an empty word is the
 // sentinel 0x80000000; a consumer polls its slots until no word is the
-// sentinel, copies them out and stores the sentinel back, and the last CTA to
-// arrive advances the generation.  The state words are [0] next generation,
-// [1] active generation (page "vllm.models.deepseek_v41.nvidia.
-// specialized_decode.boundary.publishing_gemm", module description), [2]
-// arrival count, [3] error flags.
+// sentinel, copies them out and stores the sentinel back, and the generation
+// advances.  The state words are [0] next generation, [1] active generation
+// (page "vllm.models.deepseek_v41.nvidia.specialized_decode.boundary.
+// publishing_gemm", module description), [2] zero (the all-gather counts its
+// CTAs there; this consumer needs no count), [3] error flags.
 #include <algorithm>
 
 #include "internal.h"
@@ -58,14 +58,14 @@ __global__ void __launch_bounds__(kConsumeThreads)
   ptx::launch_dependents();
   ptx::grid_dependency_wait();
   // The active generation is written only by the publisher, so every thread
-  // reads it; thread 0 of each CTA also counts the CTA in, and the last CTA
-  // to arrive advances the next generation and clears the count.  Each
-  // thread loads its pack from all three generations alongside the state
-  // word (one memory round trip instead of two) and keeps the active one.
-  // No CTA of this grid reads the word the last one advances (state[0] is
-  // read by the next publisher, after this grid completes), so the count
-  // needs atomicity only: a relaxed add, issued with the loads instead of
-  // after them.
+  // reads it, and loads its pack from all three generations alongside it
+  // (one memory round trip instead of two), keeping the active one.  The
+  // all-gather page's CTAs count themselves and the last one advances the
+  // generation, because they read the word it advances; no CTA of this grid
+  // reads the word it advances (state[0] is read by the next publisher, after
+  // this grid completes), so one CTA advances it, with no count: a count
+  // served CTA by CTA on one word measured 0.2 us a call on the N=4096,
+  // K=4096 chain.
   const int packs_per_row = n / 8;
   const int pack = blockIdx.x * kConsumeThreads + threadIdx.x;
   const bool active = pack < m * packs_per_row;
@@ -73,8 +73,6 @@ __global__ void __launch_bounds__(kConsumeThreads)
   const int c8 = active ? pack % packs_per_row : 0;
   const size_t generation_stride = static_cast<size_t>(capacity) * n;
   uint16_t* slot0 = mailbox + static_cast<size_t>(t) * n + c8 * 8;
-  uint32_t before = 0;
-  if (threadIdx.x == 0) before = ptx::atom_add_relaxed(state + 2, 1u);
   const uint32_t g = ptx::ld_volatile_u32(state + 1);
   uint4 candidates[kGenerations];
   if (active) {
@@ -82,14 +80,11 @@ __global__ void __launch_bounds__(kConsumeThreads)
     for (int gg = 0; gg < kGenerations; ++gg)
       candidates[gg] = ptx::ld_volatile_v4(slot0 + gg * generation_stride);
   }
-  if (threadIdx.x == 0) {
-    if (before == gridDim.x - 1) {
-      if (g < static_cast<uint32_t>(kGenerations)) {
-        state[0] = static_cast<int32_t>((g + 1u) % kGenerations);
-      } else {
-        raise_flag(state, kFlagBadState);
-      }
-      state[2] = 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (g < static_cast<uint32_t>(kGenerations)) {
+      state[0] = static_cast<int32_t>((g + 1u) % kGenerations);
+    } else {
+      raise_flag(state, kFlagBadState);
     }
   }
   if (g >= static_cast<uint32_t>(kGenerations) || !active) return;

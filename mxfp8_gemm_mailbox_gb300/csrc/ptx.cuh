@@ -331,13 +331,6 @@ __device__ __forceinline__ void st_v4(void* p, uint4 v) {
                "r"(v.z), "r"(v.w)
                : "memory");
 }
-// Atomicity only: no ordering with this thread's other memory operations.
-__device__ __forceinline__ uint32_t atom_add_relaxed(int32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.add.relaxed.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
-               : "memory");
-  return old;
-}
 __device__ __forceinline__ uint32_t atom_add_acq_rel(int32_t* p, uint32_t v) {
   uint32_t old;
   asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
