@@ -743,7 +743,8 @@ def run_ours(args):
             },
             "roofline": {
                 "bound": "hbm",
-                "kernel": f"publish_gemm_kernel<{wl.split_k}, 0, {cfg['fold']}>",
+                "kernel": f"publish_gemm_kernel<{wl.split_k}, 0, {cfg['fold']}, "
+                          f"{(cfg.get('cta_k') or 128) // 128}>",
                 "achieved": round(achieved, 1),
                 "peak": peak,
                 "peak_kind": peak_kind,
