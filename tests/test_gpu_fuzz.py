@@ -1,13 +1,15 @@
 """Seeded random combinations of shape and tactic -- N, ragged K, m, split-K
 S, ring depth, pipes, accumulation granularity, weight layout, TMEM read-out,
-L2 prefetch (both groups of CTAs), fold, mailbox capacity -- each run
-through GEMM and consumer on integer-valued inputs and checked bit-exactly
-against the oracle: C, the
-published mailbox words between the two kernels, the consumer's output, the
-state words and the reset mailbox.  Combinations the library refuses (a ring
+L2 prefetch (both groups of CTAs), fold, K per pipeline stage (cta_k),
+mailbox capacity -- each run through GEMM and consumer on integer-valued
+inputs and checked bit-exactly against the oracle: C, the published mailbox
+words between the two kernels, the consumer's output, the state words and
+the reset mailbox.  Combinations the library refuses (a ring
 that does not fit, pipes that do not divide it, a fold with S = 8, one slot
-per MMA or the 16x256b read-out, fold 8 with S > 1 or 4 pipes) must be
-refused on the host with MXFP8_ERR_UNSUPPORTED."""
+per MMA or the 16x256b read-out, fold 8 with S > 1 or 4 pipes, cta_k 256
+with fold 8, S = 8, one slot per MMA, the 16x256b read-out or an
+accumulator ring that is not a multiple of 2 x pipes) must be refused on
+the host with MXFP8_ERR_UNSUPPORTED."""
 import numpy as np
 import pytest
 import torch
@@ -36,6 +38,7 @@ def draw(rng):
         capacity=int(rng.integers(m, 9)),
         fold=int(rng.choice([0, 0, 1, 2, 4, 8])),
         l2_prefetch_early=int(rng.choice([-1, 0, 0, 2, 12])),
+        cta_k=int(rng.choice([0, 0, 128, 256])),
     )
 
 
@@ -52,7 +55,7 @@ def test_random_shapes_and_tactics(cuda):
                             acc_blocks=p["acc_blocks"], w_layout=p["w_layout"],
                             l2_prefetch=p["l2_prefetch"], pipes=p["pipes"],
                             tmem_load=p["tmem_load"], fold=p["fold"],
-                            l2_prefetch_early=p["l2_prefetch_early"])
+                            l2_prefetch_early=p["l2_prefetch_early"], cta_k=p["cta_k"])
         except Mxfp8Error as e:
             assert "ERR_UNSUPPORTED" in str(e), (p, str(e))
             refused += 1
