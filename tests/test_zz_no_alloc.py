@@ -32,22 +32,24 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(None)
 
 
-@pytest.mark.parametrize("fold", [1, 0])
-def test_noalloc_matches_the_handle_path_on_two_calls(cuda, fold):
+@pytest.mark.parametrize("fold,cta_k", [(1, 0), (0, 0), (0, 256)])
+def test_noalloc_matches_the_handle_path_on_two_calls(cuda, fold, cta_k):
     # Two calls in a row, each with its own weight scales: the second call's
     # re-layout overwrites the scratch the first call's GEMM read, and its
     # GEMM must see the new chunks.  Both paths run the same kernel with the
     # same tactic and summation order, so they agree bit for bit.
     lib = _lib.load()
     n, k, m, split = 1024, 4096, 5, 2
-    desc = _lib.GemmDesc(n, k, 8, split, 0, 0, 0, 0, 0, 0, 0, fold)
+    desc = _lib.GemmDesc(n, k, 8, split, cta_k, 0, 0, 0, 0, 0, 0, fold)
     handle_mb, noalloc_mb = Mailbox(8, n), Mailbox(8, n)
     for call in range(2):
         wl = synthetic.Workload("noalloc", n, k, m, split, exp_lo=-4, exp_hi=2, seed=4242 + call)
         w, ws = synthetic.make_weights(wl)
         W, WS = dev(w), dev(ws)
-        gemm = PublishGemm(W, WS, handle_mb, split_k=split, w_layout=_lib.W_IN_PLACE, fold=fold)
+        gemm = PublishGemm(W, WS, handle_mb, split_k=split, w_layout=_lib.W_IN_PLACE, fold=fold,
+                           cta_k=cta_k)
         assert gemm.config()["fold"] == (fold or 4)  # 8 tiles x 2 splits fold 4 ways by default
+        assert gemm.config()["cta_k"] == (cta_k or 128)
         x, xs = synthetic.make_activations(wl, salt=call)
         X, XS = dev(x), dev(xs)
         c_handle = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
