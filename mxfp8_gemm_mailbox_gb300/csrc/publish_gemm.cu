@@ -87,7 +87,8 @@ GemmSmemLayout gemm_smem_layout(int stages, int split_k, int tiles_per_split, in
   if (dedicated_recv && split_k > 1) {
     // The partials' own region ((S-1) x 128 x 8/S pairs of 8 bytes, at most
     // 7 KB), so a peer can send them as soon as its own main loop is done.
-    L.recv = L.misc + 16u;
+    // 16-byte stores land there: keep it 16-byte aligned whatever precedes it.
+    L.recv = (L.misc + 16u + 15u) & ~15u;
     L.recv_dedicated = 1;
     L.total = L.recv + static_cast<uint32_t>((split_k - 1) * kBlockN * (kRows / split_k) * 8) +
               1024u;
